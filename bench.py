@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark of the flux-differencing volume term on GB300.
+
+One step = one evaluation of the volume term (esdg_volume_rhs) over the whole
+mesh of the workload.  Default workload: the baroclinic-channel-shaped mesh,
+64x16x8 warped elements of order N = 7 (4,194,304 nodes), FP64; the FP32
+kernel on the same mesh is timed in the same run and reported under "fp32".
+The inputs (503 MB in FP64, 252 MB in FP32) are larger than the 129 MB L2, so
+no flush is needed between steps.
+
+Metric: volume-term GDOF/s = nodes / (kernel time per step), whole job.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank evaluates its own copy of the workload
+(elements are independent, so ranks need no exchange: weak scaling); rank 0
+prints one JSON line with the total over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+# ---------------------------------------------------------------------------
+# algorithmic operation counts (per unit of work), counted from the formulas
+# of the volume term with every +, -, *, / as one operation and a logarithm as
+# one operation (fused multiply-adds count two):
+#   per unordered node pair and direction, both nodes' contributions:
+#     averaged metric 3, averaged velocity 3, {{u}}.n 5, log mean of rho 3,
+#     inverse log mean of b 3, {{rho}} and {{b}} 2, p_hat 2, {{phi}} and [[phi]] 2,
+#     {{|u|^2}} 1, |{{u}}|^2 5, rho_hat 2, gravity scalar 2 and partner scaling 2,
+#     F_rho 1, momentum 9, gravity vectors 6, F_E 7, accumulation into both
+#     nodes 26                                               -> 84
+#   per node: u 4, |u|^2 5, p 6, b and 1/b 3, two logarithms 2, h 3,
+#     1/w scaling of three directions 15                     -> 38
+#   per end node of a line (2D form diagonal): 20, on 2 of the Nq nodes of
+#     each line in each of the 3 directions
+# Pairs per node: 3 (Nq - 1) / 2 (each unordered pair once, Sec. 4.1).
+PAIR_OPS = 84
+NODE_OPS = 38
+DIAG_OPS = 20
+
+
+def flops_per_dof(N: int, form2d: bool = True) -> float:
+    Nq = N + 1
+    f = PAIR_OPS * 3.0 * (Nq - 1) / 2.0 + NODE_OPS
+    if form2d:
+        f += DIAG_OPS * 3.0 * 2.0 / Nq
+    return f
+
+
+BYTES_PER_DOF = {"fp64": 20 * 8, "fp32": 20 * 4}  # 15 planes read + 5 written
+
+NOMINAL_FP64_TFLOPS = 1.25  # GB300 FP64 vector, nominal
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.dev)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        # samples "under load": the upper half by power draw
+        if pw:
+            cut = sorted(pw)[len(pw) // 2]
+            loaded = [num(r[1]) for r in rows if num(r[3]) is not None and num(r[3]) >= cut and num(r[1])]
+        else:
+            loaded = sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _setup(cfg, device):
+    import torch
+
+    import flux_differencing_gb300 as fd
+    import workloads as wl
+
+    g = wl.generate(cfg, device=device)
+    op = fd.VolumeOperator(cfg.Kx, cfg.Ky, cfg.Kz, cfg.N, cfg.precision)
+    Ja = op.set_geometry(g["x"], g["y"], g["z"])
+    q = g["q"].to(op.dtype).contiguous()
+    phi = g["phi"].to(op.dtype).contiguous()
+    del g
+    out = torch.empty((5, cfg.n), dtype=op.dtype, device=device)
+    torch.cuda.synchronize(device)
+    return op, q, Ja, phi, out
+
+
+def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier):
+    """Per-launch times of the volume kernel with CUDA events on its stream."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            op.volume_rhs(q, Ja, phi, out=out, stream=stream)
+        torch.cuda.synchronize()
+        barrier()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for k in range(steps):
+            op.volume_rhs(q, Ja, phi, out=out, stream=stream)
+            ev[k + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+    total = ev[0].elapsed_time(ev[steps])
+    return total, per
+
+
+def _time_e2e(op, q, Ja, phi, out, steps, warmup, stream, barrier):
+    """Same metric through host buffers: pinned H2D of q, metrics, phi, the kernel, D2H of out."""
+    import torch
+
+    hq = q.cpu().pin_memory()
+    hJ = Ja.cpu().pin_memory()
+    hp = phi.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = (hq.numel() + hJ.numel() + hp.numel()) * hq.element_size()
+    d2h = ho.numel() * ho.element_size()
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        Ja.copy_(hJ, non_blocking=True)
+        phi.copy_(hp, non_blocking=True)
+        op.volume_rhs(q, Ja, phi, out=out, stream=stream)
+        ho.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    return e0.elapsed_time(e1), h2d, d2h
+
+
+def _fma_peak(fp64: bool, device) -> float:
+    """Best-of-3 FMA throughput (FLOP/s) of the bench kernel over all SMs."""
+    import ctypes
+
+    import torch
+
+    import flux_differencing_gb300 as fd
+    lib = fd.load_library()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    blocks, threads = sms * 8, 256
+    iters = 4096 if fp64 else 65536
+    dt = torch.float64 if fp64 else torch.float32
+    sink = torch.zeros(blocks, dtype=dt, device=device)
+    s = torch.cuda.current_stream(device)
+    best = 0.0
+    for _ in range(4):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        rc = lib.esdg_bench_fma(1 if fp64 else 0, blocks, threads, iters, ctypes.c_void_p(sink.data_ptr()),
+                                ctypes.c_void_p(s.cuda_stream))
+        e1.record(s)
+        torch.cuda.synchronize(device)
+        if rc != 0:
+            return float("nan")
+        ms = e0.elapsed_time(e1)
+        best = max(best, 16.0 * iters * blocks * threads / (ms * 1e-3))
+    return best
+
+
+def _cpu_baseline(cfg, budget_s: float = 12.0):
+    """The oracle as it stands on this host's cores, on a bounded sample of elements."""
+    import oracle
+    import workloads as wl
+
+    oracle.build()
+    nthreads = oracle.max_threads()
+    # pilot on a few elements to size the sample
+    pilot = np.arange(min(cfg.K, max(8, nthreads)))
+    g = wl.generate_elements(cfg, pilot)
+    gc = {k: v.numpy() for k, v in g.items()}
+    Ja, _ = oracle.metrics(cfg.N, len(pilot), gc["x"], gc["y"], gc["z"])
+    t0 = time.perf_counter()
+    oracle.volume(cfg.N, len(pilot), gc["q"], Ja, gc["phi"], nthreads=nthreads)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    count = int(min(cfg.K, max(len(pilot), len(pilot) * budget_s / dt)))
+    elems = np.arange(count)
+    g = wl.generate_elements(cfg, elems)
+    gc = {k: v.numpy() for k, v in g.items()}
+    Ja, _ = oracle.metrics(cfg.N, count, gc["x"], gc["y"], gc["z"])
+    t0 = time.perf_counter()
+    oracle.volume(cfg.N, count, gc["q"], Ja, gc["phi"], nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    nodes = count * cfg.Nq ** 3
+    return {"value": nodes / dt / 1e9, "unit": "GDOF/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"first {count} of {cfg.K} elements of {cfg.name} ({nodes} nodes), FP64 oracle, "
+                      f"{dt:.1f} s, OpenMP over elements"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle timed on the host cores on the same workload."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    import workloads as wl
+
+    cfg = wl.get_config(args.workload)
+    oracle.build()
+    nthreads = oracle.max_threads()
+    per_step = max(1, min(cfg.K, args.ref_elements))
+    elems = np.arange(per_step)
+    g = wl.generate_elements(cfg, elems)
+    gc = {k: v.numpy() for k, v in g.items()}
+    Ja, _ = oracle.metrics(cfg.N, per_step, gc["x"], gc["y"], gc["z"])
+    for _ in range(args.warmup):
+        oracle.volume(cfg.N, per_step, gc["q"], Ja, gc["phi"], nthreads=nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.volume(cfg.N, per_step, gc["q"], Ja, gc["phi"], nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    nodes = per_step * cfg.Nq ** 3
+    val = nodes * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": "volume-term GDOF/s (FP64)", "value": val, "unit": "GDOF/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "N": cfg.N, "K": cfg.K, "nodes": cfg.n,
+                   "sample_elements_per_step": per_step},
+        "cpu_baseline": {"value": val, "unit": "GDOF/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"first {per_step} elements of {cfg.name} per step"},
+        "e2e": {"value": val, "unit": "GDOF/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import workloads as wl
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    stream = torch.cuda.Stream(device)
+    results = {}
+    clocks = None
+    for wname in [args.workload] + ([args.fp32_workload] if args.fp32_workload else []):
+        cfg = wl.get_config(wname)
+        op, q, Ja, phi, out = _setup(cfg, device)
+        sampler = ClockSampler(local) if (rank == 0 and wname == args.workload) else None
+        if sampler:
+            sampler.start()
+        total_ms, per = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier)
+        if sampler:
+            clocks = sampler.stop()
+        assert op.status() == 0, "non-physical state in the bench inputs"
+        total_ms = max_over_ranks(total_ms)
+        ms = total_ms / args.steps
+        gdof = ws * cfg.n / (ms * 1e-3) / 1e9
+        fl = flops_per_dof(cfg.N) * cfg.n
+        res = {"cfg": cfg, "ms": ms, "gdof": gdof, "per": per,
+               "flops_per_launch": fl, "achieved_tflops": fl / (statistics.mean(per) * 1e-3) / 1e12,
+               "bytes_per_launch": BYTES_PER_DOF[cfg.precision] * cfg.n}
+        if not args.no_e2e:
+            e2e_steps = max(3, min(args.steps, 20))
+            e_ms, h2d, d2h = _time_e2e(op, q, Ja, phi, out, e2e_steps, 1, stream, barrier)
+            e_ms = max_over_ranks(e_ms) / e2e_steps
+            res["e2e"] = {"value": ws * cfg.n / (e_ms * 1e-3) / 1e9, "unit": "GDOF/s",
+                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+        results[wname] = res
+        op.close()
+        del q, Ja, phi, out
+        torch.cuda.empty_cache()
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = _peaks()
+    fp64_meas = _fma_peak(True, device) / 1e12
+    fp32_meas = _fma_peak(False, device) / 1e12
+    main = results[args.workload]
+    cfg = main["cfg"]
+    peak64 = max(NOMINAL_FP64_TFLOPS, fp64_meas) if fp64_meas == fp64_meas else NOMINAL_FP64_TFLOPS
+    roof = {"bound": "alu", "achieved": main["achieved_tflops"], "peak": peak64, "unit": "TFLOP/s",
+            "frac": main["achieved_tflops"] / peak64, "traffic": None,
+            "peak_source": f"FP64 vector FMA: max(nominal {NOMINAL_FP64_TFLOPS}, measured {fp64_meas:.3f}) TFLOP/s",
+            "algorithmic_flops_per_dof": flops_per_dof(cfg.N),
+            "hbm": {"achieved_gbs": main["bytes_per_launch"] / (statistics.mean(main["per"]) * 1e-3) / 1e9,
+                    "peak_gbs": peaks.get("hbm_gbs"), "peak_source": peak_src}}
+    line = {
+        "metric": "volume-term GDOF/s (FP64)", "value": main["gdof"], "unit": "GDOF/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "N": cfg.N, "K": cfg.K, "elements": [cfg.Kx, cfg.Ky, cfg.Kz],
+                   "nodes": cfg.n, "precision": cfg.precision, "form": "2d",
+                   "l2": f"inputs {15 * cfg.n * 8 / 1e6:.0f} MB > 129 MB L2, no flush",
+                   "parallelism": f"elements, {ws} rank(s), no exchange"},
+        "roofline": roof,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if "e2e" in main:
+        line["e2e"] = {k: v for k, v in main["e2e"].items() if k != "ms_per_step"}
+        line["gpu_launches"] += max(3, min(args.steps, 20))
+    if args.fp32_workload:
+        r32 = results[args.fp32_workload]
+        c32 = r32["cfg"]
+        hbm32 = r32["bytes_per_launch"] / (statistics.mean(r32["per"]) * 1e-3) / 1e9
+        line["fp32"] = {
+            "workload": c32.name, "value": r32["gdof"], "unit": "GDOF/s", "ms_per_step": r32["ms"],
+            "roofline": {"bound": "alu", "achieved": r32["achieved_tflops"], "peak": fp32_meas,
+                         "unit": "TFLOP/s", "frac": r32["achieved_tflops"] / fp32_meas,
+                         "peak_source": "measured FP32 vector FMA",
+                         "hbm": {"achieved_gbs": hbm32, "peak_gbs": peaks.get("hbm_gbs"),
+                                 "frac": hbm32 / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None}},
+        }
+        if "e2e" in r32:
+            line["fp32"]["e2e"] = {k: v for k, v in r32["e2e"].items() if k != "ms_per_step"}
+        line["gpu_launches"] += args.steps + (max(3, min(args.steps, 20)) if "e2e" in r32 else 0)
+    line["peaks_measured"] = {"fp64_tflops": fp64_meas, "fp32_tflops": fp32_meas}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(cfg, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="channel_N7")
+    ap.add_argument("--fp32-workload", default="channel_N7_fp32")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-elements", type=int, default=256)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.fp32_workload in ("", "none"):
+        args.fp32_workload = None
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

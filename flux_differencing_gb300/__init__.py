@@ -1,0 +1,209 @@
+"""GB300 flux-differencing volume term: Python binding of libesdg.so.
+
+The binding only marshals arguments: every step of the volume term runs in
+the library's CUDA kernels (see include/esdg.h for the C-ABI).  PyTorch
+provides device memory and streams.  If the compiled library is missing the
+import of this package still works, but every call raises: there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+__all__ = [
+    "ESDG_OK", "ESDG_FP64", "ESDG_FP32", "ESDG_FORM_2D", "ESDG_FORM_SKEW", "ESDG_STATUS_NONPHYSICAL",
+    "EsdgError", "library_path", "load_library", "operators", "pair_schedule", "VolumeOperator",
+]
+
+ESDG_OK = 0
+ESDG_ERR_ARG, ESDG_ERR_UNSUPPORTED, ESDG_ERR_ALIGN, ESDG_ERR_CUDA, ESDG_ERR_STATE = 1, 2, 3, 4, 5
+ESDG_FP64, ESDG_FP32 = 0, 1
+ESDG_FORM_2D, ESDG_FORM_SKEW = 0, 1
+ESDG_STATUS_NONPHYSICAL = 1
+
+_ERRNAMES = {1: "ESDG_ERR_ARG", 2: "ESDG_ERR_UNSUPPORTED", 3: "ESDG_ERR_ALIGN", 4: "ESDG_ERR_CUDA",
+             5: "ESDG_ERR_STATE"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+_lock = threading.Lock()
+
+# every symbol include/esdg.h declares, with its ctypes signature
+_P = ctypes.c_void_p
+_SIGS = {
+    "esdg_create": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "esdg_destroy": (ctypes.c_int, [_P]),
+    "esdg_set_params": (ctypes.c_int, [_P, ctypes.c_double]),
+    "esdg_set_geometry": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
+    "esdg_volume_rhs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
+    "esdg_volume_rhs_range": (ctypes.c_int, [_P, ctypes.c_long, ctypes.c_long, _P, _P, _P, _P, _P]),
+    "esdg_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint), _P]),
+    "esdg_last_error": (ctypes.c_char_p, [_P]),
+    "esdg_get_operators": (ctypes.c_int, [ctypes.c_int, _P, _P, _P]),
+    "esdg_pair_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int), _P, _P]),
+    "esdg_version": (ctypes.c_int, []),
+    # measurement kernels, include/esdg_bench.h
+    "esdg_bench_fma": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int, _P, _P]),
+}
+
+
+class EsdgError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{_ERRNAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "_build", "libesdg.so")
+
+
+def load_library(build_if_missing: bool = False):
+    """Load libesdg.so.  Raises if it is missing (no CPU fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            if build_if_missing:
+                from . import build as _build
+                _build.build()
+            else:
+                raise RuntimeError(
+                    f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+                    "or `python flux_differencing_gb300/build.py`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, h=None):
+    if rc != ESDG_OK:
+        lib = load_library()
+        msg = lib.esdg_last_error(h).decode()
+        raise EsdgError(rc, msg)
+
+
+def operators(N: int):
+    """LGL nodes, weights and D exactly as the kernels use them (host call)."""
+    lib = load_library()
+    x = np.zeros(N + 1)
+    w = np.zeros(N + 1)
+    D = np.zeros((N + 1, N + 1))
+    _check(lib.esdg_get_operators(N, x.ctypes.data, w.ctypes.data, D.ctypes.data))
+    return x, w, D
+
+
+def pair_schedule(N: int):
+    """(H, partner[p, d-1], sides[p, d-1]) of the kernel's per-line pair schedule."""
+    lib = load_library()
+    H = ctypes.c_int(0)
+    partner = np.zeros((N + 1) * ((N + 1) // 2), dtype=np.int32)
+    sides = np.zeros_like(partner)
+    _check(lib.esdg_pair_schedule(N, ctypes.byref(H), partner.ctypes.data, sides.ctypes.data))
+    return H.value, partner.reshape(N + 1, -1), sides.reshape(N + 1, -1)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class VolumeOperator:
+    """A handle for one mesh shape, order and precision.
+
+    precision: "fp64" or "fp32"; form: "2d" (diagonal kept) or "skew".
+    Tensors passed in must be contiguous CUDA tensors of the handle's dtype
+    (node coordinates are always float64), laid out as described in esdg.h.
+    """
+
+    def __init__(self, Kx: int, Ky: int, Kz: int, N: int, precision: str = "fp64", form: str = "2d",
+                 gamma: float = 1.4):
+        import torch
+        self.lib = load_library()
+        self.Kx, self.Ky, self.Kz, self.N = int(Kx), int(Ky), int(Kz), int(N)
+        self.K = self.Kx * self.Ky * self.Kz
+        self.n = self.K * (self.N + 1) ** 3
+        self.precision = precision
+        self.dtype = {"fp64": torch.float64, "fp32": torch.float32}[precision]
+        prec = ESDG_FP64 if precision == "fp64" else ESDG_FP32
+        frm = {"2d": ESDG_FORM_2D, "skew": ESDG_FORM_SKEW}[form]
+        h = ctypes.c_void_p()
+        _check(self.lib.esdg_create(ctypes.byref(h), self.Kx, self.Ky, self.Kz, self.N, prec, frm))
+        self.h = h
+        if gamma != 1.4:
+            _check(self.lib.esdg_set_params(self.h, float(gamma)), self.h)
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.esdg_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _req(self, t, numel, dtype=None, name="tensor"):
+        dt = dtype or self.dtype
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous() or t.numel() != numel:
+            raise ValueError(f"{name}: need a contiguous CUDA {dt} tensor with {numel} elements, got "
+                             f"{t.dtype} {tuple(t.shape)} on {t.device}")
+
+    def set_geometry(self, x, y, z, metrics_out=None, J_out=None, stream=None):
+        """Curl-form metric terms (9, n) (and J (n,) if J_out is given) from node coordinates."""
+        import torch
+        for t, nm in ((x, "x"), (y, "y"), (z, "z")):
+            self._req(t, self.n, torch.float64, nm)
+        if metrics_out is None:
+            metrics_out = torch.empty((9, self.n), dtype=self.dtype, device=x.device)
+        self._req(metrics_out, 9 * self.n, name="metrics_out")
+        if J_out is not None:
+            self._req(J_out, self.n, name="J_out")
+        _check(self.lib.esdg_set_geometry(self.h, _dptr(x), _dptr(y), _dptr(z), _dptr(metrics_out),
+                                          _dptr(J_out) if J_out is not None else None, _stream_ptr(stream)),
+               self.h)
+        return metrics_out
+
+    def volume_rhs(self, q, metrics, phi, out=None, stream=None, e_begin: int | None = None,
+                   e_count: int | None = None):
+        """Volume term (5, n); optionally only elements [e_begin, e_begin + e_count)."""
+        import torch
+        self._req(q, 5 * self.n, name="q")
+        self._req(metrics, 9 * self.n, name="metrics")
+        self._req(phi, self.n, name="phi")
+        if out is None:
+            out = torch.empty((5, self.n), dtype=self.dtype, device=q.device)
+        self._req(out, 5 * self.n, name="out")
+        sp = _stream_ptr(stream)
+        if e_begin is None and e_count is None:
+            rc = self.lib.esdg_volume_rhs(self.h, _dptr(q), _dptr(metrics), _dptr(phi), _dptr(out), sp)
+        else:
+            eb = 0 if e_begin is None else int(e_begin)
+            ec = self.K - eb if e_count is None else int(e_count)
+            rc = self.lib.esdg_volume_rhs_range(self.h, eb, ec, _dptr(q), _dptr(metrics), _dptr(phi),
+                                                _dptr(out), sp)
+        _check(rc, self.h)
+        return out
+
+    def status(self, stream=None) -> int:
+        """Read and clear the status word (synchronises the stream)."""
+        v = ctypes.c_uint(0)
+        _check(self.lib.esdg_get_status(self.h, ctypes.byref(v), _stream_ptr(stream)), self.h)
+        return v.value

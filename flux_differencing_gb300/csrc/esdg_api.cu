@@ -1,0 +1,333 @@
+// Host side of the C-ABI declared in include/esdg.h: handles, argument
+// checks, operator tables and kernel dispatch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "esdg.h"
+#include "esdg_internal.h"
+
+struct esdg_ctx {
+    long long Kx = 0, Ky = 0, Kz = 0, K = 0, n = 0;
+    int N = 0, Nq = 0, precision = 0, form = 0;
+    double gamma = 1.4;
+    int device = 0;
+    unsigned* d_status = nullptr;
+    double nodes[esdg::kMaxNq];
+    double weights[esdg::kMaxNq];
+    double D[esdg::kMaxNq * esdg::kMaxNq];
+    esdg::OpTables<double> op64;
+    esdg::OpTables<float> op32;
+    std::string err;
+};
+
+namespace {
+
+thread_local std::string g_create_error;
+
+int fail(esdg_handle h, int code, const std::string& msg) {
+    if (h) h->err = msg;
+    else g_create_error = msg;
+    return code;
+}
+
+int cuda_fail(esdg_handle h, cudaError_t e, const char* what) {
+    return fail(h, ESDG_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+// Legendre P_N and its derivative by the paired recurrences
+//   (k+1) P_{k+1} = (2k+1) x P_k - k P_{k-1},   P'_{k+1} = P'_{k-1} + (2k+1) P_k.
+void legendre(int N, long double x, long double& P, long double& dP) {
+    long double p0 = 1, p1 = x, d0 = 0, d1 = 1;
+    if (N == 0) { P = 1; dP = 0; return; }
+    for (int k = 1; k < N; ++k) {
+        long double p2 = ((2 * k + 1) * x * p1 - k * p0) / (k + 1);
+        long double d2 = d0 + (2 * k + 1) * p1;
+        p0 = p1; p1 = p2; d0 = d1; d1 = d2;
+    }
+    P = p1;
+    dP = d1;
+}
+
+}  // namespace
+
+namespace esdg {
+
+// LGL nodes: +-1 and the roots of P_N', found by Newton's method on P_N' with
+// P_N'' from Legendre's equation (1 - x^2) P'' = 2 x P' - N (N+1) P.
+// Weights 2 / (N (N+1) P_N(x)^2).  D from barycentric weights
+// lambda_j = 1 / prod_{k != j} (x_j - x_k):  D_ij = (lambda_j / lambda_i) / (x_i - x_j),
+// D_ii = -sum_{j != i} D_ij (rows of D annihilate constants).
+void lgl_operators(int N, double* nodes, double* weights, double* D) {
+    const int Nq = N + 1;
+    long double x[kMaxNq], w[kMaxNq], lam[kMaxNq];
+    const long double pi = 3.141592653589793238462643383279502884L;
+    for (int j = 0; j < Nq; ++j) {
+        long double xj = -cosl(pi * j / N);
+        if (j == 0) xj = -1;
+        if (j == N) xj = 1;
+        if (j > 0 && j < N) {
+            for (int it = 0; it < 60; ++it) {
+                long double P, dP;
+                legendre(N, xj, P, dP);
+                const long double d2P = (2 * xj * dP - (long double)N * (N + 1) * P) / (1 - xj * xj);
+                const long double step = dP / d2P;
+                xj -= step;
+                if (fabsl(step) < 1e-21L) break;
+            }
+        }
+        long double P, dP;
+        legendre(N, xj, P, dP);
+        x[j] = xj;
+        w[j] = 2.0L / ((long double)N * (N + 1) * P * P);
+    }
+    for (int j = 0; j < Nq; ++j) {
+        long double prod = 1;
+        for (int k = 0; k < Nq; ++k)
+            if (k != j) prod *= (x[j] - x[k]);
+        lam[j] = 1 / prod;
+    }
+    for (int i = 0; i < Nq; ++i) {
+        long double diag = 0;
+        for (int j = 0; j < Nq; ++j) {
+            if (j == i) continue;
+            const long double dij = (lam[j] / lam[i]) / (x[i] - x[j]);
+            D[i * Nq + j] = (double)dij;
+            diag -= dij;
+        }
+        D[i * Nq + i] = (double)diag;
+        nodes[i] = (double)x[i];
+        weights[i] = (double)w[i];
+    }
+}
+
+}  // namespace esdg
+
+namespace {
+
+template <typename T>
+void fill_tables(esdg::OpTables<T>& t, int N, const double* w, const double* D) {
+    const int Nq = N + 1;
+    std::memset(&t, 0, sizeof(t));
+    for (int i = 0; i < Nq; ++i) {
+        t.invw[i] = (T)(1.0L / (long double)w[i]);
+        for (int j = 0; j < Nq; ++j) t.Q2[i * Nq + j] = (T)(2.0L * (long double)w[i] * (long double)D[i * Nq + j]);
+    }
+}
+
+template <typename T>
+esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja, const void* phi, void* out,
+                                long long e0, long long e1, const esdg::OpTables<T>& ops) {
+    esdg::VolumeArgs<T> a;
+    a.q = static_cast<const T*>(q);
+    a.Ja = static_cast<const T*>(Ja);
+    a.phi = static_cast<const T*>(phi);
+    a.out = static_cast<T*>(out);
+    a.n = h->n;
+    a.e_begin = e0;
+    a.e_end = e1;
+    a.gm1 = (T)(h->gamma - 1.0);
+    a.c_g = (T)(1.0 / (2.0 * (h->gamma - 1.0)));
+    a.c_h = (T)(h->gamma / (2.0 * (h->gamma - 1.0)));
+    a.form = h->form;
+    a.status = h->d_status;
+    a.ops = ops;
+    return a;
+}
+
+cudaError_t dispatch_fp64(int N, const esdg::VolumeArgs<double>& a, cudaStream_t s) {
+    switch (N) {
+        case 1: return esdg::launch_volume_fp64_n1(a, s);
+        case 2: return esdg::launch_volume_fp64_n2(a, s);
+        case 3: return esdg::launch_volume_fp64_n3(a, s);
+        case 4: return esdg::launch_volume_fp64_n4(a, s);
+        case 5: return esdg::launch_volume_fp64_n5(a, s);
+        case 6: return esdg::launch_volume_fp64_n6(a, s);
+        case 7: return esdg::launch_volume_fp64_n7(a, s);
+        case 8: return esdg::launch_volume_fp64_n8(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t dispatch_fp32(int N, const esdg::VolumeArgs<float>& a, cudaStream_t s) {
+    switch (N) {
+        case 1: return esdg::launch_volume_fp32_n1(a, s);
+        case 2: return esdg::launch_volume_fp32_n2(a, s);
+        case 3: return esdg::launch_volume_fp32_n3(a, s);
+        case 4: return esdg::launch_volume_fp32_n4(a, s);
+        case 5: return esdg::launch_volume_fp32_n5(a, s);
+        case 6: return esdg::launch_volume_fp32_n6(a, s);
+        case 7: return esdg::launch_volume_fp32_n7(a, s);
+        case 8: return esdg::launch_volume_fp32_n8(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+int check_device(esdg_handle h) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaGetDevice");
+    if (dev != h->device)
+        return fail(h, ESDG_ERR_STATE, "handle was created on device " + std::to_string(h->device) +
+                                           " but device " + std::to_string(dev) + " is current");
+    return ESDG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int esdg_version(void) { return 100; }
+
+int esdg_get_operators(int N, double* nodes, double* weights, double* D) {
+    if (N < 1 || N > esdg::kMaxN) return fail(nullptr, ESDG_ERR_UNSUPPORTED, "N must be in 1..8");
+    if (!nodes || !weights || !D) return fail(nullptr, ESDG_ERR_ARG, "null output pointer");
+    esdg::lgl_operators(N, nodes, weights, D);
+    return ESDG_OK;
+}
+
+int esdg_pair_schedule(int N, int* H_out, int* partner, int* sides) {
+    if (N < 1 || N > esdg::kMaxN) return fail(nullptr, ESDG_ERR_UNSUPPORTED, "N must be in 1..8");
+    if (!H_out || !partner || !sides) return fail(nullptr, ESDG_ERR_ARG, "null output pointer");
+    // Must match direction_phase in volume_kernel.cuh: offsets d = 1..Nq/2,
+    // both sides unless Nq is even and d == Nq/2.
+    const int Nq = N + 1, H = Nq / 2;
+    *H_out = H;
+    for (int p = 0; p < Nq; ++p)
+        for (int d = 1; d <= H; ++d) {
+            partner[p * H + d - 1] = (p + d) % Nq;
+            sides[p * H + d - 1] = (Nq % 2 == 0 && d == H) ? 1 : 2;
+        }
+    return ESDG_OK;
+}
+
+const char* esdg_last_error(esdg_handle h) {
+    if (h) return h->err.c_str();
+    return g_create_error.c_str();
+}
+
+int esdg_create(esdg_handle* out, long Kx, long Ky, long Kz, int N, int precision, int form) {
+    if (!out) return fail(nullptr, ESDG_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    if (N < 1 || N > esdg::kMaxN) return fail(nullptr, ESDG_ERR_UNSUPPORTED, "N must be in 1..8");
+    if (precision != ESDG_FP64 && precision != ESDG_FP32)
+        return fail(nullptr, ESDG_ERR_UNSUPPORTED, "precision must be ESDG_FP64 or ESDG_FP32");
+    if (form != ESDG_FORM_2D && form != ESDG_FORM_SKEW)
+        return fail(nullptr, ESDG_ERR_UNSUPPORTED, "form must be ESDG_FORM_2D or ESDG_FORM_SKEW");
+    if (Kx < 1 || Ky < 1 || Kz < 1) return fail(nullptr, ESDG_ERR_ARG, "element counts must be >= 1");
+    const long double Kld = (long double)Kx * Ky * Kz * (N + 1) * (N + 1) * (N + 1);
+    if (Kld > (long double)(1LL << 40)) return fail(nullptr, ESDG_ERR_ARG, "mesh too large");
+
+    esdg_ctx* h = new esdg_ctx();
+    h->Kx = Kx; h->Ky = Ky; h->Kz = Kz;
+    h->K = (long long)Kx * Ky * Kz;
+    h->N = N;
+    h->Nq = N + 1;
+    h->n = h->K * h->Nq * h->Nq * h->Nq;
+    h->precision = precision;
+    h->form = form;
+    esdg::lgl_operators(N, h->nodes, h->weights, h->D);
+    fill_tables(h->op64, N, h->weights, h->D);
+    fill_tables(h->op32, N, h->weights, h->D);
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(unsigned));
+    if (e != cudaSuccess) {
+        std::string msg = std::string("device status word: ") + cudaGetErrorString(e);
+        if (h->d_status) cudaFree(h->d_status);
+        delete h;
+        return fail(nullptr, ESDG_ERR_CUDA, msg);
+    }
+    *out = h;
+    return ESDG_OK;
+}
+
+int esdg_destroy(esdg_handle h) {
+    if (!h) return ESDG_OK;
+    if (h->d_status) cudaFree(h->d_status);
+    delete h;
+    return ESDG_OK;
+}
+
+int esdg_set_params(esdg_handle h, double gamma) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (!(gamma > 1.0 && gamma < 10.0)) return fail(h, ESDG_ERR_ARG, "gamma must be in (1, 10)");
+    h->gamma = gamma;
+    return ESDG_OK;
+}
+
+int esdg_set_geometry(esdg_handle h, const double* x, const double* y, const double* z, void* metrics_out,
+                      void* J_out, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (!x || !y || !z || !metrics_out) return fail(h, ESDG_ERR_ARG, "null coordinate or metrics pointer");
+    if (!aligned16(x) || !aligned16(y) || !aligned16(z) || !aligned16(metrics_out) || (J_out && !aligned16(J_out)))
+        return fail(h, ESDG_ERR_ALIGN, "device pointers must be 16-byte aligned");
+    if (int rc = check_device(h)) return rc;
+    esdg::GeometryArgs g;
+    std::memset(&g, 0, sizeof(g));
+    g.x = x; g.y = y; g.z = z;
+    g.Ja = metrics_out;
+    g.J = J_out;
+    g.K = h->K;
+    g.N = h->N;
+    g.fp32 = h->precision == ESDG_FP32;
+    std::memcpy(g.D, h->D, sizeof(double) * h->Nq * h->Nq);
+    cudaError_t e = esdg::launch_geometry(g, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "geometry kernel launch");
+    return ESDG_OK;
+}
+
+int esdg_volume_rhs_range(esdg_handle h, long e_begin, long e_count, const void* q, const void* metrics,
+                          const void* phi, void* out, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (!q || !metrics || !phi || !out) return fail(h, ESDG_ERR_ARG, "null device pointer");
+    if (e_begin < 0 || e_count < 1 || e_begin + e_count > h->K)
+        return fail(h, ESDG_ERR_ARG, "element range outside 0..K");
+    if (!aligned16(q) || !aligned16(metrics) || !aligned16(phi) || !aligned16(out))
+        return fail(h, ESDG_ERR_ALIGN, "device pointers must be 16-byte aligned");
+    const size_t es = h->precision == ESDG_FP64 ? sizeof(double) : sizeof(float);
+    const size_t nb = es * (size_t)h->n;
+    if (overlaps(out, 5 * nb, q, 5 * nb) || overlaps(out, 5 * nb, metrics, 9 * nb) || overlaps(out, 5 * nb, phi, nb))
+        return fail(h, ESDG_ERR_ARG, "out overlaps an input");
+    if (int rc = check_device(h)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (h->precision == ESDG_FP64)
+        e = dispatch_fp64(h->N, volume_args<double>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op64), s);
+    else
+        e = dispatch_fp32(h->N, volume_args<float>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op32), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "volume kernel launch");
+    return ESDG_OK;
+}
+
+int esdg_volume_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    return esdg_volume_rhs_range(h, 0, (long)h->K, q, metrics, phi, out, stream);
+}
+
+int esdg_get_status(esdg_handle h, unsigned* flags, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (!flags) return fail(h, ESDG_ERR_ARG, "flags is NULL");
+    if (int rc = check_device(h)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, h->d_status, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->d_status, 0, sizeof(unsigned), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "reading the status word");
+    *flags = v;
+    return ESDG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace esdg {
+
+constexpr int kMaxN = 8;
+constexpr int kMaxNq = kMaxN + 1;
+
+// Operator tables passed by value to the volume kernel (they live in the
+// kernel's parameter space, i.e. the constant bank).
+//   Q2[i*Nq + j] = 2 w_i D_ij   (twice the SBP matrix Q = W D)
+//   invw[i]      = 1 / w_i
+template <typename T>
+struct OpTables {
+    T Q2[kMaxNq * kMaxNq];
+    T invw[kMaxNq];
+};
+
+template <typename T>
+struct VolumeArgs {
+    const T* q;        // 5 planes
+    const T* Ja;       // 9 planes
+    const T* phi;      // 1 plane
+    T* out;            // 5 planes
+    long long n;       // plane stride (all nodes of the mesh)
+    long long e_begin; // first element of this launch
+    long long e_end;   // one past the last element
+    T gm1;             // gamma - 1
+    T c_g;             // 1 / (2 (gamma - 1))
+    T c_h;             // gamma / (2 (gamma - 1))
+    int form;          // 0: 2D form (diagonal kept), 1: skew form
+    unsigned* status;  // device status word (atomicOr of ESDG_STATUS_* bits)
+    OpTables<T> ops;
+};
+
+// Launchers, one per (precision, N); defined in the instantiation units.
+#define ESDG_DECLARE_LAUNCH(N)                                                       \
+    cudaError_t launch_volume_fp64_n##N(const VolumeArgs<double>& a, cudaStream_t s); \
+    cudaError_t launch_volume_fp32_n##N(const VolumeArgs<float>& a, cudaStream_t s);
+ESDG_DECLARE_LAUNCH(1)
+ESDG_DECLARE_LAUNCH(2)
+ESDG_DECLARE_LAUNCH(3)
+ESDG_DECLARE_LAUNCH(4)
+ESDG_DECLARE_LAUNCH(5)
+ESDG_DECLARE_LAUNCH(6)
+ESDG_DECLARE_LAUNCH(7)
+ESDG_DECLARE_LAUNCH(8)
+#undef ESDG_DECLARE_LAUNCH
+
+// Geometry: curl-form metrics in FP64 from node coordinates.
+struct GeometryArgs {
+    const double* x;
+    const double* y;
+    const double* z;
+    void* Ja;          // 9 planes, double or float
+    void* J;           // 1 plane or nullptr
+    long long K;
+    int N;
+    int fp32;          // output element type
+    double D[kMaxNq * kMaxNq];
+};
+cudaError_t launch_geometry(const GeometryArgs& a, cudaStream_t s);
+
+// Host-side operators (long double internally, rounded once to double).
+void lgl_operators(int N, double* nodes, double* weights, double* D);
+
+}  // namespace esdg

@@ -1,0 +1,156 @@
+/*
+ * esdg.h -- C-ABI of the GB300 flux-differencing volume-term library.
+ *
+ * The library evaluates the volume term of the entropy-stable discontinuous
+ * Galerkin (ESDG) discretisation of the Euler equations with buoyancy in
+ * "GPU Performance of an Entropy-Stable Discontinuous Galerkin Euler Solver
+ * with Non-Conservative Terms" (Sec. 3 Eq. 2, volume part; Sec. 4.1 Eqs. 3-6
+ * and Fig. 1).  For every hexahedral element of (N+1)^3 Legendre-Gauss-Lobatto
+ * (LGL) nodes, every node i and every reference direction r it forms
+ *
+ *     out_i = sum_r sum_{m on the r-line through i} 2 D_{a_r(i) a_r(m)} F^r(q_i, q_m)
+ *
+ * where F^r is the two-point entropy-conservative flux of Eqs. 3-4 contracted
+ * with the averaged metric terms (Ja^r(i) + Ja^r(m))/2, plus the
+ * non-conservative two-point gravity term of Eqs. 4-5 (rho_hat [[phi]] / 2).
+ * The output is NOT divided by the Jacobian J and NOT negated: the volume
+ * contribution to dq/dt is -out / J.  The Coriolis source h of Eq. 2 is not
+ * included.
+ *
+ * Conventions shared by every call:
+ *   - element e = ex + Kx*(ey + Ky*ez); node = a + Nq*(b + Nq*c) with Nq = N+1,
+ *     a along the first reference direction (xi), b along eta, c along zeta.
+ *   - n = K * Nq^3 nodes, K = Kx*Ky*Kz.  Every field is stored as planes of n
+ *     values: value (v, e, node) sits at offset v*n + e*Nq^3 + node.
+ *   - q:       5 planes (rho, rho*u1, rho*u2, rho*u3, E), E = p/(gamma-1) +
+ *              rho|u|^2/2 + rho*phi (Sec. 2).
+ *   - metrics: 9 planes, plane 3*r + j holds Ja^r_j = J d(xi_r)/d(x_j).
+ *   - phi:     1 plane, the geopotential g*z at the nodes.
+ *   - out:     5 planes in the order of q.
+ *   - "precision" selects the element type of q, metrics, phi, out and J:
+ *     ESDG_FP64 -> double, ESDG_FP32 -> float.  Node coordinates are always
+ *     double.
+ *   - Device pointers must be 16-byte aligned.  The caller allocates and owns
+ *     every buffer and stream; the library never frees caller memory.
+ *   - Streams are passed as cudaStream_t cast to void* (NULL = legacy default).
+ *   - Calls are asynchronous on the given stream unless stated otherwise.
+ *   - Every call returns ESDG_OK or an ESDG_ERR_* code; on error nothing is
+ *     launched and esdg_last_error() describes the cause.
+ *   - A handle is not thread-safe: use one handle per host thread.
+ */
+#ifndef ESDG_H
+#define ESDG_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct esdg_ctx* esdg_handle;
+
+enum {
+    ESDG_OK = 0,
+    ESDG_ERR_ARG = 1,          /* null handle/pointer, bad size, aliasing */
+    ESDG_ERR_UNSUPPORTED = 2,  /* N outside 1..8, unknown precision or form */
+    ESDG_ERR_ALIGN = 3,        /* a device pointer is not 16-byte aligned */
+    ESDG_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    ESDG_ERR_STATE = 5         /* call not valid in the handle's state */
+};
+
+enum { ESDG_FP64 = 0, ESDG_FP32 = 1 };
+
+/* ESDG_FORM_2D keeps the diagonal pairs m == i (the strong form whose
+ * diagonal contributes 2 D_ii Ja^r(i).f(q_i) at the two end nodes of a line);
+ * ESDG_FORM_SKEW drops them (the skew-symmetric operator whose diagonal is
+ * zero; Fig. 1 omits diagonal pairs).  The two differ only at element-face
+ * nodes, by exactly that end-node flux. */
+enum { ESDG_FORM_2D = 0, ESDG_FORM_SKEW = 1 };
+
+/* Status bits set by kernels and read with esdg_get_status(). */
+enum {
+    ESDG_STATUS_NONPHYSICAL = 1u  /* some node had rho <= 0, p <= 0 or NaN */
+};
+
+/* Create a handle for a mesh of Kx*Ky*Kz elements of order N (1..8).
+ * Builds the LGL nodes, weights and differentiation matrix (Sec. 3) on the
+ * host in long double.  Allocates host memory and one 4-byte device status
+ * word on the current device; the handle must be used on that device.
+ * Errors: ESDG_ERR_ARG (out == NULL, K < 1 or K*Nq^3 > 2^40),
+ * ESDG_ERR_UNSUPPORTED (N, precision or form), ESDG_ERR_CUDA. */
+int esdg_create(esdg_handle* out, long Kx, long Ky, long Kz, int N, int precision, int form);
+
+/* Release the handle and its status word.  Not stream-ordered: the caller
+ * must make sure no launch that uses the handle is still running.
+ * Accepts NULL. */
+int esdg_destroy(esdg_handle h);
+
+/* Ratio of specific heats (default 1.4).  Errors: ESDG_ERR_ARG unless
+ * 1 < gamma < 10. */
+int esdg_set_params(esdg_handle h, double gamma);
+
+/* Metric terms of the element geometry (Sec. 3, G_jk) in the conservative
+ * curl form Ja^r_j = -(curl_xi (X_l grad_xi X_m))_r, (j, m, l) cyclic, with
+ * every derivative taken by the LGL differentiation matrix, computed in FP64
+ * on the GPU and rounded to the handle's precision.  Also J = x_xi . (x_eta x
+ * x_zeta) when J_out != NULL.
+ *   x, y, z      device, double, n values each: node coordinates.
+ *   metrics_out  device, 9*n values of the handle's precision (written).
+ *   J_out        device, n values of the handle's precision, or NULL.
+ * Errors: ESDG_ERR_ARG (null handle or pointers), ESDG_ERR_ALIGN,
+ * ESDG_ERR_CUDA. */
+int esdg_set_geometry(esdg_handle h, const double* x, const double* y, const double* z,
+                      void* metrics_out, void* J_out, void* stream);
+
+/* The volume term for all K elements (see the top of this file).
+ *   q        device, 5*n values (read).
+ *   metrics  device, 9*n values (read).
+ *   phi      device, n values (read).
+ *   out      device, 5*n values (written); must not overlap any input.
+ * Enqueues one kernel launch on `stream`; no synchronisation and no
+ * allocation.  Nodes with rho <= 0 or p <= 0 set ESDG_STATUS_NONPHYSICAL in
+ * the handle's status word and produce non-finite values; nothing traps.
+ * Errors: ESDG_ERR_ARG, ESDG_ERR_ALIGN, ESDG_ERR_CUDA (launch failure). */
+int esdg_volume_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi,
+                    void* out, void* stream);
+
+/* As esdg_volume_rhs, restricted to elements [e_begin, e_begin + e_count)
+ * of the same full-size arrays (planes keep their stride n).  Elements are
+ * independent, so disjoint ranges compose bitwise into the full result; this
+ * is how the element range of a mesh is split across calls, streams or
+ * devices.  Errors as esdg_volume_rhs, plus ESDG_ERR_ARG when the range is
+ * empty or leaves 0..K. */
+int esdg_volume_rhs_range(esdg_handle h, long e_begin, long e_count, const void* q,
+                          const void* metrics, const void* phi, void* out, void* stream);
+
+/* Copy the status word to *flags and clear it.  Synchronises `stream`.
+ * Errors: ESDG_ERR_ARG, ESDG_ERR_CUDA. */
+int esdg_get_status(esdg_handle h, unsigned* flags, void* stream);
+
+/* Human-readable description of the last error on this handle (or of the last
+ * failed esdg_create when h == NULL).  Never NULL. */
+const char* esdg_last_error(esdg_handle h);
+
+/* LGL nodes (ascending), weights and differentiation matrix D (row-major,
+ * D[i*(N+1) + j] = l_j'(x_i)) exactly as the kernels use them, in double.
+ * Host only; no GPU needed.  Errors: ESDG_ERR_ARG, ESDG_ERR_UNSUPPORTED. */
+int esdg_get_operators(int N, double* nodes, double* weights, double* D);
+
+/* The pair schedule of one coordinate line, as the volume kernel runs it
+ * (Sec. 4.1 Eq. 6 and Fig. 1(b), weighted cyclic assignment).  The thread at
+ * line position p evaluates the pairs (p, (p + d) mod Nq) for d = 1..H with
+ * H = floor(Nq/2).  For d < Nq/2 the pair's result is added to both nodes;
+ * when Nq is even, d = Nq/2 joins antipodal nodes, each of which evaluates
+ * the pair itself and keeps only its own side (the weight-1/2 evaluations of
+ * Fig. 1(b) summed per node).  Writes, for each p and d, the partner index to
+ * partner[p*H + d-1] and 2 (both sides) or 1 (own side only) to
+ * sides[p*H + d-1].  Returns H through *H_out.  Host only.
+ * Errors: ESDG_ERR_ARG, ESDG_ERR_UNSUPPORTED. */
+int esdg_pair_schedule(int N, int* H_out, int* partner, int* sides);
+
+/* Library version as an integer (major*10000 + minor*100 + patch). */
+int esdg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ESDG_H */

@@ -1,0 +1,30 @@
+/*
+ * esdg_bench.h -- measurement kernels shipped with the volume-term library.
+ *
+ * Not part of the volume term.  They give the denominators of the volume
+ * kernel's roofline on the machine at hand: the FP64 and FP32 vector FMA
+ * throughput.  The ESDG GPU paper ("GPU Performance of an Entropy-Stable
+ * Discontinuous Galerkin Euler Solver with Non-Conservative Terms", Sec. 4.2,
+ * Fig. 3) reports the volume kernel against the FP64 peak of its GPU; this
+ * kernel measures that peak instead of quoting a data sheet.
+ */
+#ifndef ESDG_BENCH_H
+#define ESDG_BENCH_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Launch `blocks` CTAs of `threads` threads; every thread runs `iters`
+ * iterations of 8 independent fused multiply-adds (FP64 when fp64 != 0, FP32
+ * otherwise).  The launch performs 16 * iters * blocks * threads floating-
+ * point operations.  sink: device buffer of at least `blocks` elements of the
+ * chosen type (written only to keep the work observable).  Asynchronous on
+ * `stream`.  Returns 0, 1 (bad argument) or 4 (CUDA launch error). */
+int esdg_bench_fma(int fp64, long blocks, int threads, int iters, void* sink, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ESDG_BENCH_H */
