@@ -66,6 +66,33 @@ BYTES_PER_DOF = {"fp64": 20 * 8, "fp32": 20 * 4}  # 15 planes read + 5 written
 NOMINAL_FP64_TFLOPS = 1.25  # GB300 FP64 vector, nominal
 
 
+KERNEL_SOURCES = [os.path.join(ROOT, "flux_differencing_gb300", "csrc", f)
+                  for f in ("volume_kernel.cuh", "esdg_internal.h", "volume_inst.cu")]
+
+
+def kernel_source_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, only if the kernel source is unchanged."""
+    import glob
+    sha = kernel_source_sha()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as f:
+            for line in f:
+                if line.startswith("traffic_record:"):
+                    rec = json.loads(line.split(":", 1)[1])
+                    if rec["kernel"] == kernel and rec["workload"] == workload and rec["source_sha"] == sha:
+                        return rec["dram_bytes_per_launch"]
+    return None
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -377,13 +404,18 @@ def run_ours(args):
         return
 
     peaks, peak_src = _peaks()
-    fp64_meas = _fma_peak(True, device) / 1e12
-    fp32_meas = _fma_peak(False, device) / 1e12
+    if args.no_peaks:
+        fp64_meas, fp32_meas = float("nan"), float("nan")
+    else:
+        fp64_meas = _fma_peak(True, device) / 1e12
+        fp32_meas = _fma_peak(False, device) / 1e12
     main = results[args.workload]
     cfg = main["cfg"]
     peak64 = max(NOMINAL_FP64_TFLOPS, fp64_meas) if fp64_meas == fp64_meas else NOMINAL_FP64_TFLOPS
+    traffic = recorded_traffic(f"volume_kernel<double, {cfg.N}>", cfg.name)
     roof = {"bound": "alu", "achieved": main["achieved_tflops"], "peak": peak64, "unit": "TFLOP/s",
-            "frac": main["achieved_tflops"] / peak64, "traffic": None,
+            "frac": main["achieved_tflops"] / peak64, "traffic": traffic,
+            "traffic_unit": "bytes per launch (ncu dram read + write)",
             "peak_source": f"FP64 vector FMA: max(nominal {NOMINAL_FP64_TFLOPS}, measured {fp64_meas:.3f}) TFLOP/s",
             "algorithmic_flops_per_dof": flops_per_dof(cfg.N),
             "hbm": {"achieved_gbs": main["bytes_per_launch"] / (statistics.mean(main["per"]) * 1e-3) / 1e9,
@@ -436,6 +468,7 @@ def main():
     ap.add_argument("--fp32-workload", default="channel_N7_fp32")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-peaks", action="store_true", help="skip the FMA-throughput peak measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=int, default=256)
     args = ap.parse_args()

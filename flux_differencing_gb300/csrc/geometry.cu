@@ -48,10 +48,19 @@ __global__ void geometry_kernel(const __grid_constant__ GeometryArgs g) {
     const int t = threadIdx.x;
     const bool act = t < NP3;
     const int a = t % NQ, b = (t / NQ) % NQ, c = t / (NQ * NQ);
+    // Coordinates relative to an element-local origin (midpoint of two
+    // opposite corners).  The curl form is exactly invariant under a shift of
+    // X_l (the shift multiplies curl(grad X_m), which vanishes because the 1-D
+    // derivative matrices commute), while the rounding of D (X_l D X_m) grows
+    // with |X|^2: the shift keeps the metric terms accurate far from the origin.
+    const long long e0 = e * NP3, e1 = e * NP3 + NP3 - 1;
+    const double ox = 0.5 * (g.x[e0] + g.x[e1]);
+    const double oy = 0.5 * (g.y[e0] + g.y[e1]);
+    const double oz = 0.5 * (g.z[e0] + g.z[e1]);
     if (act) {
-        X[0 * NP3 + t] = g.x[e * NP3 + t];
-        X[1 * NP3 + t] = g.y[e * NP3 + t];
-        X[2 * NP3 + t] = g.z[e * NP3 + t];
+        X[0 * NP3 + t] = g.x[e * NP3 + t] - ox;
+        X[1 * NP3 + t] = g.y[e * NP3 + t] - oy;
+        X[2 * NP3 + t] = g.z[e * NP3 + t] - oz;
     }
     __syncthreads();
     if (act) {
