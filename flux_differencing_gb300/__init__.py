@@ -47,6 +47,9 @@ _SIGS = {
     "esdg_get_operators": (ctypes.c_int, [ctypes.c_int, _P, _P, _P]),
     "esdg_pair_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int), _P, _P]),
     "esdg_version": (ctypes.c_int, []),
+    "esdg_volume_rhs_noalloc": (ctypes.c_int, [ctypes.c_long, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_double, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_uint),
+                                               _P]),
     # measurement kernels, include/esdg_bench.h
     "esdg_bench_fma": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int, _P, _P]),
 }

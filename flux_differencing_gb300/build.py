@@ -34,7 +34,8 @@ def _nvcc() -> str:
 def _units():
     units = [("esdg_api", os.path.join(CSRC, "esdg_api.cu"), []),
              ("geometry", os.path.join(CSRC, "geometry.cu"), []),
-             ("peak_bench", os.path.join(CSRC, "peak_bench.cu"), [])]
+             ("peak_bench", os.path.join(CSRC, "peak_bench.cu"), []),
+             ("esdg_noalloc", os.path.join(CSRC, "esdg_noalloc.cu"), [])]
     for n in range(1, 9):
         for fp64 in (1, 0):
             units.append((f"volume_{'fp64' if fp64 else 'fp32'}_n{n}", os.path.join(CSRC, "volume_inst.cu"),

@@ -112,6 +112,8 @@ void lgl_operators(int N, double* nodes, double* weights, double* D) {
     }
 }
 
+void set_unhandled_error(const char* msg) { g_create_error = msg; }
+
 }  // namespace esdg
 
 namespace {

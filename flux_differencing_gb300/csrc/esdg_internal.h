@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 namespace esdg {
 
 constexpr int kMaxN = 8;
@@ -66,5 +68,10 @@ cudaError_t launch_geometry(const GeometryArgs& a, cudaStream_t s);
 
 // Host-side operators (long double internally, rounded once to double).
 void lgl_operators(int N, double* nodes, double* weights, double* D);
+
+// Record the message that esdg_last_error(NULL) returns on this thread (for
+// entry points that have no handle).
+void set_unhandled_error(const char* msg);
+inline void set_unhandled_error(const std::string& msg) { set_unhandled_error(msg.c_str()); }
 
 }  // namespace esdg

@@ -149,6 +149,40 @@ int esdg_pair_schedule(int N, int* H_out, int* partner, int* sides);
 /* Library version as an integer (major*10000 + minor*100 + patch). */
 int esdg_version(void);
 
+/* The volume term of esdg_volume_rhs for callers that cannot allocate device
+ * memory.  The paper has no counterpart: this is a library service.
+ *
+ * esdg_create allocates a 4-byte device status word per handle with
+ * cudaMalloc.  Some callers cannot allow that: applications that give all of
+ * the device memory to their own pool and forbid any other allocation, or
+ * code that must not call cudaMalloc on a busy device because the call can
+ * wait for work on other streams.  This entry point takes no handle and
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * Its only scratch is a file-scope __device__ array of 64 words (256 bytes)
+ * in the library, of which the volume kernel uses one status word; every
+ * device that loads the library holds that array until the process exits.
+ *
+ *   K          number of elements; n = K*(N+1)^3 nodes per plane.  At most
+ *              2^31-1 elements and 2^40 nodes per call (ESDG_ERR_ARG beyond).
+ *   N, precision, form, gamma   as for esdg_create / esdg_set_params.
+ *   q, metrics, phi, out        device pointers exactly as for esdg_volume_rhs.
+ *   status_out host pointer or NULL.  When non-NULL the call waits for the
+ *              kernel (synchronises `stream`) and stores the status bits
+ *              (ESDG_STATUS_*) of this call there.
+ *   stream     cudaStream_t cast to void*.
+ *
+ * The first call on a device looks up the device address of the scratch
+ * array with cudaGetSymbolAddress (once per device, with that device
+ * current); make that first call before any stream capture.  Every call on a
+ * device shares the one status word: the call clears it on `stream` before
+ * its kernel, so calls whose work overlaps on the GPU (different streams)
+ * race on it and may see each other's bits.
+ * Errors: ESDG_ERR_ARG, ESDG_ERR_UNSUPPORTED, ESDG_ERR_ALIGN, ESDG_ERR_CUDA;
+ * esdg_last_error(NULL) describes the cause. */
+int esdg_volume_rhs_noalloc(long K, int N, int precision, int form, double gamma, const void* q,
+                            const void* metrics, const void* phi, void* out, unsigned* status_out,
+                            void* stream);
+
 #ifdef __cplusplus
 }
 #endif
