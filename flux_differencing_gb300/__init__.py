@@ -52,6 +52,7 @@ _SIGS = {
                                                _P]),
     # measurement kernels, include/esdg_bench.h
     "esdg_bench_fma": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int, _P, _P]),
+    "esdg_selftest_rcp": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, _P, _P, _P]),
 }
 
 

@@ -2,6 +2,7 @@
 #include <cuda_runtime.h>
 
 #include "esdg_bench.h"
+#include "volume_kernel.cuh"
 
 namespace {
 
@@ -33,5 +34,24 @@ extern "C" int esdg_bench_fma(int fp64, long blocks, int threads, int iters, voi
     else
         fma_throughput<float><<<(unsigned)blocks, threads, 0, s>>>(static_cast<float*>(sink), iters, 0.9999f,
                                                                      1e-4f);
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+namespace {
+template <typename T>
+__global__ void rcp_selftest(const T* __restrict__ x, T* __restrict__ y, long n) {
+    const long k = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < n) y[k] = esdg::Num<T>::rcp(x[k]);
+}
+}  // namespace
+
+extern "C" int esdg_selftest_rcp(int fp64, long n, const void* x, void* y, void* stream) {
+    if (n < 1 || !x || !y) return 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const unsigned blocks = (unsigned)((n + 255) / 256);
+    if (fp64)
+        rcp_selftest<double><<<blocks, 256, 0, s>>>(static_cast<const double*>(x), static_cast<double*>(y), n);
+    else
+        rcp_selftest<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(x), static_cast<float*>(y), n);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }

@@ -4,7 +4,7 @@
 // What it computes (the volume part of Eq. 2 of "GPU Performance of an
 // Entropy-Stable Discontinuous Galerkin Euler Solver with Non-Conservative
 // Terms", Sec. 3): for every node i and reference direction r,
-//     out_i += (1/w_{p}) sum_m 2 Q_{p p'} (F + G)^r(i, m)
+//     out_i += (1/w_p) sum_m 2 Q_{p p'} (F + G)^r(i, m)
 // over the nodes m of the r-line through i (p, p' their positions on the
 // line, Q = W D so that 2 Q_{pp'}/w_p = 2 D_{pp'}).  F is the
 // entropy-conservative two-point flux (Eqs. 3-4), G the gravity term (Eqs.
@@ -15,7 +15,9 @@
 //    planes with coalesced loads straight into registers and writes per-node
 //    derived quantities to shared memory: u = m/rho, b = rho/(2p), 1/b,
 //    log rho, log b, h = phi/2 - |u|^2/4 (Sec. 4.1: primitives and logarithms
-//    once per node, not per pair), plus phi and the metric terms.
+//    once per node, not per pair), plus phi and the metric terms.  The same
+//    phase adds the diagonal pairs m == i of the 2D form, which only exist at
+//    element-face nodes, for all three directions at once.
 //  * Three direction phases (eta, zeta, then xi).  In each, every line's Nq
 //    nodes occupy Nq consecutive lanes of one warp.  The lane at line
 //    position p evaluates the pairs (p, p+d mod Nq), d = 1..floor(Nq/2) --
@@ -27,13 +29,21 @@
 //    atomics and a fixed summation order (bitwise deterministic).  For the
 //    antipodal offset d = Nq/2 (Nq even) both nodes evaluate the pair and
 //    keep their own side, which is Fig. 1(b)'s two weight-1/2 evaluations.
+//  * Shared memory is laid out per order (padding or an XOR swizzle, and the
+//    order in which lines are dealt to warps) so that the partner loads of
+//    every direction phase are free of bank conflicts where possible.
 //  * The mass flux is {{rho}}_log {{u}}.n, the energy flux the entropy-
-//    conserving completion (see the oracle); both are formed directly from
-//    the contravariant direction vector, never as a 3x5 flux matrix (Sec.
-//    4.1).  Log means use the per-node logarithms, switching to a series in
-//    ((a+ - a-)/(a+ + a-))^2 when the two logarithms are close, and 1/{{b}}_log
-//    is computed directly (Sec. 4.1).  The choice between the two is a select,
-//    not a branch, so lanes of a warp never diverge on it.
+//    conserving completion; both are formed directly from the contravariant
+//    direction vector, never as a 3x5 flux matrix (Sec. 4.1).  Log means use
+//    the per-node logarithms, switching to a series in ((a+ - a-)/(a+ + a-))^2
+//    when the two logarithms are close, and 1/{{b}}_log is computed directly
+//    (Sec. 4.1).  The switch is a select on one reciprocal, so lanes never
+//    diverge on it, and the closeness test runs on the integer pipe.
+//  * FP64 on GB300 has 1/64 of the FP32 rate, so the FP64 kernel is bound by
+//    its FP64 instruction count: reciprocals are a hardware estimate refined
+//    by one third-order Newton-Raphson step rather than a correctly rounded
+//    division, constants that depend only on the lane are hoisted, and sums
+//    are written as FMA chains.
 //  * Per-direction sums are scaled by 1/w once per node and combined in
 //    shared memory; the xi phase writes the result with coalesced stores.
 //  * No tensor cores: the flux is a nonlinear function of each pair.
@@ -55,7 +65,7 @@ struct Shape {
     static constexpr int H = NQ / 2;         // pair offsets per lane
     static constexpr bool EVEN = (NQ % 2) == 0;
     // elements per CTA: keeps lanes busy and the CTA at <= 512 threads
-    // (<= 864 for N = 8, where a single element already needs 27 warps)
+    // (864 for N = 8, where one element already needs 27 warps)
     static constexpr int EPB = (N == 1) ? 16 : (N == 2) ? 10 : (N == 3) ? 4 : (N == 4) ? 3
                              : (N == 5) ? 2 : 1;
     static constexpr int LINES = EPB * NL;
@@ -64,7 +74,38 @@ struct Shape {
     static constexpr int NODES = EPB * NP3;
 };
 
-// shared-memory field indices (each field is an array of Shape::NODES values)
+// Shared-memory layout of one node field.  SWZ: rows of Nq along xi with the
+// column XOR-swizzled by (c ^ (b & MASK)); otherwise padded strides P1 (eta)
+// and P2 (zeta).  ORDr = 1 deals the lines of direction r to warps with the
+// second of the two other indices varying fastest.  The values come from a
+// search over paddings, swizzles and line orders that minimises shared-memory
+// wavefronts of the partner loads (32-bit words): conflict-free for N = 1, 3,
+// 7, 8; about 1.3x of ideal for N = 4, 5, 6 and 1.7x for N = 2.
+template <int N>
+struct Layout;
+template <> struct Layout<1> { static constexpr bool SWZ = false; static constexpr int P1 = 2, P2 = 4, MASK = 0, ORD0 = 0, ORD1 = 0, ORD2 = 0; };
+template <> struct Layout<2> { static constexpr bool SWZ = false; static constexpr int P1 = 3, P2 = 9, MASK = 0, ORD0 = 0, ORD1 = 0, ORD2 = 0; };
+template <> struct Layout<3> { static constexpr bool SWZ = true; static constexpr int P1 = 4, P2 = 16, MASK = 0, ORD0 = 0, ORD1 = 0, ORD2 = 1; };
+template <> struct Layout<4> { static constexpr bool SWZ = false; static constexpr int P1 = 5, P2 = 26, MASK = 0, ORD0 = 0, ORD1 = 0, ORD2 = 0; };
+template <> struct Layout<5> { static constexpr bool SWZ = false; static constexpr int P1 = 6, P2 = 37, MASK = 0, ORD0 = 0, ORD1 = 1, ORD2 = 0; };
+template <> struct Layout<6> { static constexpr bool SWZ = false; static constexpr int P1 = 7, P2 = 50, MASK = 0, ORD0 = 0, ORD1 = 0, ORD2 = 0; };
+template <> struct Layout<7> { static constexpr bool SWZ = true; static constexpr int P1 = 8, P2 = 64, MASK = 6, ORD0 = 0, ORD1 = 0, ORD2 = 1; };
+template <> struct Layout<8> { static constexpr bool SWZ = false; static constexpr int P1 = 9, P2 = 93, MASK = 0, ORD0 = 0, ORD1 = 1, ORD2 = 0; };
+
+template <int N>
+struct Slots {
+    using S = Shape<N>;
+    using Lo = Layout<N>;
+    static constexpr int NQ = S::NQ;
+    static constexpr int ES = Lo::SWZ ? S::NP3 : Lo::P2 * NQ;  // element stride
+    static constexpr int SIZE = S::EPB * ES;                    // values per field
+    static __device__ __forceinline__ int at(int el, int a, int b, int c) {
+        if constexpr (Lo::SWZ) return el * ES + NQ * (b + NQ * c) + (a ^ ((c ^ (b & Lo::MASK)) & (NQ - 1)));
+        else return el * ES + a + Lo::P1 * b + Lo::P2 * c;
+    }
+};
+
+// shared-memory fields (each an array of Slots<N>::SIZE values)
 enum SmemField {
     F_RHO = 0, F_U1, F_U2, F_U3, F_B, F_INVB, F_LNRHO, F_LNB, F_PHI, F_H,
     F_JA0,              // 9 metric planes F_JA0 .. F_JA0 + 8
@@ -76,75 +117,64 @@ template <typename T>
 struct Num;
 template <>
 struct Num<double> {
-    // |log a+ - log a-| below which the series form of the log mean is used:
-    // (a+ - a-)/(a+ + a-) < ~1e-2, series truncation error < 1e-17
-    static __device__ __forceinline__ double tau() { return 2.0e-2; }
+    // 1/x: hardware estimate (rcp.approx.ftz.f64) and one Newton-Raphson step
+    // of third order, r' = r (1 + e + e^2) with e = 1 - x r, which cubes the
+    // estimate's relative error.  Zeros and infinities never reach a result
+    // that is used (the selects pick the other branch).
+    static __device__ __forceinline__ double rcp(double x) {
+        double r;
+        asm("rcp.approx.ftz.f64 %0, %1;" : "=d"(r) : "d"(x));
+        const double e = fma(-x, r, 1.0);
+        return fma(r, fma(e, e, e), r);
+    }
+    // |d| < 0.02 (high word of 0.02 = 0x3F947AE1), tested on the integer pipe
+    static __device__ __forceinline__ bool close(double d) {
+        return (static_cast<unsigned>(__double2hiint(d)) & 0x7fffffffu) < 0x3F947AE1u;
+    }
     static __device__ __forceinline__ double log_(double x) { return log(x); }
-    static __device__ __forceinline__ double rcp(double x) { return 1.0 / x; }
 };
 template <>
 struct Num<float> {
-    // (a+ - a-)/(a+ + a-) < ~0.1, series truncation error < 1e-9
-    static __device__ __forceinline__ float tau() { return 0.2f; }
+    static __device__ __forceinline__ float rcp(float x) {
+        float r;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+        return r;
+    }
+    // |d| < 0.2 (0x3E4CCCCD)
+    static __device__ __forceinline__ bool close(float d) {
+        return (__float_as_uint(d) & 0x7fffffffu) < 0x3E4CCCCDu;
+    }
     static __device__ __forceinline__ float log_(float x) { return logf(x); }
-    static __device__ __forceinline__ float rcp(float x) { return 1.0f / x; }
 };
-
-// Log mean {{a}}_log = (a+ - a-)/(log a+ - log a-) (Eq. 3) from per-node
-// logarithms.  With f = (a+ - a-)/(a+ + a-) and u = f^2,
-//   {{a}}_log = {{a}} * f / atanh(f) = {{a}} (1 - u/3 - 4u^2/45 - 44u^3/945 - ...),
-// which is used when the logarithms are close.  One reciprocal either way.
-template <typename T>
-__device__ __forceinline__ T log_mean(T ai, T am, T lai, T lam) {
-    const T d = am - ai;
-    const T s = am + ai;
-    const T dl = lam - lai;
-    const bool close = fabs(dl) < Num<T>::tau();
-    const T r = Num<T>::rcp(close ? s : dl);
-    const T t = d * r;          // close: f ; far: the log mean itself
-    const T u = t * t;
-    const T poly = T(1) - u * (T(1.0 / 3.0) + u * (T(4.0 / 45.0) + u * T(44.0 / 945.0)));
-    const T ser = T(0.5) * s * poly;
-    return close ? ser : t;
-}
-
-// 1/{{b}}_log (computed directly, Sec. 4.1) and 1/(b+ + b-).  With f and u as
-// above, 1/{{b}}_log = (2/(b+ + b-)) atanh(f)/f = (2/(b+ + b-)) (1 + u/3 + u^2/5 + u^3/7 + ...).
-// Far apart: 1/{{b}}_log = (log b+ - log b-)/(b+ - b-); both reciprocals then
-// come from the single reciprocal of (b+ - b-)(b+ + b-).
-template <typename T>
-__device__ __forceinline__ void inv_log_mean(T bi, T bm, T lbi, T lbm, T& inv_ln, T& inv_sum) {
-    const T d = bm - bi;
-    const T s = bm + bi;
-    const T dl = lbm - lbi;
-    const bool close = fabs(dl) < Num<T>::tau();
-    const T ds = d * s;
-    const T r = Num<T>::rcp(close ? s : ds);
-    inv_sum = close ? r : d * r;
-    const T f = d * inv_sum;
-    const T u = f * f;
-    const T P = T(1) + u * (T(1.0 / 3.0) + u * (T(1.0 / 5.0) + u * T(1.0 / 7.0)));
-    const T ser = T(2) * inv_sum * P;
-    const T far = dl * (s * r);
-    inv_ln = close ? ser : far;
-}
 
 template <typename T>
 __device__ __forceinline__ T shfl(T v, int src) {
     return __shfl_sync(0xffffffffu, v, src);
 }
 
-// One direction phase.  R = 0 (xi), 1 (eta), 2 (zeta).  MODE = 0: write the
-// scaled sum to the shared accumulators; 1: add to them; 2: add the shared
-// accumulators and store to global memory.
-template <typename T, int N, int R, int MODE>
-__device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __restrict__ sm,
-                                                int e_count, long long node0) {
+// Node (a, b, c) of line `ell` of direction R at line position p.
+template <int N, int R>
+__device__ __forceinline__ void line_node(int ell, int p, int& a, int& b, int& c) {
+    using Lo = Layout<N>;
+    constexpr int NQ = N + 1;
+    constexpr int ORD = (R == 0) ? Lo::ORD0 : (R == 1) ? Lo::ORD1 : Lo::ORD2;
+    const int o1 = ORD ? ell / NQ : ell % NQ;
+    const int o2 = ORD ? ell % NQ : ell / NQ;
+    if (R == 0) { a = p; b = o1; c = o2; }
+    else if (R == 1) { a = o1; b = p; c = o2; }
+    else { a = o1; b = o2; c = p; }
+}
+
+// One direction phase.  R = 0 (xi), 1 (eta), 2 (zeta).  FINAL = false: add
+// the scaled sum to the shared accumulators; true: add the shared
+// accumulators and store the node's result to global memory.
+template <typename T, int N, int R, bool FINAL>
+__device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __restrict__ sm, int e_count,
+                                                long long node0, const T (&c8)[Shape<N>::H], T iw) {
     using S = Shape<N>;
+    using SL = Slots<N>;
     constexpr int NQ = S::NQ;
-    constexpr int NP3 = S::NP3;
-    constexpr int NODES = S::NODES;
-    constexpr int STR = (R == 0) ? 1 : (R == 1) ? NQ : NQ * NQ;
+    constexpr int FS = SL::SIZE;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -155,30 +185,29 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __res
     if (!valid) L = 0;  // compute on element 0's first line, discard
     const int el = L / S::NL;
     const int ell = L - el * S::NL;
-    int base;
-    if (R == 0) base = el * NP3 + NQ * ell;
-    else if (R == 1) base = el * NP3 + (ell % NQ) + NQ * NQ * (ell / NQ);
-    else base = el * NP3 + ell;
-    const int i = base + p * STR;
+    int ia, ib, ic;
+    line_node<N, R>(ell, p, ia, ib, ic);
+    const int i = SL::at(el, ia, ib, ic);
 
-    const T* __restrict__ s_rho = sm + F_RHO * NODES;
-    const T* __restrict__ s_u1 = sm + F_U1 * NODES;
-    const T* __restrict__ s_u2 = sm + F_U2 * NODES;
-    const T* __restrict__ s_u3 = sm + F_U3 * NODES;
-    const T* __restrict__ s_b = sm + F_B * NODES;
-    const T* __restrict__ s_ib = sm + F_INVB * NODES;
-    const T* __restrict__ s_lr = sm + F_LNRHO * NODES;
-    const T* __restrict__ s_lb = sm + F_LNB * NODES;
-    const T* __restrict__ s_phi = sm + F_PHI * NODES;
-    const T* __restrict__ s_h = sm + F_H * NODES;
-    const T* __restrict__ s_A0 = sm + (F_JA0 + 3 * R + 0) * NODES;
-    const T* __restrict__ s_A1 = sm + (F_JA0 + 3 * R + 1) * NODES;
-    const T* __restrict__ s_A2 = sm + (F_JA0 + 3 * R + 2) * NODES;
+    const T* __restrict__ s_rho = sm + F_RHO * FS;
+    const T* __restrict__ s_u1 = sm + F_U1 * FS;
+    const T* __restrict__ s_u2 = sm + F_U2 * FS;
+    const T* __restrict__ s_u3 = sm + F_U3 * FS;
+    const T* __restrict__ s_b = sm + F_B * FS;
+    const T* __restrict__ s_ib = sm + F_INVB * FS;
+    const T* __restrict__ s_lr = sm + F_LNRHO * FS;
+    const T* __restrict__ s_lb = sm + F_LNB * FS;
+    const T* __restrict__ s_phi = sm + F_PHI * FS;
+    const T* __restrict__ s_h = sm + F_H * FS;
+    const T* __restrict__ s_A0 = sm + (F_JA0 + 3 * R + 0) * FS;
+    const T* __restrict__ s_A1 = sm + (F_JA0 + 3 * R + 1) * FS;
+    const T* __restrict__ s_A2 = sm + (F_JA0 + 3 * R + 2) * FS;
 
     const T rho_i = s_rho[i], u1_i = s_u1[i], u2_i = s_u2[i], u3_i = s_u3[i];
     const T b_i = s_b[i], ib_i = s_ib[i], lr_i = s_lr[i], lb_i = s_lb[i];
     const T phi_i = s_phi[i], h_i = s_h[i];
     const T A0_i = s_A0[i], A1_i = s_A1[i], A2_i = s_A2[i];
+    const T c_g = a.c_g;
 
     T acc0 = T(0), acc1 = T(0), acc2 = T(0), acc3 = T(0), acc4 = T(0);
 
@@ -187,42 +216,69 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __res
         const bool both = !(S::EVEN && d == S::H);  // antipodal: own side only
         int pm = p + d;
         if (pm >= NQ) pm -= NQ;
-        const T c2q = a.ops.Q2[p * NQ + pm];
-        const int m = base + pm * STR;
+        int ma = ia, mb = ib, mc = ic;
+        if (R == 0) ma = pm;
+        else if (R == 1) mb = pm;
+        else mc = pm;
+        const int m = SL::at(el, ma, mb, mc);
 
         const T rho_m = s_rho[m], u1_m = s_u1[m], u2_m = s_u2[m], u3_m = s_u3[m];
-        const T b_m = s_b[m], ib_m = s_ib[m];
+        const T b_m = s_b[m];
 
-        const T A0 = A0_i + s_A0[m], A1 = A1_i + s_A1[m], A2 = A2_i + s_A2[m];  // 2 x avg metric
-        const T s1 = u1_i + u1_m, s2 = u2_i + u2_m, s3 = u3_i + u3_m;          // 2 x avg velocity
-        const T Un = s1 * A0 + s2 * A1 + s3 * A2;                               // 4 x {{u}}.n
+        // 2 x averaged metric, 2 x averaged velocity, 4 x {{u}}.n
+        const T A0 = A0_i + s_A0[m], A1 = A1_i + s_A1[m], A2 = A2_i + s_A2[m];
+        const T s1 = u1_i + u1_m, s2 = u2_i + u2_m, s3 = u3_i + u3_m;
+        const T Un = fma(s3, A2, fma(s2, A1, s1 * A0));
 
-        const T rho_ln = log_mean<T>(rho_i, rho_m, lr_i, s_lr[m]);
-        T inv_bln, inv_bsum;
-        inv_log_mean<T>(b_i, b_m, lb_i, s_lb[m], inv_bln, inv_bsum);
+        // {{rho}}_log: (rho+ - rho-)/(ln rho+ - ln rho-), or the series when close
+        const T rsum = rho_i + rho_m;
+        const T drho = rho_m - rho_i;
+        const T dlr = s_lr[m] - lr_i;
+        const bool cr = Num<T>::close(dlr);
+        const T rr = Num<T>::rcp(cr ? rsum : dlr);
+        const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
+        const T ur = tr * tr;
+        // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945)
+        const T polr = fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
+        const T rho_ln = cr ? rsum * polr : tr;
+
+        // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
         const T bsum = b_i + b_m;
-        const T ph = T(0.25) * (rho_i + rho_m) * inv_bsum;       // {{rho}}/(2{{b}}) / 2
-        const T g = T(0.125) * rho_ln * bsum * (s_phi[m] - phi_i);  // gravity, Eqs. 4-5
-        const T frh = (T(0.125) * c2q) * rho_ln * Un;             // 2Q F_rho / 2
-        const T fr = frh + frh;                                     // 2Q F_rho
-        const T ss = s1 * s1 + s2 * s2 + s3 * s3;
-        const T Kf = a.c_g * inv_bln + (h_i + s_h[m]) + T(0.25) * ss;
-        const T fE = fr * Kf + (T(0.5) * c2q) * Un * ph;          // 2Q F_E
-        const T gq = c2q * g;
-        const T phq = c2q * ph;
-        const T Pi = gq * ib_i + phq;   // own:     2Q (p_hat/2 + G scale at b_i)
+        const T db = b_m - b_i;
+        const T dlb = s_lb[m] - lb_i;
+        const bool cb = Num<T>::close(dlb);
+        const T rb = Num<T>::rcp(cb ? bsum : db * bsum);
+        const T inv_bsum = cb ? rb : db * rb;
+        const T fb = db * inv_bsum;
+        const T ub = fb * fb;
+        // (2/bsum) atanh(f)/f = (2/bsum)(1 + u/3 + u^2/5 + u^3/7)
+        const T polb = fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
+        const T inv_bln = cb ? inv_bsum * polb : dlb * (bsum * rb);
+
+        // flux scalars, already multiplied by 2Q_{pp'} (c8 = 2Q/8)
+        const T cr8 = c8[d - 1] * rho_ln;
+        const T frh = cr8 * Un;                                // 2Q F_rho / 2
+        const T fr = frh + frh;                                // 2Q F_rho
+        const T gq = cr8 * (bsum * (s_phi[m] - phi_i));        // 2Q rho_ln {{b}} [[phi]] / 2: gravity
+        const T cp = c8[d - 1] * (rsum * inv_bsum);            // 2Q {{rho}}/(2{{b}}) / 4
+        const T phq = cp + cp;                                 // 2Q p_hat / 2
+        const T ss = fma(s3, s3, fma(s2, s2, s1 * s1));
+        const T Kf = fma(c_g, inv_bln, fma(T(0.25), ss, h_i + s_h[m]));
+        const T fE = fma(fr, Kf, cp * Un);                     // 2Q F_E
+        const T Pi = fma(gq, ib_i, phq);  // own: pressure mean + gravity at b_i
+
         acc0 += fr;
-        acc1 += frh * s1 + A0 * Pi;
-        acc2 += frh * s2 + A1 * Pi;
-        acc3 += frh * s3 + A2 * Pi;
+        acc1 = fma(A0, Pi, fma(frh, s1, acc1));
+        acc2 = fma(A1, Pi, fma(frh, s2, acc2));
+        acc3 = fma(A2, Pi, fma(frh, s3, acc3));
         acc4 += fE;
         if (both) {
             // partner's share: 2Q_{p'p} (F + G(m,i)) with 2Q_{p'p} = -2Q_{pp'} and
             // G(m,i) = -G(i,m) b_i/b_m
-            const T Pm = gq * ib_m - phq;
-            const T t1 = A0 * Pm - frh * s1;
-            const T t2 = A1 * Pm - frh * s2;
-            const T t3 = A2 * Pm - frh * s3;
+            const T Pm = fma(gq, s_ib[m], -phq);
+            const T t1 = fma(A0, Pm, -(frh * s1));
+            const T t2 = fma(A1, Pm, -(frh * s2));
+            const T t3 = fma(A2, Pm, -(frh * s3));
             int src = p - d;
             if (src < 0) src += NQ;
             src += slot * NQ;
@@ -234,44 +290,27 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __res
         }
     }
 
-    if (a.form == 0 && (p == 0 || p == N)) {
-        // diagonal pair m == i: 2 Q_pp Ja^r(i) . f(q_i), f the physical flux (Eq. 1)
-        const T qd = a.ops.Q2[p * NQ + p];
-        const T Uc = u1_i * A0_i + u2_i * A1_i + u3_i * A2_i;
-        const T rU = qd * rho_i * Uc;
-        const T pr = qd * T(0.5) * rho_i * ib_i;
-        const T Hh = a.c_h * ib_i + T(2) * (phi_i - h_i);  // (E + p)/rho
-        acc0 += rU;
-        acc1 += rU * u1_i + pr * A0_i;
-        acc2 += rU * u2_i + pr * A1_i;
-        acc3 += rU * u3_i + pr * A2_i;
-        acc4 += rU * Hh;
-    }
-
-    const T iw = a.ops.invw[p];
-    T* s_acc = sm + F_ACC0 * NODES;
-    if (MODE == 0 && valid) {
-        s_acc[0 * NODES + i] = acc0 * iw;
-        s_acc[1 * NODES + i] = acc1 * iw;
-        s_acc[2 * NODES + i] = acc2 * iw;
-        s_acc[3 * NODES + i] = acc3 * iw;
-        s_acc[4 * NODES + i] = acc4 * iw;
-    } else if (MODE == 1 && valid) {
-        s_acc[0 * NODES + i] += acc0 * iw;
-        s_acc[1 * NODES + i] += acc1 * iw;
-        s_acc[2 * NODES + i] += acc2 * iw;
-        s_acc[3 * NODES + i] += acc3 * iw;
-        s_acc[4 * NODES + i] += acc4 * iw;
-    } else if (MODE == 2 && valid) {
-        // xi phase: i = L*NQ + p is the block-linear node, so lanes store contiguously
-        const long long g = node0 + i;
+    T* s_acc = sm + F_ACC0 * FS;
+    if (!FINAL) {
+        if (valid) {
+            s_acc[0 * FS + i] = fma(acc0, iw, s_acc[0 * FS + i]);
+            s_acc[1 * FS + i] = fma(acc1, iw, s_acc[1 * FS + i]);
+            s_acc[2 * FS + i] = fma(acc2, iw, s_acc[2 * FS + i]);
+            s_acc[3 * FS + i] = fma(acc3, iw, s_acc[3 * FS + i]);
+            s_acc[4 * FS + i] = fma(acc4, iw, s_acc[4 * FS + i]);
+        }
+    } else if (valid) {
+        // xi phase: lines of a warp are consecutive (b, c) rows, so the block-
+        // linear node L*Nq + p is contiguous across lanes: coalesced stores
+        static_assert(R != 0 || Layout<N>::ORD0 == 0, "xi lines must be dealt b-fastest");
+        const long long g = node0 + (long long)L * NQ + p;
         T* __restrict__ o = a.out;
         const long long n = a.n;
-        o[0 * n + g] = s_acc[0 * NODES + i] + acc0 * iw;
-        o[1 * n + g] = s_acc[1 * NODES + i] + acc1 * iw;
-        o[2 * n + g] = s_acc[2 * NODES + i] + acc2 * iw;
-        o[3 * n + g] = s_acc[3 * NODES + i] + acc3 * iw;
-        o[4 * n + g] = s_acc[4 * NODES + i] + acc4 * iw;
+        o[0 * n + g] = fma(acc0, iw, s_acc[0 * FS + i]);
+        o[1 * n + g] = fma(acc1, iw, s_acc[1 * FS + i]);
+        o[2 * n + g] = fma(acc2, iw, s_acc[2 * FS + i]);
+        o[3 * n + g] = fma(acc3, iw, s_acc[3 * FS + i]);
+        o[4 * n + g] = fma(acc4, iw, s_acc[4 * FS + i]);
     }
 }
 
@@ -279,8 +318,10 @@ template <typename T, int N>
 __global__ void __launch_bounds__(Shape<N>::THREADS, (sizeof(T) == 4 && Shape<N>::THREADS <= 512) ? 2 : 1)
 volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     using S = Shape<N>;
+    using SL = Slots<N>;
+    constexpr int NQ = S::NQ;
     constexpr int NP3 = S::NP3;
-    constexpr int NODES = S::NODES;
+    constexpr int FS = SL::SIZE;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* sm = reinterpret_cast<T*>(smem_raw);
 
@@ -291,12 +332,17 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
 
     // ---- load phase: one node per thread, coalesced plane reads -> derived values
     bool bad = false;
-    for (int t = threadIdx.x; t < NODES; t += S::THREADS) {
+    for (int t = threadIdx.x; t < S::NODES; t += S::THREADS) {
+        const int el = t / NP3;
+        const int nd = t - el * NP3;
+        const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
+        const int sl = SL::at(el, na, nb, nc);
         T rho = T(1), m1 = T(0), m2 = T(0), m3 = T(0), E = T(1), phi = T(0);
         T ja[9];
 #pragma unroll
         for (int k = 0; k < 9; ++k) ja[k] = T(0);
-        if (t < e_count * NP3) {
+        const bool real = t < e_count * NP3;
+        if (real) {
             const long long g = node0 + t;
             const long long n = a.n;
             rho = __ldg(a.q + g);
@@ -310,34 +356,71 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         }
         const T irho = Num<T>::rcp(rho);
         const T u1 = m1 * irho, u2 = m2 * irho, u3 = m3 * irho;
-        const T uu = u1 * u1 + u2 * u2 + u3 * u3;
-        T pr = a.gm1 * (E - T(0.5) * rho * uu - rho * phi);
-        if (t >= e_count * NP3) pr = T(0.5) * a.gm1;  // padding node: b = 1/gm1, finite
+        const T uu = fma(u3, u3, fma(u2, u2, u1 * u1));
+        T pr = a.gm1 * (E - rho * fma(T(0.5), uu, phi));
+        if (!real) pr = T(0.5) * a.gm1;  // padding node: finite values, never stored
         bad |= !(rho > T(0)) || !(pr > T(0));
         const T ipr = Num<T>::rcp(pr);
         const T b = T(0.5) * rho * ipr;
         const T ib = T(2) * pr * irho;
-        sm[F_RHO * NODES + t] = rho;
-        sm[F_U1 * NODES + t] = u1;
-        sm[F_U2 * NODES + t] = u2;
-        sm[F_U3 * NODES + t] = u3;
-        sm[F_B * NODES + t] = b;
-        sm[F_INVB * NODES + t] = ib;
-        sm[F_LNRHO * NODES + t] = Num<T>::log_(rho);
-        sm[F_LNB * NODES + t] = Num<T>::log_(b);
-        sm[F_PHI * NODES + t] = phi;
-        sm[F_H * NODES + t] = T(0.5) * phi - T(0.25) * uu;
+        const T h = fma(T(-0.25), uu, T(0.5) * phi);
+        sm[F_RHO * FS + sl] = rho;
+        sm[F_U1 * FS + sl] = u1;
+        sm[F_U2 * FS + sl] = u2;
+        sm[F_U3 * FS + sl] = u3;
+        sm[F_B * FS + sl] = b;
+        sm[F_INVB * FS + sl] = ib;
+        sm[F_LNRHO * FS + sl] = Num<T>::log_(rho);
+        sm[F_LNB * FS + sl] = Num<T>::log_(b);
+        sm[F_PHI * FS + sl] = phi;
+        sm[F_H * FS + sl] = h;
 #pragma unroll
-        for (int k = 0; k < 9; ++k) sm[(F_JA0 + k) * NODES + t] = ja[k];
+        for (int k = 0; k < 9; ++k) sm[(F_JA0 + k) * FS + sl] = ja[k];
+
+        // diagonal pairs of the 2D form: sum_r 2 D_{a_r a_r} Ja^r(i) . f(q_i), nonzero
+        // only where a_r is 0 or N; f is the physical flux of Eq. 1
+        T f0 = T(0), f1 = T(0), f2 = T(0), f3 = T(0), f4 = T(0);
+        if (a.form == 0) {
+            const T dA = (na == 0 || na == N) ? a.ops.Q2[na * NQ + na] * a.ops.invw[na] : T(0);
+            const T dB = (nb == 0 || nb == N) ? a.ops.Q2[nb * NQ + nb] * a.ops.invw[nb] : T(0);
+            const T dC = (nc == 0 || nc == N) ? a.ops.Q2[nc * NQ + nc] * a.ops.invw[nc] : T(0);
+            const T V0 = fma(dC, ja[6], fma(dB, ja[3], dA * ja[0]));
+            const T V1 = fma(dC, ja[7], fma(dB, ja[4], dA * ja[1]));
+            const T V2 = fma(dC, ja[8], fma(dB, ja[5], dA * ja[2]));
+            const T rU = rho * fma(u3, V2, fma(u2, V1, u1 * V0));
+            const T pp = T(0.5) * rho * ib;
+            f0 = rU;
+            f1 = fma(rU, u1, pp * V0);
+            f2 = fma(rU, u2, pp * V1);
+            f3 = fma(rU, u3, pp * V2);
+            f4 = rU * fma(a.c_h, ib, T(2) * (phi - h));  // (E + p) U
+        }
+        sm[(F_ACC0 + 0) * FS + sl] = f0;
+        sm[(F_ACC0 + 1) * FS + sl] = f1;
+        sm[(F_ACC0 + 2) * FS + sl] = f2;
+        sm[(F_ACC0 + 3) * FS + sl] = f3;
+        sm[(F_ACC0 + 4) * FS + sl] = f4;
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(a.status, 1u);
+
+    // lane constants: 2Q_{p,p+d}/8 for every offset and 1/w_p
+    const int lane = threadIdx.x & 31;
+    const int p = lane - (lane / NQ) * NQ;
+    T c8[S::H];
+#pragma unroll
+    for (int d = 1; d <= S::H; ++d) {
+        int pm = p + d;
+        if (pm >= NQ) pm -= NQ;
+        c8[d - 1] = T(0.125) * a.ops.Q2[p * NQ + pm];
+    }
+    const T iw = a.ops.invw[p];
     __syncthreads();
 
-    direction_phase<T, N, 1, 0>(a, sm, e_count, node0);
+    direction_phase<T, N, 1, false>(a, sm, e_count, node0, c8, iw);
     __syncthreads();
-    direction_phase<T, N, 2, 1>(a, sm, e_count, node0);
+    direction_phase<T, N, 2, false>(a, sm, e_count, node0, c8, iw);
     __syncthreads();
-    direction_phase<T, N, 0, 2>(a, sm, e_count, node0);
+    direction_phase<T, N, 0, true>(a, sm, e_count, node0, c8, iw);
 }
 
 template <typename T, int N>
@@ -345,7 +428,7 @@ cudaError_t launch_volume(const VolumeArgs<T>& a, cudaStream_t s) {
     using S = Shape<N>;
     const long long K = a.e_end - a.e_begin;
     if (K <= 0) return cudaSuccess;
-    const size_t smem = sizeof(T) * (size_t)F_COUNT * S::NODES;
+    const size_t smem = sizeof(T) * (size_t)F_COUNT * Slots<N>::SIZE;
     static bool attr_done = false;  // per instantiation; set once per process
     if (!attr_done) {
         cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N>,

@@ -23,6 +23,14 @@ extern "C" {
  * `stream`.  Returns 0, 1 (bad argument) or 4 (CUDA launch error). */
 int esdg_bench_fma(int fp64, long blocks, int threads, int iters, void* sink, void* stream);
 
+/* Self-test of the volume kernel's reciprocal: y[k] = 1/x[k] computed exactly
+ * as the kernel computes it (hardware estimate plus one third-order
+ * Newton-Raphson step in FP64; the hardware estimate alone in FP32), so the
+ * test suite can measure its error against correctly rounded division.
+ * x, y: device arrays of n doubles (fp64 != 0) or floats.  Asynchronous on
+ * `stream`.  Returns 0, 1 (bad argument) or 4 (CUDA launch error). */
+int esdg_selftest_rcp(int fp64, long n, const void* x, void* y, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

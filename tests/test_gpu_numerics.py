@@ -1,0 +1,58 @@
+"""Accuracy of the volume kernel's reciprocal (GPU required).
+
+FP64: hardware estimate refined by one third-order Newton-Raphson step; it
+must stay within 2 ulp of correctly rounded division.  FP32: the hardware
+estimate alone, within 2^-22 relative.  Reference values are numpy's IEEE
+division on the host.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import flux_differencing_gb300 as fd
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lib, x, fp64):
+    dt = torch.float64 if fp64 else torch.float32
+    xd = torch.from_numpy(x).to("cuda", dt)
+    yd = torch.empty_like(xd)
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.esdg_selftest_rcp(1 if fp64 else 0, xd.numel(), ctypes.c_void_p(xd.data_ptr()),
+                                 ctypes.c_void_p(yd.data_ptr()), s) == 0
+    torch.cuda.synchronize()
+    return yd.cpu().numpy()
+
+
+def _inputs(rng, n, lo, hi):
+    mag = np.exp(rng.uniform(np.log(lo), np.log(hi), size=n))
+    x = mag * rng.choice([-1.0, 1.0], size=n)
+    # also mantissas near 1 and near 2 (worst cases of table-based estimates)
+    x[:64] = 1.0 + np.arange(64) * 2.0 ** -52
+    x[64:128] = 2.0 - np.arange(1, 65) * 2.0 ** -52
+    return x
+
+
+def test_rcp_fp64_within_two_ulp(cuda_ok):
+    lib = fd.load_library(build_if_missing=True)
+    rng = np.random.default_rng(17)
+    x = _inputs(rng, 1 << 20, 1e-300, 1e300)
+    y = _run(lib, x, True)
+    ref = 1.0 / x
+    ulp = np.spacing(np.abs(ref))
+    err = np.abs(y - ref) / ulp
+    assert np.all(np.isfinite(y))
+    assert err.max() <= 2.0, err.max()
+
+
+def test_rcp_fp32_relative_error(cuda_ok):
+    lib = fd.load_library(build_if_missing=True)
+    rng = np.random.default_rng(18)
+    x = _inputs(rng, 1 << 20, 1e-30, 1e30).astype(np.float32)
+    y = _run(lib, x, False).astype(np.float64)
+    ref = 1.0 / x.astype(np.float64)
+    rel = np.abs(y - ref) / np.abs(ref)
+    assert rel.max() < 2.0 ** -22, rel.max()
