@@ -168,6 +168,27 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+def element_shard(K: int, world: int, rank: int):
+    """Contiguous, balanced element range (e_begin, e_count) of `rank` out of `world`.
+
+    Elements are independent in the volume term, so ranks that each take one
+    range need no exchange; the union of the ranges is 0..K exactly once."""
+    base, extra = divmod(K, world)
+    e_begin = rank * base + min(rank, extra)
+    return e_begin, base + (1 if rank < extra else 0)
+
+
+def max_over_ranks(x: float, group=None, device=None) -> float:
+    """Largest value over all ranks (the timing rule: the slowest rank counts)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size(group) == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -360,12 +381,8 @@ def run_ours(args):
         if ws > 1:
             dist.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if ws == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def slowest(x: float) -> float:
+        return max_over_ranks(x, device=device)
 
     stream = torch.cuda.Stream(device)
     results = {}
@@ -380,7 +397,7 @@ def run_ours(args):
         if sampler:
             clocks = sampler.stop()
         assert op.status() == 0, "non-physical state in the bench inputs"
-        total_ms = max_over_ranks(total_ms)
+        total_ms = slowest(total_ms)
         ms = total_ms / args.steps
         gdof = ws * cfg.n / (ms * 1e-3) / 1e9
         fl = flops_per_dof(cfg.N) * cfg.n
@@ -390,7 +407,7 @@ def run_ours(args):
         if not args.no_e2e:
             e2e_steps = max(3, min(args.steps, 20))
             e_ms, h2d, d2h = _time_e2e(op, q, Ja, phi, out, e2e_steps, 1, stream, barrier)
-            e_ms = max_over_ranks(e_ms) / e2e_steps
+            e_ms = slowest(e_ms) / e2e_steps
             res["e2e"] = {"value": ws * cfg.n / (e_ms * 1e-3) / 1e9, "unit": "GDOF/s",
                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
         results[wname] = res
@@ -443,6 +460,7 @@ def run_ours(args):
             "workload": c32.name, "value": r32["gdof"], "unit": "GDOF/s", "ms_per_step": r32["ms"],
             "roofline": {"bound": "alu", "achieved": r32["achieved_tflops"], "peak": fp32_meas,
                          "unit": "TFLOP/s", "frac": r32["achieved_tflops"] / fp32_meas,
+                         "traffic": recorded_traffic(f"volume_kernel<float, {c32.N}>", c32.name),
                          "peak_source": "measured FP32 vector FMA",
                          "hbm": {"achieved_gbs": hbm32, "peak_gbs": peaks.get("hbm_gbs"),
                                  "frac": hbm32 / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None}},

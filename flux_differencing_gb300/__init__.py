@@ -45,7 +45,7 @@ _SIGS = {
     "esdg_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint), _P]),
     "esdg_last_error": (ctypes.c_char_p, [_P]),
     "esdg_get_operators": (ctypes.c_int, [ctypes.c_int, _P, _P, _P]),
-    "esdg_pair_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int), _P, _P]),
+    "esdg_pair_schedule": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int), _P, _P]),
     "esdg_version": (ctypes.c_int, []),
     "esdg_volume_rhs_noalloc": (ctypes.c_int, [ctypes.c_long, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_double, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_uint),
@@ -107,13 +107,14 @@ def operators(N: int):
     return x, w, D
 
 
-def pair_schedule(N: int):
+def pair_schedule(N: int, precision: str = "fp64"):
     """(H, partner[p, d-1], sides[p, d-1]) of the kernel's per-line pair schedule."""
     lib = load_library()
     H = ctypes.c_int(0)
     partner = np.zeros((N + 1) * ((N + 1) // 2), dtype=np.int32)
     sides = np.zeros_like(partner)
-    _check(lib.esdg_pair_schedule(N, ctypes.byref(H), partner.ctypes.data, sides.ctypes.data))
+    prec = ESDG_FP64 if precision == "fp64" else ESDG_FP32
+    _check(lib.esdg_pair_schedule(N, prec, ctypes.byref(H), partner.ctypes.data, sides.ctypes.data))
     return H.value, partner.reshape(N + 1, -1), sides.reshape(N + 1, -1)
 
 

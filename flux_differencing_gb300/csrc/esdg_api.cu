@@ -199,17 +199,27 @@ int esdg_get_operators(int N, double* nodes, double* weights, double* D) {
     return ESDG_OK;
 }
 
-int esdg_pair_schedule(int N, int* H_out, int* partner, int* sides) {
+int esdg_pair_schedule(int N, int precision, int* H_out, int* partner, int* sides) {
     if (N < 1 || N > esdg::kMaxN) return fail(nullptr, ESDG_ERR_UNSUPPORTED, "N must be in 1..8");
+    if (precision != ESDG_FP64 && precision != ESDG_FP32)
+        return fail(nullptr, ESDG_ERR_UNSUPPORTED, "precision must be ESDG_FP64 or ESDG_FP32");
     if (!H_out || !partner || !sides) return fail(nullptr, ESDG_ERR_ARG, "null output pointer");
-    // Must match direction_phase in volume_kernel.cuh: offsets d = 1..Nq/2,
-    // both sides unless Nq is even and d == Nq/2.
+    // Must match volume_kernel.cuh: direction_phase evaluates offsets
+    // d < Nq/2 on every position.  For even Nq the antipodal offset d = Nq/2
+    // is, in FP64 (SplitAntipodal), evaluated once by the lower position in
+    // antipodal_phase; in FP32 both positions evaluate it and keep their own
+    // share.
+    const bool split = precision == ESDG_FP64;
     const int Nq = N + 1, H = Nq / 2;
     *H_out = H;
     for (int p = 0; p < Nq; ++p)
         for (int d = 1; d <= H; ++d) {
-            partner[p * H + d - 1] = (p + d) % Nq;
-            sides[p * H + d - 1] = (Nq % 2 == 0 && d == H) ? 1 : 2;
+            const bool antipodal = (Nq % 2 == 0) && d == H;
+            int pt = (p + d) % Nq, sd = 2;
+            if (antipodal && split && p >= H) { pt = -1; sd = 0; }
+            else if (antipodal && !split) sd = 1;
+            partner[p * H + d - 1] = pt;
+            sides[p * H + d - 1] = sd;
         }
     return ESDG_OK;
 }

@@ -20,15 +20,19 @@
 //    element-face nodes, for all three directions at once.
 //  * Three direction phases (eta, zeta, then xi).  In each, every line's Nq
 //    nodes occupy Nq consecutive lanes of one warp.  The lane at line
-//    position p evaluates the pairs (p, p+d mod Nq), d = 1..floor(Nq/2) --
-//    the weighted cyclic assignment of Sec. 4.1 Eq. 6 / Fig. 1(b): every lane
-//    does the same number of evaluations.  For d < Nq/2 the pair's result
-//    feeds both nodes ("half-sweep"): the partner's share is formed with
-//    2 Q_{p'p} = -2 Q_{pp'} and the gravity partner scaling G -> -G b_i/b_m
-//    (Sec. 4.1) and moved to the partner lane by a warp shuffle, so no
-//    atomics and a fixed summation order (bitwise deterministic).  For the
-//    antipodal offset d = Nq/2 (Nq even) both nodes evaluate the pair and
-//    keep their own side, which is Fig. 1(b)'s two weight-1/2 evaluations.
+//    position p evaluates the pairs (p, p+d mod Nq) for d < Nq/2 -- the
+//    cyclic assignment of Sec. 4.1 Eq. 6: every lane does the same number of
+//    evaluations.  Each pair's result feeds both nodes ("half-sweep"): the
+//    partner's share is formed with 2 Q_{p'p} = -2 Q_{pp'} and the gravity
+//    partner scaling G -> -G b_i/b_m (Sec. 4.1) and moved to the partner lane
+//    by a warp shuffle, so no atomics and a fixed summation order (bitwise
+//    deterministic).
+//  * For even Nq the antipodal pairs (p, p + Nq/2) are where Eq. 6 loses
+//    balance and Fig. 1(b) evaluates each pair twice with weight 1/2.  Here
+//    they get a pass of their own per direction: within one direction every
+//    node is in exactly one antipodal pair, so one thread evaluates the pair
+//    once and adds both shares to shared memory without races, and the
+//    threads left over are whole idle warps, which cost no issue slots.
 //  * Shared memory is laid out per order (padding or an XOR swizzle, and the
 //    order in which lines are dealt to warps) so that the partner loads of
 //    every direction phase are free of bank conflicts where possible.
@@ -165,9 +169,112 @@ __device__ __forceinline__ void line_node(int ell, int p, int& a, int& b, int& c
     else { a = o1; b = o2; c = p; }
 }
 
+// Whether the antipodal pairs of even Nq get their own pass (evaluated once,
+// both shares written to shared memory) or stay in the direction phases
+// (evaluated by both nodes, own share kept).  The pass halves those
+// evaluations, which pays in FP64, where the FP64 pipe is the bound; the FP32
+// kernel is bound by instruction issue and shared-memory traffic, where the
+// pass's extra loads, stores and barriers cost as much as they save.
+template <typename T>
+struct SplitAntipodal {
+    static constexpr bool value = sizeof(T) == 8;
+};
+
+// Values of one node that a pair evaluation reads (metric terms of the
+// current direction only).
+template <typename T>
+struct NodeVals {
+    T rho, u1, u2, u3, b, ib, lr, lb, phi, h, A0, A1, A2;
+};
+
+template <int N, int R, typename T>
+__device__ __forceinline__ NodeVals<T> load_node(const T* __restrict__ sm, int i) {
+    constexpr int FS = Slots<N>::SIZE;
+    NodeVals<T> v;
+    v.rho = sm[F_RHO * FS + i];
+    v.u1 = sm[F_U1 * FS + i];
+    v.u2 = sm[F_U2 * FS + i];
+    v.u3 = sm[F_U3 * FS + i];
+    v.b = sm[F_B * FS + i];
+    v.ib = sm[F_INVB * FS + i];
+    v.lr = sm[F_LNRHO * FS + i];
+    v.lb = sm[F_LNB * FS + i];
+    v.phi = sm[F_PHI * FS + i];
+    v.h = sm[F_H * FS + i];
+    v.A0 = sm[(F_JA0 + 3 * R + 0) * FS + i];
+    v.A1 = sm[(F_JA0 + 3 * R + 1) * FS + i];
+    v.A2 = sm[(F_JA0 + 3 * R + 2) * FS + i];
+    return v;
+}
+
+// One pair (i, m) of a line, evaluated once for both nodes.  c8 = 2 Q_{pp'}/8
+// with p, p' the positions of i and m.  Adds node i's share 2Q_{pp'} (F +
+// G(i,m)) to o0..o4 and returns node m's share 2Q_{p'p} (F + G(m,i)) =
+// -2Q_{pp'} (F + G(m,i)) in t0..t4, G(m,i) = -G(i,m) b_i/b_m (Sec. 4.1).
+// Both shares still need the 1/w scaling of their own node.
+template <typename T>
+__device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T>& M, T c8, T c_g, T& o0, T& o1,
+                                          T& o2, T& o3, T& o4, T& t0, T& t1, T& t2, T& t3, T& t4) {
+    // 2 x averaged metric, 2 x averaged velocity, 4 x {{u}}.n
+    const T A0 = I.A0 + M.A0, A1 = I.A1 + M.A1, A2 = I.A2 + M.A2;
+    const T s1 = I.u1 + M.u1, s2 = I.u2 + M.u2, s3 = I.u3 + M.u3;
+    const T Un = fma(s3, A2, fma(s2, A1, s1 * A0));
+
+    // {{rho}}_log: (rho+ - rho-)/(ln rho+ - ln rho-), or the series when close
+    const T rsum = I.rho + M.rho;
+    const T drho = M.rho - I.rho;
+    const T dlr = M.lr - I.lr;
+    const bool cr = Num<T>::close(dlr);
+    const T rr = Num<T>::rcp(cr ? rsum : dlr);
+    const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
+    const T ur = tr * tr;
+    // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945)
+    const T polr = fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
+    const T rho_ln = cr ? rsum * polr : tr;
+
+    // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
+    const T bsum = I.b + M.b;
+    const T db = M.b - I.b;
+    const T dlb = M.lb - I.lb;
+    const bool cb = Num<T>::close(dlb);
+    const T rb = Num<T>::rcp(cb ? bsum : db * bsum);
+    const T inv_bsum = cb ? rb : db * rb;
+    const T fb = db * inv_bsum;
+    const T ub = fb * fb;
+    // (2/bsum) atanh(f)/f = (2/bsum)(1 + u/3 + u^2/5 + u^3/7)
+    const T polb = fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
+    const T inv_bln = cb ? inv_bsum * polb : dlb * (bsum * rb);
+
+    // flux scalars, already multiplied by 2Q_{pp'}
+    const T cr8 = c8 * rho_ln;
+    const T frh = cr8 * Un;                            // 2Q F_rho / 2
+    const T fr = frh + frh;                            // 2Q F_rho
+    const T gq = cr8 * (bsum * (M.phi - I.phi));       // 2Q rho_ln {{b}} [[phi]] / 2: gravity
+    const T cp = c8 * (rsum * inv_bsum);               // 2Q {{rho}}/(2{{b}}) / 4
+    const T phq = cp + cp;                             // 2Q p_hat / 2
+    const T ss = fma(s3, s3, fma(s2, s2, s1 * s1));
+    const T Kf = fma(c_g, inv_bln, fma(T(0.25), ss, I.h + M.h));
+    const T fE = fma(fr, Kf, cp * Un);                 // 2Q F_E
+    const T Pi = fma(gq, I.ib, phq);  // own: pressure mean + gravity scaled at b_i
+    const T Pm = fma(gq, M.ib, -phq); // partner: -pressure mean + gravity scaled at b_m
+
+    o0 += fr;
+    o1 = fma(A0, Pi, fma(frh, s1, o1));
+    o2 = fma(A1, Pi, fma(frh, s2, o2));
+    o3 = fma(A2, Pi, fma(frh, s3, o3));
+    o4 += fE;
+    t0 = -fr;
+    t1 = fma(A0, Pm, -(frh * s1));
+    t2 = fma(A1, Pm, -(frh * s2));
+    t3 = fma(A2, Pm, -(frh * s3));
+    t4 = -fE;
+}
+
 // One direction phase.  R = 0 (xi), 1 (eta), 2 (zeta).  FINAL = false: add
 // the scaled sum to the shared accumulators; true: add the shared
-// accumulators and store the node's result to global memory.
+// accumulators and store the node's result to global memory.  Offsets
+// d = 1..NEAR; the antipodal offset Nq/2 of even Nq is left to
+// antipodal_phase.
 template <typename T, int N, int R, bool FINAL>
 __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __restrict__ sm, int e_count,
                                                 long long node0, const T (&c8)[Shape<N>::H], T iw) {
@@ -175,6 +282,7 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __res
     using SL = Slots<N>;
     constexpr int NQ = S::NQ;
     constexpr int FS = SL::SIZE;
+    constexpr int NEAR = (S::EVEN && SplitAntipodal<T>::value) ? S::H - 1 : S::H;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -188,106 +296,36 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __res
     int ia, ib, ic;
     line_node<N, R>(ell, p, ia, ib, ic);
     const int i = SL::at(el, ia, ib, ic);
-
-    const T* __restrict__ s_rho = sm + F_RHO * FS;
-    const T* __restrict__ s_u1 = sm + F_U1 * FS;
-    const T* __restrict__ s_u2 = sm + F_U2 * FS;
-    const T* __restrict__ s_u3 = sm + F_U3 * FS;
-    const T* __restrict__ s_b = sm + F_B * FS;
-    const T* __restrict__ s_ib = sm + F_INVB * FS;
-    const T* __restrict__ s_lr = sm + F_LNRHO * FS;
-    const T* __restrict__ s_lb = sm + F_LNB * FS;
-    const T* __restrict__ s_phi = sm + F_PHI * FS;
-    const T* __restrict__ s_h = sm + F_H * FS;
-    const T* __restrict__ s_A0 = sm + (F_JA0 + 3 * R + 0) * FS;
-    const T* __restrict__ s_A1 = sm + (F_JA0 + 3 * R + 1) * FS;
-    const T* __restrict__ s_A2 = sm + (F_JA0 + 3 * R + 2) * FS;
-
-    const T rho_i = s_rho[i], u1_i = s_u1[i], u2_i = s_u2[i], u3_i = s_u3[i];
-    const T b_i = s_b[i], ib_i = s_ib[i], lr_i = s_lr[i], lb_i = s_lb[i];
-    const T phi_i = s_phi[i], h_i = s_h[i];
-    const T A0_i = s_A0[i], A1_i = s_A1[i], A2_i = s_A2[i];
+    const NodeVals<T> I = load_node<N, R>(sm, i);
     const T c_g = a.c_g;
 
     T acc0 = T(0), acc1 = T(0), acc2 = T(0), acc3 = T(0), acc4 = T(0);
 
 #pragma unroll
-    for (int d = 1; d <= S::H; ++d) {
-        const bool both = !(S::EVEN && d == S::H);  // antipodal: own side only
+    for (int d = 1; d <= NEAR; ++d) {
         int pm = p + d;
         if (pm >= NQ) pm -= NQ;
         int ma = ia, mb = ib, mc = ic;
         if (R == 0) ma = pm;
         else if (R == 1) mb = pm;
         else mc = pm;
-        const int m = SL::at(el, ma, mb, mc);
-
-        const T rho_m = s_rho[m], u1_m = s_u1[m], u2_m = s_u2[m], u3_m = s_u3[m];
-        const T b_m = s_b[m];
-
-        // 2 x averaged metric, 2 x averaged velocity, 4 x {{u}}.n
-        const T A0 = A0_i + s_A0[m], A1 = A1_i + s_A1[m], A2 = A2_i + s_A2[m];
-        const T s1 = u1_i + u1_m, s2 = u2_i + u2_m, s3 = u3_i + u3_m;
-        const T Un = fma(s3, A2, fma(s2, A1, s1 * A0));
-
-        // {{rho}}_log: (rho+ - rho-)/(ln rho+ - ln rho-), or the series when close
-        const T rsum = rho_i + rho_m;
-        const T drho = rho_m - rho_i;
-        const T dlr = s_lr[m] - lr_i;
-        const bool cr = Num<T>::close(dlr);
-        const T rr = Num<T>::rcp(cr ? rsum : dlr);
-        const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
-        const T ur = tr * tr;
-        // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945)
-        const T polr = fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
-        const T rho_ln = cr ? rsum * polr : tr;
-
-        // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
-        const T bsum = b_i + b_m;
-        const T db = b_m - b_i;
-        const T dlb = s_lb[m] - lb_i;
-        const bool cb = Num<T>::close(dlb);
-        const T rb = Num<T>::rcp(cb ? bsum : db * bsum);
-        const T inv_bsum = cb ? rb : db * rb;
-        const T fb = db * inv_bsum;
-        const T ub = fb * fb;
-        // (2/bsum) atanh(f)/f = (2/bsum)(1 + u/3 + u^2/5 + u^3/7)
-        const T polb = fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
-        const T inv_bln = cb ? inv_bsum * polb : dlb * (bsum * rb);
-
-        // flux scalars, already multiplied by 2Q_{pp'} (c8 = 2Q/8)
-        const T cr8 = c8[d - 1] * rho_ln;
-        const T frh = cr8 * Un;                                // 2Q F_rho / 2
-        const T fr = frh + frh;                                // 2Q F_rho
-        const T gq = cr8 * (bsum * (s_phi[m] - phi_i));        // 2Q rho_ln {{b}} [[phi]] / 2: gravity
-        const T cp = c8[d - 1] * (rsum * inv_bsum);            // 2Q {{rho}}/(2{{b}}) / 4
-        const T phq = cp + cp;                                 // 2Q p_hat / 2
-        const T ss = fma(s3, s3, fma(s2, s2, s1 * s1));
-        const T Kf = fma(c_g, inv_bln, fma(T(0.25), ss, h_i + s_h[m]));
-        const T fE = fma(fr, Kf, cp * Un);                     // 2Q F_E
-        const T Pi = fma(gq, ib_i, phq);  // own: pressure mean + gravity at b_i
-
-        acc0 += fr;
-        acc1 = fma(A0, Pi, fma(frh, s1, acc1));
-        acc2 = fma(A1, Pi, fma(frh, s2, acc2));
-        acc3 = fma(A2, Pi, fma(frh, s3, acc3));
-        acc4 += fE;
-        if (both) {
-            // partner's share: 2Q_{p'p} (F + G(m,i)) with 2Q_{p'p} = -2Q_{pp'} and
-            // G(m,i) = -G(i,m) b_i/b_m
-            const T Pm = fma(gq, s_ib[m], -phq);
-            const T t1 = fma(A0, Pm, -(frh * s1));
-            const T t2 = fma(A1, Pm, -(frh * s2));
-            const T t3 = fma(A2, Pm, -(frh * s3));
-            int src = p - d;
-            if (src < 0) src += NQ;
-            src += slot * NQ;
-            acc0 -= shfl(fr, src);
-            acc1 += shfl(t1, src);
-            acc2 += shfl(t2, src);
-            acc3 += shfl(t3, src);
-            acc4 -= shfl(fE, src);
-        }
+        const NodeVals<T> M = load_node<N, R>(sm, SL::at(el, ma, mb, mc));
+        T t0, t1, t2, t3, t4;
+        pair_flux<T>(I, M, c8[d - 1], c_g, acc0, acc1, acc2, acc3, acc4, t0, t1, t2, t3, t4);
+        // In-phase antipodal offset (when not split off): both nodes evaluate
+        // the pair and keep their own share -- Fig. 1(b)'s two weight-1/2
+        // evaluations summed per node.
+        if (S::EVEN && d == S::H) continue;
+        // the partner share goes to the lane at position p + d; this lane
+        // receives from the lane at p - d
+        int src = p - d;
+        if (src < 0) src += NQ;
+        src += slot * NQ;
+        acc0 += shfl(t0, src);
+        acc1 += shfl(t1, src);
+        acc2 += shfl(t2, src);
+        acc3 += shfl(t3, src);
+        acc4 += shfl(t4, src);
     }
 
     T* s_acc = sm + F_ACC0 * FS;
@@ -311,6 +349,50 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __res
         o[2 * n + g] = fma(acc2, iw, s_acc[2 * FS + i]);
         o[3 * n + g] = fma(acc3, iw, s_acc[3 * FS + i]);
         o[4 * n + g] = fma(acc4, iw, s_acc[4 * FS + i]);
+    }
+}
+
+// Antipodal pairs (p, p + Nq/2) of every line of direction R, for even Nq.
+// Each node belongs to exactly one such pair per direction, so the pairs are
+// disjoint: one thread evaluates a pair once and adds both shares to the
+// shared accumulators without races (Fig. 1(b)'s two weight-1/2 evaluations
+// become one).  There are Nq^3/2 pairs per element; the surplus threads are
+// whole warps, which issue nothing.
+template <typename T, int N, int R>
+__device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, T* __restrict__ sm, int e_count) {
+    using S = Shape<N>;
+    using SL = Slots<N>;
+    constexpr int NQ = S::NQ;
+    constexpr int H = S::H;
+    constexpr int FS = SL::SIZE;
+    constexpr int PER_EL = S::NL * H;
+    T* s_acc = sm + F_ACC0 * FS;
+    for (int k = threadIdx.x; k < S::EPB * PER_EL; k += S::THREADS) {
+        const int el = k / PER_EL;
+        if (el >= e_count) break;
+        const int kk = k - el * PER_EL;
+        const int p = kk % H;   // position of the lower node; consecutive threads walk a line
+        const int ell = kk / H;
+        int ia, ib, ic, ja, jb, jc;
+        line_node<N, R>(ell, p, ia, ib, ic);
+        line_node<N, R>(ell, p + H, ja, jb, jc);
+        const int i = SL::at(el, ia, ib, ic);
+        const int j = SL::at(el, ja, jb, jc);
+        const NodeVals<T> I = load_node<N, R>(sm, i);
+        const NodeVals<T> M = load_node<N, R>(sm, j);
+        T o0 = T(0), o1 = T(0), o2 = T(0), o3 = T(0), o4 = T(0), t0, t1, t2, t3, t4;
+        pair_flux<T>(I, M, T(0.125) * a.ops.Q2[p * NQ + p + H], a.c_g, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
+        const T iwi = a.ops.invw[p], iwj = a.ops.invw[p + H];
+        s_acc[0 * FS + i] = fma(o0, iwi, s_acc[0 * FS + i]);
+        s_acc[1 * FS + i] = fma(o1, iwi, s_acc[1 * FS + i]);
+        s_acc[2 * FS + i] = fma(o2, iwi, s_acc[2 * FS + i]);
+        s_acc[3 * FS + i] = fma(o3, iwi, s_acc[3 * FS + i]);
+        s_acc[4 * FS + i] = fma(o4, iwi, s_acc[4 * FS + i]);
+        s_acc[0 * FS + j] = fma(t0, iwj, s_acc[0 * FS + j]);
+        s_acc[1 * FS + j] = fma(t1, iwj, s_acc[1 * FS + j]);
+        s_acc[2 * FS + j] = fma(t2, iwj, s_acc[2 * FS + j]);
+        s_acc[3 * FS + j] = fma(t3, iwj, s_acc[3 * FS + j]);
+        s_acc[4 * FS + j] = fma(t4, iwj, s_acc[4 * FS + j]);
     }
 }
 
@@ -420,6 +502,14 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     __syncthreads();
     direction_phase<T, N, 2, false>(a, sm, e_count, node0, c8, iw);
     __syncthreads();
+    if constexpr (S::EVEN && SplitAntipodal<T>::value) {
+        antipodal_phase<T, N, 1>(a, sm, e_count);
+        __syncthreads();
+        antipodal_phase<T, N, 2>(a, sm, e_count);
+        __syncthreads();
+        antipodal_phase<T, N, 0>(a, sm, e_count);
+        __syncthreads();
+    }
     direction_phase<T, N, 0, true>(a, sm, e_count, node0, c8, iw);
 }
 

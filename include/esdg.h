@@ -134,17 +134,19 @@ const char* esdg_last_error(esdg_handle h);
  * Host only; no GPU needed.  Errors: ESDG_ERR_ARG, ESDG_ERR_UNSUPPORTED. */
 int esdg_get_operators(int N, double* nodes, double* weights, double* D);
 
-/* The pair schedule of one coordinate line, as the volume kernel runs it
- * (Sec. 4.1 Eq. 6 and Fig. 1(b), weighted cyclic assignment).  The thread at
- * line position p evaluates the pairs (p, (p + d) mod Nq) for d = 1..H with
- * H = floor(Nq/2).  For d < Nq/2 the pair's result is added to both nodes;
- * when Nq is even, d = Nq/2 joins antipodal nodes, each of which evaluates
- * the pair itself and keeps only its own side (the weight-1/2 evaluations of
- * Fig. 1(b) summed per node).  Writes, for each p and d, the partner index to
- * partner[p*H + d-1] and 2 (both sides) or 1 (own side only) to
- * sides[p*H + d-1].  Returns H through *H_out.  Host only.
- * Errors: ESDG_ERR_ARG, ESDG_ERR_UNSUPPORTED. */
-int esdg_pair_schedule(int N, int* H_out, int* partner, int* sides);
+/* The pair schedule of one coordinate line, as the volume kernel of the given
+ * precision runs it (Sec. 4.1 Eq. 6, cyclic assignment).  Line position p
+ * evaluates the pairs (p, (p + d) mod Nq) for d = 1..H with H = floor(Nq/2),
+ * each pair once, its result added to both nodes.  When Nq is even, d = Nq/2
+ * joins antipodal nodes, the pairs Fig. 1(b) evaluates twice with weight 1/2.
+ * ESDG_FP64: only the lower position p < Nq/2 evaluates such a pair, once, in
+ * a separate pass of the kernel (sides 2; the upper position has partner -1,
+ * sides 0).  ESDG_FP32: both positions evaluate it and keep their own share
+ * (sides 1), which is Fig. 1(b)'s weighting summed per node.  Writes, for each
+ * p and d, the partner index to partner[p*H + d-1] and the number of nodes
+ * that receive the evaluation's result to sides[p*H + d-1].  Returns H
+ * through *H_out.  Host only.  Errors: ESDG_ERR_ARG, ESDG_ERR_UNSUPPORTED. */
+int esdg_pair_schedule(int N, int precision, int* H_out, int* partner, int* sides);
 
 /* Library version as an integer (major*10000 + minor*100 + patch). */
 int esdg_version(void);

@@ -107,33 +107,52 @@ def test_fig1_counts_and_library_schedule_N3(lib):
     # (a) upper triangular: thread i computes j > i
     ut = [sum(1 for j in range(1, 5) if j > i) for i in range(1, 5)]
     assert ut == [int(v) for v in g["upper_triangular_counts"]]
-    # (b) the library's schedule: same count on every lane, antipodal pairs own-side only
-    H, partner, sides = fd.pair_schedule(3)
+    # (b) the weighted cyclic assignment runs Nq/2 offsets on every thread; the
+    # library runs the same offsets, but its antipodal offset -- the pairs
+    # Fig. 1(b) evaluates twice with weight 1/2 -- once per pair
+    # FP32: exactly Fig. 1(b) -- two evaluations per thread, antipodal pairs in both
+    # orientations, each keeping its own share (weight 1/2 per evaluation, summed)
+    H, partner, sides = fd.pair_schedule(3, "fp32")
     assert [H] * 4 == [int(v) for v in g["weighted_cyclic_counts"]]
-    antipodal = sorted({tuple(sorted((p + 1, int(partner[p, d]) + 1)))
-                        for p in range(4) for d in range(H) if sides[p, d] == 1})
+    antipodal = sorted({tuple(sorted((p + 1, int(partner[p, H - 1]) + 1))) for p in range(4)})
+    assert all(sides[p, H - 1] == 1 for p in range(4))
+    assert antipodal == sorted(tuple(map(int, s.split(","))) for s in g["antipodal_pairs"])
+    # FP64: the same antipodal pairs, each evaluated once in a pass of its own
+    H, partner, sides = fd.pair_schedule(3, "fp64")
+    antipodal = sorted(tuple(sorted((p + 1, int(partner[p, H - 1]) + 1))) for p in range(4) if sides[p, H - 1])
     assert antipodal == sorted(tuple(map(int, s.split(","))) for s in g["antipodal_pairs"])
 
 
+@pytest.mark.parametrize("precision", ["fp64", "fp32"])
 @pytest.mark.parametrize("N", range(1, 9))
-def test_library_schedule_covers_each_ordered_pair_once(lib, N):
-    """Each node receives exactly one contribution from every other node of its line."""
-    H, partner, sides = fd.pair_schedule(N)
+def test_library_schedule_covers_each_ordered_pair_once(lib, N, precision):
+    """Each node receives exactly one contribution from every other node of its line.
+    FP64 evaluations per line position are Eq. 6's loop counts N_l - 1; FP32 runs
+    floor(Nq/2) evaluations on every position (Fig. 1(b))."""
+    H, partner, sides = fd.pair_schedule(N, precision)
     Nq = N + 1
     assert H == Nq // 2
     got = np.zeros((Nq, Nq), dtype=int)
+    evals = np.zeros(Nq, dtype=int)
     for p in range(Nq):
         for d in range(H):
+            antipodal = Nq % 2 == 0 and d + 1 == H
+            if sides[p, d] == 0:
+                assert partner[p, d] == -1 and antipodal and p >= H and precision == "fp64"
+                continue
             m = int(partner[p, d])
             assert m == (p + d + 1) % Nq
-            got[p, m] += 1           # own side
+            got[p, m] += 1               # own share
             if sides[p, d] == 2:
-                got[m, p] += 1       # partner side, by shuffle
+                got[m, p] += 1           # partner's share
             else:
-                assert Nq % 2 == 0 and d + 1 == Nq // 2
+                assert sides[p, d] == 1 and antipodal and precision == "fp32"
+            evals[p] += 1
     assert np.array_equal(got, 1 - np.eye(Nq, dtype=int))
-    # load balance: every lane evaluates H pairs (Eq. 6 with the weighted variant)
-    assert partner.shape == (Nq, H)
+    if precision == "fp64":
+        assert list(evals) == [len(_eq6_pairs(N, i)) for i in range(1, Nq + 1)]
+    else:
+        assert list(evals) == [H] * Nq
 
 
 def test_create_rejects_bad_arguments_before_touching_the_gpu(lib):
