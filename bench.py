@@ -476,6 +476,51 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """Opt-in measurement sweeps, one JSON line per point on stdout.
+
+    orders:   the ~6.4e7-node warped cube for N = 2..8 in FP64 and FP32
+              (the order-sweep workloads).
+    elements: throughput against element count for several orders on a
+              warped cube with K = k^3 elements (as in the paper's Fig. 5:
+              single-GPU saturation), reported in GDOF/s and in thousands of
+              element evaluations per second."""
+    import torch
+
+    import workloads as wl
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    points = []
+    if args.sweep == "orders":
+        for N in range(2, 9):
+            for prec in ("fp64", "fp32"):
+                points.append(wl.get_config(f"sweep_N{N}" + ("" if prec == "fp64" else "_fp32")))
+    else:
+        for N in (2, 4, 7, 8):
+            for k in (2, 4, 8, 16, 32, 48, 64):
+                if k ** 3 * (N + 1) ** 3 > 1.1e8:
+                    continue
+                for prec in ("fp64", "fp32"):
+                    points.append(wl.small_config(N, K=(k, k, k), warp=True, precision=prec))
+    for cfg in points:
+        op, q, Ja, phi, out = _setup(cfg, device)
+        # short launches need more of them for a stable mean
+        steps = max(args.steps, 3)
+        total_ms, per = _time_device(op, q, Ja, phi, out, steps, args.warmup, stream, lambda: None)
+        ms = total_ms / steps
+        line = {"sweep": args.sweep, "config": cfg.name, "N": cfg.N, "K": cfg.K, "nodes": cfg.n,
+                "precision": cfg.precision, "ms_per_launch": ms, "GDOF/s": cfg.n / (ms * 1e-3) / 1e9,
+                "kilo_element_evals_per_s": cfg.K / (ms * 1e-3) / 1e3,
+                "algorithmic_TFLOP/s": flops_per_dof(cfg.N) * cfg.n / (ms * 1e-3) / 1e12,
+                "HBM_GB/s": BYTES_PER_DOF[cfg.precision] * cfg.n / (ms * 1e-3) / 1e9}
+        print(json.dumps(line), flush=True)
+        op.close()
+        del q, Ja, phi, out
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -489,6 +534,8 @@ def main():
     ap.add_argument("--no-peaks", action="store_true", help="skip the FMA-throughput peak measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=int, default=256)
+    ap.add_argument("--sweep", choices=["orders", "elements"], default=None,
+                    help="opt-in measurement sweeps (one JSON line per point) instead of the bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -496,6 +543,8 @@ def main():
         args.fp32_workload = None
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 
