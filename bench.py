@@ -61,7 +61,7 @@ def flops_per_dof(N: int, form2d: bool = True) -> float:
     return f
 
 
-BYTES_PER_DOF = {"fp64": 20 * 8, "fp32": 20 * 4}  # 15 planes read + 5 written
+BYTES_PER_DOF = {"fp64": 20 * 8, "fp32": 20 * 4, "fp64ff": 20 * 8}  # 15 planes read + 5 written
 
 NOMINAL_FP64_TFLOPS = 1.25  # GB300 FP64 vector, nominal
 
@@ -387,7 +387,8 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     results = {}
     clocks = None
-    for wname in [args.workload] + ([args.fp32_workload] if args.fp32_workload else []):
+    extra = [w for w in (args.fp32_workload, args.ff_workload) if w]
+    for wname in [args.workload] + extra:
         cfg = wl.get_config(wname)
         op, q, Ja, phi, out = _setup(cfg, device)
         sampler = ClockSampler(local) if (rank == 0 and wname == args.workload) else None
@@ -468,6 +469,24 @@ def run_ours(args):
         if "e2e" in r32:
             line["fp32"]["e2e"] = {k: v for k, v in r32["e2e"].items() if k != "ms_per_step"}
         line["gpu_launches"] += args.steps + (max(3, min(args.steps, 20)) if "e2e" in r32 else 0)
+    if args.ff_workload:
+        rf = results[args.ff_workload]
+        cf = rf["cfg"]
+        # FP64 results from float-float pair arithmetic on the FP32 pipes: the
+        # roofline is the FP32 vector peak (the FP64 pipe only converts and
+        # computes the per-node logarithms)
+        line["fp64ff"] = {
+            "workload": cf.name, "value": rf["gdof"], "unit": "GDOF/s", "ms_per_step": rf["ms"],
+            "dtype": "f64 storage, f32x2 (float-float) arithmetic",
+            "speedup_vs_fp64": main["ms"] / rf["ms"],
+            "roofline": {"bound": "alu", "achieved_fp64_equivalent": rf["achieved_tflops"],
+                         "unit": "TFLOP/s", "fp64_peak": peak64,
+                         "frac_of_fp64_peak": rf["achieved_tflops"] / peak64,
+                         "traffic": recorded_traffic(f"volume_kernel<double, {cf.N}, ff>", cf.name)},
+        }
+        if "e2e" in rf:
+            line["fp64ff"]["e2e"] = {k: v for k, v in rf["e2e"].items() if k != "ms_per_step"}
+        line["gpu_launches"] += args.steps + (max(3, min(args.steps, 20)) if "e2e" in rf else 0)
     line["peaks_measured"] = {"fp64_tflops": fp64_meas, "fp32_tflops": fp32_meas}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(cfg, args.cpu_seconds)
@@ -495,14 +514,14 @@ def run_sweep(args):
     points = []
     if args.sweep == "orders":
         for N in range(2, 9):
-            for prec in ("fp64", "fp32"):
-                points.append(wl.get_config(f"sweep_N{N}" + ("" if prec == "fp64" else "_fp32")))
+            for prec in ("fp64", "fp32", "fp64ff"):
+                points.append(wl.get_config(f"sweep_N{N}" + {"fp64": "", "fp32": "_fp32", "fp64ff": "_ff"}[prec]))
     else:
         for N in (2, 4, 7, 8):
             for k in (2, 4, 8, 16, 32, 48, 64):
                 if k ** 3 * (N + 1) ** 3 > 1.1e8:
                     continue
-                for prec in ("fp64", "fp32"):
+                for prec in ("fp64", "fp32", "fp64ff"):
                     points.append(wl.small_config(N, K=(k, k, k), warp=True, precision=prec))
     for cfg in points:
         op, q, Ja, phi, out = _setup(cfg, device)
@@ -529,6 +548,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="channel_N7")
     ap.add_argument("--fp32-workload", default="channel_N7_fp32")
+    ap.add_argument("--ff-workload", default="channel_N7_ff",
+                    help="FP64 buffers with float-float pair arithmetic, reported under \"fp64ff\"")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-peaks", action="store_true", help="skip the FMA-throughput peak measurement")
@@ -541,6 +562,8 @@ def main():
         args.warmup = 3
     if args.fp32_workload in ("", "none"):
         args.fp32_workload = None
+    if args.ff_workload in ("", "none"):
+        args.ff_workload = None
     if args.impl == "reference":
         run_reference(args)
     elif args.sweep:

@@ -15,13 +15,14 @@ import threading
 import numpy as np
 
 __all__ = [
-    "ESDG_OK", "ESDG_FP64", "ESDG_FP32", "ESDG_FORM_2D", "ESDG_FORM_SKEW", "ESDG_STATUS_NONPHYSICAL",
+    "ESDG_OK", "ESDG_FP64", "ESDG_FP32", "ESDG_FP64_FF", "ESDG_FORM_2D", "ESDG_FORM_SKEW", "ESDG_STATUS_NONPHYSICAL",
     "EsdgError", "library_path", "load_library", "operators", "pair_schedule", "VolumeOperator",
 ]
 
 ESDG_OK = 0
 ESDG_ERR_ARG, ESDG_ERR_UNSUPPORTED, ESDG_ERR_ALIGN, ESDG_ERR_CUDA, ESDG_ERR_STATE = 1, 2, 3, 4, 5
-ESDG_FP64, ESDG_FP32 = 0, 1
+ESDG_FP64, ESDG_FP32, ESDG_FP64_FF = 0, 1, 2
+_PRECISIONS = {"fp64": ESDG_FP64, "fp32": ESDG_FP32, "fp64ff": ESDG_FP64_FF}
 ESDG_FORM_2D, ESDG_FORM_SKEW = 0, 1
 ESDG_STATUS_NONPHYSICAL = 1
 
@@ -53,6 +54,7 @@ _SIGS = {
     # measurement kernels, include/esdg_bench.h
     "esdg_bench_fma": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int, _P, _P]),
     "esdg_selftest_rcp": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, _P, _P, _P]),
+    "esdg_selftest_ff": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, _P, _P, _P, _P]),
 }
 
 
@@ -113,7 +115,7 @@ def pair_schedule(N: int, precision: str = "fp64"):
     H = ctypes.c_int(0)
     partner = np.zeros((N + 1) * ((N + 1) // 2), dtype=np.int32)
     sides = np.zeros_like(partner)
-    prec = ESDG_FP64 if precision == "fp64" else ESDG_FP32
+    prec = _PRECISIONS[precision]
     _check(lib.esdg_pair_schedule(N, prec, ctypes.byref(H), partner.ctypes.data, sides.ctypes.data))
     return H.value, partner.reshape(N + 1, -1), sides.reshape(N + 1, -1)
 
@@ -132,7 +134,8 @@ def _dptr(t):
 class VolumeOperator:
     """A handle for one mesh shape, order and precision.
 
-    precision: "fp64" or "fp32"; form: "2d" (diagonal kept) or "skew".
+    precision: "fp64", "fp32" or "fp64ff" (FP64 buffers, float-float pair
+    arithmetic); form: "2d" (diagonal kept) or "skew".
     Tensors passed in must be contiguous CUDA tensors of the handle's dtype
     (node coordinates are always float64), laid out as described in esdg.h.
     """
@@ -145,8 +148,8 @@ class VolumeOperator:
         self.K = self.Kx * self.Ky * self.Kz
         self.n = self.K * (self.N + 1) ** 3
         self.precision = precision
-        self.dtype = {"fp64": torch.float64, "fp32": torch.float32}[precision]
-        prec = ESDG_FP64 if precision == "fp64" else ESDG_FP32
+        self.dtype = {"fp64": torch.float64, "fp32": torch.float32, "fp64ff": torch.float64}[precision]
+        prec = _PRECISIONS[precision]
         frm = {"2d": ESDG_FORM_2D, "skew": ESDG_FORM_SKEW}[form]
         h = ctypes.c_void_p()
         _check(self.lib.esdg_create(ctypes.byref(h), self.Kx, self.Ky, self.Kz, self.N, prec, frm))

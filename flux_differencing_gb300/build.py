@@ -37,9 +37,9 @@ def _units():
              ("peak_bench", os.path.join(CSRC, "peak_bench.cu"), []),
              ("esdg_noalloc", os.path.join(CSRC, "esdg_noalloc.cu"), [])]
     for n in range(1, 9):
-        for fp64 in (1, 0):
-            units.append((f"volume_{'fp64' if fp64 else 'fp32'}_n{n}", os.path.join(CSRC, "volume_inst.cu"),
-                          [f"-DESDG_INST_N={n}", f"-DESDG_INST_FP64={fp64}"]))
+        for prec, tag in ((0, "fp64"), (1, "fp32"), (2, "fp64ff")):
+            units.append((f"volume_{tag}_n{n}", os.path.join(CSRC, "volume_inst.cu"),
+                          [f"-DESDG_INST_N={n}", f"-DESDG_INST_PREC={prec}"]))
     return units
 
 

@@ -162,6 +162,20 @@ cudaError_t dispatch_fp64(int N, const esdg::VolumeArgs<double>& a, cudaStream_t
     return cudaErrorInvalidValue;
 }
 
+cudaError_t dispatch_fp64ff(int N, const esdg::VolumeArgs<double>& a, cudaStream_t s) {
+    switch (N) {
+        case 1: return esdg::launch_volume_fp64ff_n1(a, s);
+        case 2: return esdg::launch_volume_fp64ff_n2(a, s);
+        case 3: return esdg::launch_volume_fp64ff_n3(a, s);
+        case 4: return esdg::launch_volume_fp64ff_n4(a, s);
+        case 5: return esdg::launch_volume_fp64ff_n5(a, s);
+        case 6: return esdg::launch_volume_fp64ff_n6(a, s);
+        case 7: return esdg::launch_volume_fp64ff_n7(a, s);
+        case 8: return esdg::launch_volume_fp64ff_n8(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t dispatch_fp32(int N, const esdg::VolumeArgs<float>& a, cudaStream_t s) {
     switch (N) {
         case 1: return esdg::launch_volume_fp32_n1(a, s);
@@ -201,15 +215,15 @@ int esdg_get_operators(int N, double* nodes, double* weights, double* D) {
 
 int esdg_pair_schedule(int N, int precision, int* H_out, int* partner, int* sides) {
     if (N < 1 || N > esdg::kMaxN) return fail(nullptr, ESDG_ERR_UNSUPPORTED, "N must be in 1..8");
-    if (precision != ESDG_FP64 && precision != ESDG_FP32)
-        return fail(nullptr, ESDG_ERR_UNSUPPORTED, "precision must be ESDG_FP64 or ESDG_FP32");
+    if (precision != ESDG_FP64 && precision != ESDG_FP32 && precision != ESDG_FP64_FF)
+        return fail(nullptr, ESDG_ERR_UNSUPPORTED, "precision must be ESDG_FP64, ESDG_FP32 or ESDG_FP64_FF");
     if (!H_out || !partner || !sides) return fail(nullptr, ESDG_ERR_ARG, "null output pointer");
     // Must match volume_kernel.cuh: direction_phase evaluates offsets
     // d < Nq/2 on every position.  For even Nq the antipodal offset d = Nq/2
     // is, in FP64 (SplitAntipodal), evaluated once by the lower position in
     // antipodal_phase; in FP32 both positions evaluate it and keep their own
     // share.
-    const bool split = precision == ESDG_FP64;
+    const bool split = precision != ESDG_FP32;
     const int Nq = N + 1, H = Nq / 2;
     *H_out = H;
     for (int p = 0; p < Nq; ++p)
@@ -233,8 +247,8 @@ int esdg_create(esdg_handle* out, long Kx, long Ky, long Kz, int N, int precisio
     if (!out) return fail(nullptr, ESDG_ERR_ARG, "out is NULL");
     *out = nullptr;
     if (N < 1 || N > esdg::kMaxN) return fail(nullptr, ESDG_ERR_UNSUPPORTED, "N must be in 1..8");
-    if (precision != ESDG_FP64 && precision != ESDG_FP32)
-        return fail(nullptr, ESDG_ERR_UNSUPPORTED, "precision must be ESDG_FP64 or ESDG_FP32");
+    if (precision != ESDG_FP64 && precision != ESDG_FP32 && precision != ESDG_FP64_FF)
+        return fail(nullptr, ESDG_ERR_UNSUPPORTED, "precision must be ESDG_FP64, ESDG_FP32 or ESDG_FP64_FF");
     if (form != ESDG_FORM_2D && form != ESDG_FORM_SKEW)
         return fail(nullptr, ESDG_ERR_UNSUPPORTED, "form must be ESDG_FORM_2D or ESDG_FORM_SKEW");
     if (Kx < 1 || Ky < 1 || Kz < 1) return fail(nullptr, ESDG_ERR_ARG, "element counts must be >= 1");
@@ -308,7 +322,7 @@ int esdg_volume_rhs_range(esdg_handle h, long e_begin, long e_count, const void*
         return fail(h, ESDG_ERR_ARG, "element range outside 0..K");
     if (!aligned16(q) || !aligned16(metrics) || !aligned16(phi) || !aligned16(out))
         return fail(h, ESDG_ERR_ALIGN, "device pointers must be 16-byte aligned");
-    const size_t es = h->precision == ESDG_FP64 ? sizeof(double) : sizeof(float);
+    const size_t es = h->precision == ESDG_FP32 ? sizeof(float) : sizeof(double);
     const size_t nb = es * (size_t)h->n;
     if (overlaps(out, 5 * nb, q, 5 * nb) || overlaps(out, 5 * nb, metrics, 9 * nb) || overlaps(out, 5 * nb, phi, nb))
         return fail(h, ESDG_ERR_ARG, "out overlaps an input");
@@ -317,6 +331,8 @@ int esdg_volume_rhs_range(esdg_handle h, long e_begin, long e_count, const void*
     cudaError_t e;
     if (h->precision == ESDG_FP64)
         e = dispatch_fp64(h->N, volume_args<double>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op64), s);
+    else if (h->precision == ESDG_FP64_FF)
+        e = dispatch_fp64ff(h->N, volume_args<double>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op64), s);
     else
         e = dispatch_fp32(h->N, volume_args<float>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op32), s);
     if (e != cudaSuccess) return cuda_fail(h, e, "volume kernel launch");

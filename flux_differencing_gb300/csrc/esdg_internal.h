@@ -39,9 +39,11 @@ struct VolumeArgs {
 };
 
 // Launchers, one per (precision, N); defined in the instantiation units.
-#define ESDG_DECLARE_LAUNCH(N)                                                       \
-    cudaError_t launch_volume_fp64_n##N(const VolumeArgs<double>& a, cudaStream_t s); \
-    cudaError_t launch_volume_fp32_n##N(const VolumeArgs<float>& a, cudaStream_t s);
+// fp64ff: FP64 inputs and outputs, pair arithmetic in float-float.
+#define ESDG_DECLARE_LAUNCH(N)                                                         \
+    cudaError_t launch_volume_fp64_n##N(const VolumeArgs<double>& a, cudaStream_t s);   \
+    cudaError_t launch_volume_fp32_n##N(const VolumeArgs<float>& a, cudaStream_t s);    \
+    cudaError_t launch_volume_fp64ff_n##N(const VolumeArgs<double>& a, cudaStream_t s);
 ESDG_DECLARE_LAUNCH(1)
 ESDG_DECLARE_LAUNCH(2)
 ESDG_DECLARE_LAUNCH(3)

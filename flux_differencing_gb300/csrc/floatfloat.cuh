@@ -1,0 +1,135 @@
+// Float-float arithmetic: a value is the unevaluated sum hi + lo of two FP32
+// numbers with |lo| <= ulp(hi)/2, which carries about 48 significant bits.
+// The building blocks are the error-free transformations of Dekker (1971) and
+// Knuth: two_sum gives a + b = s + e exactly, fast_two_sum does the same when
+// |a| >= |b|, and a fused multiply-add gives the exact rounding error of a
+// product.  Relative error of one operation is a small multiple of 2^-48
+// (the addition is the "sloppy" variant, whose error is bounded relative to
+// the operands rather than to the result -- the same kind of bound as a
+// difference of rounded FP64 inputs).
+//
+// Why: GB300 executes FP32 at 64 times its FP64 rate, so FP64-accurate
+// arithmetic built from FP32 operations on the FP32 pipes can beat native
+// FP64.  The volume kernel uses this type for its pair arithmetic in the
+// ESDG_FP64_FF precision (FP64 inputs and outputs).
+//
+// Range: the FP32 exponent range, about 1e-38 .. 3e38; magnitudes below
+// about 1e-30 lose relative precision in lo.  Values are assumed finite.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace esdg {
+
+struct ff {
+    float hi, lo;
+    ff() = default;
+    __host__ __device__ constexpr ff(float h, float l) : hi(h), lo(l) {}
+    // exact split of a compile-time or host constant; on the device use from_double()
+    __host__ __device__ constexpr explicit ff(double d)
+        : hi(static_cast<float>(d)), lo(static_cast<float>(d - static_cast<double>(static_cast<float>(d)))) {}
+};
+
+__device__ __forceinline__ void ff_two_sum(float a, float b, float& s, float& e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+__device__ __forceinline__ ff ff_fast(float s, float e) {  // renormalise, |s| >= |e|
+    const float h = s + e;
+    return ff(h, e - (h - s));
+}
+
+__device__ __forceinline__ ff operator+(ff x, ff y) {
+    float s, e;
+    ff_two_sum(x.hi, y.hi, s, e);
+    e += x.lo + y.lo;
+    return ff_fast(s, e);
+}
+
+__device__ __forceinline__ ff operator-(ff x) { return ff(-x.hi, -x.lo); }
+__device__ __forceinline__ ff operator-(ff x, ff y) { return x + (-y); }
+
+__device__ __forceinline__ ff operator*(ff x, ff y) {
+    const float p = x.hi * y.hi;
+    float e = __fmaf_rn(x.hi, y.hi, -p);
+    e = __fmaf_rn(x.hi, y.lo, e);
+    e = __fmaf_rn(x.lo, y.hi, e);
+    return ff_fast(p, e);
+}
+
+__device__ __forceinline__ ff& operator+=(ff& x, ff y) { return x = x + y; }
+__device__ __forceinline__ ff& operator-=(ff& x, ff y) { return x = x - y; }
+
+// the float and double overloads stay visible next to the float-float one
+using ::fma;
+
+// x*y + z with the product's rounding error kept and one renormalisation
+__device__ __forceinline__ ff fma(ff x, ff y, ff z) {
+    const float p = x.hi * y.hi;
+    float e = __fmaf_rn(x.hi, y.hi, -p);
+    e = __fmaf_rn(x.hi, y.lo, e);
+    e = __fmaf_rn(x.lo, y.hi, e);
+    float s, t;
+    ff_two_sum(p, z.hi, s, t);
+    t += e + z.lo;
+    return ff_fast(s, t);
+}
+
+// conversions from and to FP64 with the conversion instructions (FP64 pipe)
+__device__ __forceinline__ ff ff_from_double(double d) {
+    const float h = __double2float_rn(d);
+    return ff(h, __double2float_rn(d - static_cast<double>(h)));
+}
+__device__ __forceinline__ double ff_to_double(ff x) {
+    return static_cast<double>(x.hi) + static_cast<double>(x.lo);
+}
+
+// The same conversions on the integer pipe, which keeps them off GB300's
+// narrow FP64 pipe.  Split: hi is d with its significand cut to 24 bits
+// (exact as a float), lo the remaining 29 bits scaled by 2^(E-1075), i.e.
+// hi + lo = d up to the rounding of those 29 bits to a float (< 2^-48 |d|).
+// Zeros are exact; magnitudes outside 2^-74 .. 2^128 take the conversion
+// instructions instead.
+__device__ __forceinline__ ff ff_split(double d) {
+    const unsigned hw = static_cast<unsigned>(__double2hiint(d));
+    const unsigned lw = static_cast<unsigned>(__double2loint(d));
+    const unsigned sign = hw & 0x80000000u;
+    const int ef = static_cast<int>((hw >> 20) & 0x7FFu) - 896;  // float biased exponent
+    if (ef >= 53 && ef <= 254) {
+        const float hi = __uint_as_float(sign | (static_cast<unsigned>(ef) << 23) | ((hw & 0xFFFFFu) << 3) |
+                                         (lw >> 29));
+        const float lo = __uint2float_rn(lw & 0x1FFFFFFFu) * __uint_as_float(sign | (static_cast<unsigned>(ef - 52) << 23));
+        return ff(hi, lo);
+    }
+    if (((hw & 0x7FFFFFFFu) | lw) == 0u) return ff(__uint_as_float(sign), 0.0f);
+    return ff_from_double(d);
+}
+
+// A normal float widened to double by moving its bits (exact); zeros and
+// subnormals go through the conversion instruction.
+__device__ __forceinline__ double ff_widen(float f) {
+    const unsigned b = __float_as_uint(f);
+    const unsigned e = (b >> 23) & 0xFFu;
+    if (e == 0u || e == 0xFFu) return static_cast<double>(f);
+    return __hiloint2double(static_cast<int>((b & 0x80000000u) | ((e + 896u) << 20) | ((b & 0x7FFFFFu) >> 3)),
+                            static_cast<int>(b << 29));
+}
+__device__ __forceinline__ double ff_join(ff x) { return ff_widen(x.hi) + ff_widen(x.lo); }
+
+// 1/x: FP32 hardware estimate r, then one Newton-Raphson step in float-float,
+// r' = r + r (1 - x r); the estimate's error (about 2^-23) squares.
+__device__ __forceinline__ ff ff_rcp(ff x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x.hi));
+    const ff xr = x * ff(r, 0.0f);
+    const ff e = ff(1.0f, 0.0f) - xr;
+    return ff(r, 0.0f) + ff(r, 0.0f) * e;
+}
+
+__device__ __forceinline__ ff shfl_ff(ff v, int src) {
+    return ff(__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src));
+}
+
+}  // namespace esdg

@@ -55,3 +55,29 @@ extern "C" int esdg_selftest_rcp(int fp64, long n, const void* x, void* y, void*
         rcp_selftest<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(x), static_cast<float*>(y), n);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
+
+namespace {
+__global__ void ff_selftest(int op, const double* __restrict__ x, const double* __restrict__ y,
+                            double* __restrict__ out, long n) {
+    const long k = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n) return;
+    const esdg::ff a = esdg::ff_split(x[k]);
+    const esdg::ff b = esdg::ff_split(y[k]);
+    esdg::ff r;
+    switch (op) {
+        case 0: r = a + b; break;
+        case 1: r = a - b; break;
+        case 2: r = a * b; break;
+        case 3: r = esdg::fma(a, b, a); break;
+        default: r = esdg::ff_rcp(a); break;
+    }
+    out[k] = esdg::ff_join(r);
+}
+}  // namespace
+
+extern "C" int esdg_selftest_ff(int op, long n, const double* x, const double* y, double* out, void* stream) {
+    if (n < 1 || op < 0 || op > 4 || !x || !y || !out) return 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ff_selftest<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(op, x, y, out, n);
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}

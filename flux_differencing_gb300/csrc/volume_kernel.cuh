@@ -57,6 +57,7 @@
 #include <stdint.h>
 
 #include "esdg_internal.h"
+#include "floatfloat.cuh"
 
 namespace esdg {
 
@@ -150,23 +151,58 @@ struct Num<float> {
     }
     static __device__ __forceinline__ float log_(float x) { return logf(x); }
 };
+// float-float pair arithmetic (ESDG_FP64_FF): thresholds as in FP64, tested on hi
+template <>
+struct Num<ff> {
+    static __device__ __forceinline__ ff rcp(ff x) { return ff_rcp(x); }
+    static __device__ __forceinline__ bool close(ff d) {
+        return (__float_as_uint(d.hi) & 0x7fffffffu) < 0x3CA3D70Au;  // |d| < 0.02
+    }
+};
+
+template <typename C>
+struct IsFF {
+    static constexpr bool value = false;
+};
+template <>
+struct IsFF<ff> {
+    static constexpr bool value = true;
+};
 
 template <typename T>
 __device__ __forceinline__ T shfl(T v, int src) {
     return __shfl_sync(0xffffffffu, v, src);
 }
+template <>
+__device__ __forceinline__ ff shfl<ff>(ff v, int src) {
+    return shfl_ff(v, src);
+}
 
-// Node (a, b, c) of line `ell` of direction R at line position p.
-template <int N, int R>
-__device__ __forceinline__ void line_node(int ell, int p, int& a, int& b, int& c) {
+// Conversion between the I/O type T of the kernel's arguments and the type C
+// its pair arithmetic runs in (the same type, or float-float for FP64 I/O).
+template <typename T, typename C>
+struct Conv {
+    static __device__ __forceinline__ C in(T x) { return x; }
+    static __device__ __forceinline__ T out(C x) { return x; }
+};
+template <>
+struct Conv<double, ff> {
+    static __device__ __forceinline__ ff in(double x) { return ff_split(x); }
+    static __device__ __forceinline__ double out(ff x) { return ff_join(x); }
+};
+
+// Node (a, b, c) of line `ell` of direction R at line position p.  R may be
+// a compile-time constant (folded) or a runtime value.
+template <int N>
+__device__ __forceinline__ void line_node(int R, int ell, int p, int& a, int& b, int& c) {
     using Lo = Layout<N>;
     constexpr int NQ = N + 1;
-    constexpr int ORD = (R == 0) ? Lo::ORD0 : (R == 1) ? Lo::ORD1 : Lo::ORD2;
-    const int o1 = ORD ? ell / NQ : ell % NQ;
-    const int o2 = ORD ? ell % NQ : ell / NQ;
-    if (R == 0) { a = p; b = o1; c = o2; }
-    else if (R == 1) { a = o1; b = p; c = o2; }
-    else { a = o1; b = o2; c = p; }
+    const int ord = (R == 0) ? Lo::ORD0 : (R == 1) ? Lo::ORD1 : Lo::ORD2;
+    const int o1 = ord ? ell / NQ : ell % NQ;
+    const int o2 = ord ? ell % NQ : ell / NQ;
+    a = (R == 0) ? p : o1;
+    b = (R == 1) ? p : (R == 0) ? o1 : o2;
+    c = (R == 2) ? p : o2;
 }
 
 // Whether the antipodal pairs of even Nq get their own pass (evaluated once,
@@ -187,8 +223,8 @@ struct NodeVals {
     T rho, u1, u2, u3, b, ib, lr, lb, phi, h, A0, A1, A2;
 };
 
-template <int N, int R, typename T>
-__device__ __forceinline__ NodeVals<T> load_node(const T* __restrict__ sm, int i) {
+template <int N, typename T>
+__device__ __forceinline__ NodeVals<T> load_node(const T* __restrict__ sm, int i, int R) {
     constexpr int FS = Slots<N>::SIZE;
     NodeVals<T> v;
     v.rho = sm[F_RHO * FS + i];
@@ -275,47 +311,45 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
 // accumulators and store the node's result to global memory.  Offsets
 // d = 1..NEAR; the antipodal offset Nq/2 of even Nq is left to
 // antipodal_phase.
-template <typename T, int N, int R, bool FINAL>
-__device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __restrict__ sm, int e_count,
-                                                long long node0, const T (&c8)[Shape<N>::H], T iw) {
+template <typename T, typename C, int N, bool FINAL>
+__device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count,
+                                                long long node0, const C (&c8)[Shape<N>::H], C iw, C c_g,
+                                                int vwarp, int R) {
     using S = Shape<N>;
     using SL = Slots<N>;
     constexpr int NQ = S::NQ;
     constexpr int FS = SL::SIZE;
-    constexpr int NEAR = (S::EVEN && SplitAntipodal<T>::value) ? S::H - 1 : S::H;
+    constexpr int NEAR = (S::EVEN && SplitAntipodal<C>::value) ? S::H - 1 : S::H;
 
     const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
     const int slot = lane / NQ;
     const int p = lane - slot * NQ;
-    int L = warp * S::LPW + slot;
+    int L = vwarp * S::LPW + slot;
     const bool valid = (slot < S::LPW) && (L < S::LINES) && (L / S::NL < e_count);
     if (!valid) L = 0;  // compute on element 0's first line, discard
     const int el = L / S::NL;
     const int ell = L - el * S::NL;
     int ia, ib, ic;
-    line_node<N, R>(ell, p, ia, ib, ic);
+    line_node<N>(R, ell, p, ia, ib, ic);
     const int i = SL::at(el, ia, ib, ic);
-    const NodeVals<T> I = load_node<N, R>(sm, i);
-    const T c_g = a.c_g;
+    const NodeVals<C> I = load_node<N>(sm, i, R);
 
-    T acc0 = T(0), acc1 = T(0), acc2 = T(0), acc3 = T(0), acc4 = T(0);
+    C acc0 = C(0.0), acc1 = C(0.0), acc2 = C(0.0), acc3 = C(0.0), acc4 = C(0.0);
 
-#pragma unroll
-    for (int d = 1; d <= NEAR; ++d) {
+    auto offset = [&](int d, C c8d) {
         int pm = p + d;
         if (pm >= NQ) pm -= NQ;
         int ma = ia, mb = ib, mc = ic;
         if (R == 0) ma = pm;
         else if (R == 1) mb = pm;
         else mc = pm;
-        const NodeVals<T> M = load_node<N, R>(sm, SL::at(el, ma, mb, mc));
-        T t0, t1, t2, t3, t4;
-        pair_flux<T>(I, M, c8[d - 1], c_g, acc0, acc1, acc2, acc3, acc4, t0, t1, t2, t3, t4);
+        const NodeVals<C> M = load_node<N>(sm, SL::at(el, ma, mb, mc), R);
+        C t0, t1, t2, t3, t4;
+        pair_flux<C>(I, M, c8d, c_g, acc0, acc1, acc2, acc3, acc4, t0, t1, t2, t3, t4);
         // In-phase antipodal offset (when not split off): both nodes evaluate
         // the pair and keep their own share -- Fig. 1(b)'s two weight-1/2
         // evaluations summed per node.
-        if (S::EVEN && d == S::H) continue;
+        if (S::EVEN && d == S::H) return;
         // the partner share goes to the lane at position p + d; this lane
         // receives from the lane at p - d
         int src = p - d;
@@ -326,9 +360,22 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __res
         acc2 += shfl(t2, src);
         acc3 += shfl(t3, src);
         acc4 += shfl(t4, src);
+    };
+    if constexpr (IsFF<C>::value) {
+        // one copy of the (long) float-float pair evaluation: no unrolling,
+        // the offset's 2Q/8 read from the operator table each time
+#pragma unroll 1
+        for (int d = 1; d <= NEAR; ++d) {
+            int pm = p + d;
+            if (pm >= NQ) pm -= NQ;
+            offset(d, Conv<T, C>::in(T(0.125) * a.ops.Q2[p * NQ + pm]));
+        }
+    } else {
+#pragma unroll
+        for (int d = 1; d <= NEAR; ++d) offset(d, c8[d - 1]);
     }
 
-    T* s_acc = sm + F_ACC0 * FS;
+    C* s_acc = sm + F_ACC0 * FS;
     if (!FINAL) {
         if (valid) {
             s_acc[0 * FS + i] = fma(acc0, iw, s_acc[0 * FS + i]);
@@ -340,16 +387,43 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __res
     } else if (valid) {
         // xi phase: lines of a warp are consecutive (b, c) rows, so the block-
         // linear node L*Nq + p is contiguous across lanes: coalesced stores
-        static_assert(R != 0 || Layout<N>::ORD0 == 0, "xi lines must be dealt b-fastest");
+        static_assert(Layout<N>::ORD0 == 0, "xi lines must be dealt b-fastest");
         const long long g = node0 + (long long)L * NQ + p;
         T* __restrict__ o = a.out;
         const long long n = a.n;
-        o[0 * n + g] = fma(acc0, iw, s_acc[0 * FS + i]);
-        o[1 * n + g] = fma(acc1, iw, s_acc[1 * FS + i]);
-        o[2 * n + g] = fma(acc2, iw, s_acc[2 * FS + i]);
-        o[3 * n + g] = fma(acc3, iw, s_acc[3 * FS + i]);
-        o[4 * n + g] = fma(acc4, iw, s_acc[4 * FS + i]);
+        o[0 * n + g] = Conv<T, C>::out(fma(acc0, iw, s_acc[0 * FS + i]));
+        o[1 * n + g] = Conv<T, C>::out(fma(acc1, iw, s_acc[1 * FS + i]));
+        o[2 * n + g] = Conv<T, C>::out(fma(acc2, iw, s_acc[2 * FS + i]));
+        o[3 * n + g] = Conv<T, C>::out(fma(acc3, iw, s_acc[3 * FS + i]));
+        o[4 * n + g] = Conv<T, C>::out(fma(acc4, iw, s_acc[4 * FS + i]));
     }
+}
+
+// Threads per CTA and line sets per warp.  A warp walks REPS sets of lines in
+// each direction phase: 2 for float-float, which gives 256-thread CTAs at
+// N = 7 and lets two CTAs share an SM, so that one CTA's load phase (FP64
+// logarithms and divisions) overlaps the other's pair arithmetic on the FP32
+// pipes; 1 otherwise.
+template <int N, typename C>
+struct Launch {
+    using S = Shape<N>;
+    static constexpr int REPS = IsFF<C>::value ? 2 : 1;
+    static constexpr int VWARPS = (S::LINES + S::LPW - 1) / S::LPW;  // warps' worth of lines
+    static constexpr int WARPS = (VWARPS + REPS - 1) / REPS;
+    static constexpr int THREADS = WARPS * 32;
+    static constexpr size_t SMEM = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
+    static constexpr bool TWO_FIT = 2 * SMEM <= 227 * 1024;
+    static constexpr int MIN_BLOCKS = ((sizeof(C) == 4 && THREADS <= 512) || IsFF<C>::value) && TWO_FIT ? 2 : 1;
+};
+
+template <typename T, typename C, int N, int R, bool FINAL>
+__device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count,
+                                                long long node0, const C (&c8)[Shape<N>::H], C iw, C c_g) {
+    using LA = Launch<N, C>;
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int rep = 0; rep < LA::REPS; ++rep)
+        direction_lines<T, C, N, FINAL>(a, sm, e_count, node0, c8, iw, c_g, warp + rep * LA::WARPS, R);
 }
 
 // Antipodal pairs (p, p + Nq/2) of every line of direction R, for even Nq.
@@ -358,31 +432,32 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, T* __res
 // shared accumulators without races (Fig. 1(b)'s two weight-1/2 evaluations
 // become one).  There are Nq^3/2 pairs per element; the surplus threads are
 // whole warps, which issue nothing.
-template <typename T, int N, int R>
-__device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, T* __restrict__ sm, int e_count) {
+template <typename T, typename C, int N>
+__device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count, C c_g, int R) {
     using S = Shape<N>;
     using SL = Slots<N>;
     constexpr int NQ = S::NQ;
     constexpr int H = S::H;
     constexpr int FS = SL::SIZE;
     constexpr int PER_EL = S::NL * H;
-    T* s_acc = sm + F_ACC0 * FS;
-    for (int k = threadIdx.x; k < S::EPB * PER_EL; k += S::THREADS) {
+    C* s_acc = sm + F_ACC0 * FS;
+    for (int k = threadIdx.x; k < S::EPB * PER_EL; k += Launch<N, C>::THREADS) {
         const int el = k / PER_EL;
         if (el >= e_count) break;
         const int kk = k - el * PER_EL;
         const int p = kk % H;   // position of the lower node; consecutive threads walk a line
         const int ell = kk / H;
         int ia, ib, ic, ja, jb, jc;
-        line_node<N, R>(ell, p, ia, ib, ic);
-        line_node<N, R>(ell, p + H, ja, jb, jc);
+        line_node<N>(R, ell, p, ia, ib, ic);
+        line_node<N>(R, ell, p + H, ja, jb, jc);
         const int i = SL::at(el, ia, ib, ic);
         const int j = SL::at(el, ja, jb, jc);
-        const NodeVals<T> I = load_node<N, R>(sm, i);
-        const NodeVals<T> M = load_node<N, R>(sm, j);
-        T o0 = T(0), o1 = T(0), o2 = T(0), o3 = T(0), o4 = T(0), t0, t1, t2, t3, t4;
-        pair_flux<T>(I, M, T(0.125) * a.ops.Q2[p * NQ + p + H], a.c_g, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
-        const T iwi = a.ops.invw[p], iwj = a.ops.invw[p + H];
+        const NodeVals<C> I = load_node<N>(sm, i, R);
+        const NodeVals<C> M = load_node<N>(sm, j, R);
+        C o0 = C(0.0), o1 = C(0.0), o2 = C(0.0), o3 = C(0.0), o4 = C(0.0), t0, t1, t2, t3, t4;
+        const C c8 = Conv<T, C>::in(T(0.125) * a.ops.Q2[p * NQ + p + H]);
+        pair_flux<C>(I, M, c8, c_g, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
+        const C iwi = Conv<T, C>::in(a.ops.invw[p]), iwj = Conv<T, C>::in(a.ops.invw[p + H]);
         s_acc[0 * FS + i] = fma(o0, iwi, s_acc[0 * FS + i]);
         s_acc[1 * FS + i] = fma(o1, iwi, s_acc[1 * FS + i]);
         s_acc[2 * FS + i] = fma(o2, iwi, s_acc[2 * FS + i]);
@@ -396,8 +471,8 @@ __device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, T* __res
     }
 }
 
-template <typename T, int N>
-__global__ void __launch_bounds__(Shape<N>::THREADS, (sizeof(T) == 4 && Shape<N>::THREADS <= 512) ? 2 : 1)
+template <typename T, int N, typename C>
+__global__ void __launch_bounds__(Launch<N, C>::THREADS, Launch<N, C>::MIN_BLOCKS)
 volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     using S = Shape<N>;
     using SL = Slots<N>;
@@ -405,7 +480,8 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     constexpr int NP3 = S::NP3;
     constexpr int FS = SL::SIZE;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    T* sm = reinterpret_cast<T*>(smem_raw);
+    C* sm = reinterpret_cast<C*>(smem_raw);
+    using CV = Conv<T, C>;
 
     const long long e0 = a.e_begin + (long long)blockIdx.x * S::EPB;
     const long long rem = a.e_end - e0;
@@ -414,7 +490,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
 
     // ---- load phase: one node per thread, coalesced plane reads -> derived values
     bool bad = false;
-    for (int t = threadIdx.x; t < S::NODES; t += S::THREADS) {
+    for (int t = threadIdx.x; t < S::NODES; t += Launch<N, C>::THREADS) {
         const int el = t / NP3;
         const int nd = t - el * NP3;
         const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
@@ -446,18 +522,18 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         const T b = T(0.5) * rho * ipr;
         const T ib = T(2) * pr * irho;
         const T h = fma(T(-0.25), uu, T(0.5) * phi);
-        sm[F_RHO * FS + sl] = rho;
-        sm[F_U1 * FS + sl] = u1;
-        sm[F_U2 * FS + sl] = u2;
-        sm[F_U3 * FS + sl] = u3;
-        sm[F_B * FS + sl] = b;
-        sm[F_INVB * FS + sl] = ib;
-        sm[F_LNRHO * FS + sl] = Num<T>::log_(rho);
-        sm[F_LNB * FS + sl] = Num<T>::log_(b);
-        sm[F_PHI * FS + sl] = phi;
-        sm[F_H * FS + sl] = h;
+        sm[F_RHO * FS + sl] = CV::in(rho);
+        sm[F_U1 * FS + sl] = CV::in(u1);
+        sm[F_U2 * FS + sl] = CV::in(u2);
+        sm[F_U3 * FS + sl] = CV::in(u3);
+        sm[F_B * FS + sl] = CV::in(b);
+        sm[F_INVB * FS + sl] = CV::in(ib);
+        sm[F_LNRHO * FS + sl] = CV::in(Num<T>::log_(rho));
+        sm[F_LNB * FS + sl] = CV::in(Num<T>::log_(b));
+        sm[F_PHI * FS + sl] = CV::in(phi);
+        sm[F_H * FS + sl] = CV::in(h);
 #pragma unroll
-        for (int k = 0; k < 9; ++k) sm[(F_JA0 + k) * FS + sl] = ja[k];
+        for (int k = 0; k < 9; ++k) sm[(F_JA0 + k) * FS + sl] = CV::in(ja[k]);
 
         // diagonal pairs of the 2D form: sum_r 2 D_{a_r a_r} Ja^r(i) . f(q_i), nonzero
         // only where a_r is 0 or N; f is the physical flux of Eq. 1
@@ -477,57 +553,91 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             f3 = fma(rU, u3, pp * V2);
             f4 = rU * fma(a.c_h, ib, T(2) * (phi - h));  // (E + p) U
         }
-        sm[(F_ACC0 + 0) * FS + sl] = f0;
-        sm[(F_ACC0 + 1) * FS + sl] = f1;
-        sm[(F_ACC0 + 2) * FS + sl] = f2;
-        sm[(F_ACC0 + 3) * FS + sl] = f3;
-        sm[(F_ACC0 + 4) * FS + sl] = f4;
+        sm[(F_ACC0 + 0) * FS + sl] = CV::in(f0);
+        sm[(F_ACC0 + 1) * FS + sl] = CV::in(f1);
+        sm[(F_ACC0 + 2) * FS + sl] = CV::in(f2);
+        sm[(F_ACC0 + 3) * FS + sl] = CV::in(f3);
+        sm[(F_ACC0 + 4) * FS + sl] = CV::in(f4);
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(a.status, 1u);
 
     // lane constants: 2Q_{p,p+d}/8 for every offset and 1/w_p
     const int lane = threadIdx.x & 31;
     const int p = lane - (lane / NQ) * NQ;
-    T c8[S::H];
+    C c8[S::H];
 #pragma unroll
     for (int d = 1; d <= S::H; ++d) {
         int pm = p + d;
         if (pm >= NQ) pm -= NQ;
-        c8[d - 1] = T(0.125) * a.ops.Q2[p * NQ + pm];
+        c8[d - 1] = CV::in(T(0.125) * a.ops.Q2[p * NQ + pm]);
     }
-    const T iw = a.ops.invw[p];
+    const C iw = CV::in(a.ops.invw[p]);
+    const C c_g = CV::in(a.c_g);
     __syncthreads();
 
-    direction_phase<T, N, 1, false>(a, sm, e_count, node0, c8, iw);
-    __syncthreads();
-    direction_phase<T, N, 2, false>(a, sm, e_count, node0, c8, iw);
-    __syncthreads();
-    if constexpr (S::EVEN && SplitAntipodal<T>::value) {
-        antipodal_phase<T, N, 1>(a, sm, e_count);
+    if constexpr (IsFF<C>::value) {
+        // Float-float: one pair evaluation is ~850 instructions, so the
+        // phases run as loops over a runtime direction (not unrolled) to keep
+        // a single copy of each loop body in the instruction cache; a last
+        // pass stores the sums.
+        using LA = Launch<N, C>;
+        const int warp = threadIdx.x >> 5;
+#pragma unroll 1
+        for (int k = 0; k < 3; ++k) {
+            const int R = (k == 0) ? 1 : (k == 1) ? 2 : 0;
+#pragma unroll 1
+            for (int rep = 0; rep < LA::REPS; ++rep)
+                direction_lines<T, C, N, false>(a, sm, e_count, node0, c8, iw, c_g, warp + rep * LA::WARPS, R);
+            __syncthreads();
+        }
+        if constexpr (S::EVEN && SplitAntipodal<C>::value) {
+#pragma unroll 1
+            for (int k = 0; k < 3; ++k) {
+                antipodal_phase<T, C, N>(a, sm, e_count, c_g, (k == 0) ? 1 : (k == 1) ? 2 : 0);
+                __syncthreads();
+            }
+        }
+        const C* s_acc = sm + F_ACC0 * FS;
+        for (int t = threadIdx.x; t < e_count * NP3; t += LA::THREADS) {
+            const int el = t / NP3;
+            const int nd = t - el * NP3;
+            const int sl = SL::at(el, nd % NQ, (nd / NQ) % NQ, nd / (NQ * NQ));
+            const long long g = node0 + t;
+#pragma unroll
+            for (int v = 0; v < 5; ++v) a.out[v * a.n + g] = CV::out(s_acc[v * FS + sl]);
+        }
+    } else {
+        direction_phase<T, C, N, 1, false>(a, sm, e_count, node0, c8, iw, c_g);
         __syncthreads();
-        antipodal_phase<T, N, 2>(a, sm, e_count);
+        direction_phase<T, C, N, 2, false>(a, sm, e_count, node0, c8, iw, c_g);
         __syncthreads();
-        antipodal_phase<T, N, 0>(a, sm, e_count);
-        __syncthreads();
+        if constexpr (S::EVEN && SplitAntipodal<C>::value) {
+            antipodal_phase<T, C, N>(a, sm, e_count, c_g, 1);
+            __syncthreads();
+            antipodal_phase<T, C, N>(a, sm, e_count, c_g, 2);
+            __syncthreads();
+            antipodal_phase<T, C, N>(a, sm, e_count, c_g, 0);
+            __syncthreads();
+        }
+        direction_phase<T, C, N, 0, true>(a, sm, e_count, node0, c8, iw, c_g);
     }
-    direction_phase<T, N, 0, true>(a, sm, e_count, node0, c8, iw);
 }
 
-template <typename T, int N>
+template <typename T, int N, typename C = T>
 cudaError_t launch_volume(const VolumeArgs<T>& a, cudaStream_t s) {
     using S = Shape<N>;
     const long long K = a.e_end - a.e_begin;
     if (K <= 0) return cudaSuccess;
-    const size_t smem = sizeof(T) * (size_t)F_COUNT * Slots<N>::SIZE;
+    const size_t smem = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
     static bool attr_done = false;  // per instantiation; set once per process
     if (!attr_done) {
-        cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N>,
+        cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N, C>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         attr_done = true;
     }
     const long long blocks = (K + S::EPB - 1) / S::EPB;
-    volume_kernel<T, N><<<(unsigned)blocks, S::THREADS, smem, s>>>(a);
+    volume_kernel<T, N, C><<<(unsigned)blocks, Launch<N, C>::THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 

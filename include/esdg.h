@@ -56,7 +56,14 @@ enum {
     ESDG_ERR_STATE = 5         /* call not valid in the handle's state */
 };
 
-enum { ESDG_FP64 = 0, ESDG_FP32 = 1 };
+/* ESDG_FP64_FF: FP64 inputs, metrics and outputs (element type double, the
+ * same buffers as ESDG_FP64); the per-node precompute runs in FP64 and the
+ * pair arithmetic in float-float (each value the unevaluated sum of two
+ * floats, about 48 significant bits) on the FP32 pipes, which on GB300 run at
+ * 64 times the FP64 rate.  Results agree with the FP64 oracle within the same
+ * 1e-11 tolerance as ESDG_FP64.  Values must stay inside the FP32 exponent
+ * range (about 1e-30 .. 1e38 in magnitude for full accuracy). */
+enum { ESDG_FP64 = 0, ESDG_FP32 = 1, ESDG_FP64_FF = 2 };
 
 /* ESDG_FORM_2D keeps the diagonal pairs m == i (the strong form whose
  * diagonal contributes 2 D_ii Ja^r(i).f(q_i) at the two end nodes of a line);

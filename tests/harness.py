@@ -14,7 +14,7 @@ import torch
 import flux_differencing_gb300 as fd
 import oracle
 
-TOL = {"fp64": 1e-11, "fp32": 1e-4}
+TOL = {"fp64": 1e-11, "fp32": 1e-4, "fp64ff": 1e-11}
 
 
 def to_device(g, device="cuda"):

@@ -56,3 +56,48 @@ def test_rcp_fp32_relative_error(cuda_ok):
     ref = 1.0 / x.astype(np.float64)
     rel = np.abs(y - ref) / np.abs(ref)
     assert rel.max() < 2.0 ** -22, rel.max()
+
+
+def _ff(lib, op, x, y):
+    xd = torch.from_numpy(x).to("cuda")
+    yd = torch.from_numpy(y).to("cuda")
+    od = torch.empty_like(xd)
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.esdg_selftest_ff(op, xd.numel(), ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(yd.data_ptr()),
+                                ctypes.c_void_p(od.data_ptr()), s) == 0
+    torch.cuda.synchronize()
+    return od.cpu().numpy()
+
+
+@pytest.mark.parametrize("op", [0, 1, 2, 3, 4])
+def test_float_float_arithmetic_error_bounds(cuda_ok, op):
+    """Float-float add, sub, mul, fma and reciprocal against FP64.
+
+    Each input is first split into hi + lo (about 2^-48 relative), so the
+    bounds are relative to the operands: |err| <= 2^-44 (|x| + |y|) for sums,
+    2^-44 |x y| for products and 2^-43 |1/x| for the Newton reciprocal."""
+    lib = fd.load_library(build_if_missing=True)
+    rng = np.random.default_rng(30 + op)
+    n = 1 << 18
+    x = np.exp(rng.uniform(np.log(1e-25), np.log(1e25), n)) * rng.choice([-1.0, 1.0], n)
+    y = np.exp(rng.uniform(np.log(1e-25), np.log(1e25), n)) * rng.choice([-1.0, 1.0], n)
+    # nearly equal operands exercise cancellation in sums and differences
+    y[: n // 4] = -x[: n // 4] * (1 + rng.uniform(-1e-9, 1e-9, n // 4))
+    got = _ff(lib, op, x, y)
+    with np.errstate(over="ignore"):
+        if op == 0:
+            ref, scale = x + y, np.abs(x) + np.abs(y)
+        elif op == 1:
+            ref, scale = x - y, np.abs(x) + np.abs(y)
+        elif op == 2:
+            ref, scale = x * y, np.abs(x * y)
+        elif op == 3:
+            ref, scale = x * y + x, np.abs(x * y) + np.abs(x)
+        else:
+            ref, scale = 1.0 / x, np.abs(1.0 / x)
+    ok = np.isfinite(ref) & (scale < 1e37) & (scale > 1e-28)
+    rel = np.abs(got[ok] - ref[ok]) / scale[ok]
+    bound = 2.0 ** -43 if op == 4 else 2.0 ** -44
+    assert rel.max() < bound, (op, rel.max())
+    # and the pair arithmetic really carries more than FP32 precision
+    assert np.median(rel) < 2.0 ** -40

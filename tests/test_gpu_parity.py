@@ -29,8 +29,11 @@ SMALL = [(N, K) for N in range(1, 9) for K in [(2, 2, 1), (3, 2, 3)]] + [(1, (17
                                                                           (5, (3, 1, 1))]
 
 
+PRECISIONS = ["fp64", "fp32", "fp64ff"]
+
+
 @pytest.mark.parametrize("N,K", SMALL)
-@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+@pytest.mark.parametrize("precision", PRECISIONS)
 def test_small_meshes(N, K, precision):
     cfg = wl.small_config(N, K=K, warp=True, precision=precision)
     g = wl.generate(cfg)
@@ -42,7 +45,7 @@ def test_small_meshes(N, K, precision):
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8])
-@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+@pytest.mark.parametrize("precision", PRECISIONS)
 def test_skew_form(N, precision):
     cfg = wl.small_config(N, K=(2, 3, 1), warp=True, precision=precision)
     g = wl.generate(cfg)
@@ -88,7 +91,7 @@ def test_metrics_parity(N):
 # ----------------------------------------------------------------------------
 # the named workloads at full size
 
-@pytest.mark.parametrize("name", ["tiny_box_N3", "bubble_N4", "channel_N7", "channel_N7_fp32"])
+@pytest.mark.parametrize("name", ["tiny_box_N3", "bubble_N4", "channel_N7", "channel_N7_fp32", "channel_N7_ff"])
 def test_named_workload_full(name):
     cfg = wl.get_config(name)
     g = wl.generate(cfg, device="cuda")
@@ -102,10 +105,10 @@ def test_named_workload_full(name):
 
 
 @pytest.mark.parametrize("N", range(2, 9))
-@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+@pytest.mark.parametrize("precision", PRECISIONS)
 def test_order_sweep_sampled(N, precision):
     """About 6.4e7 nodes per order; the oracle checks a sample of whole elements."""
-    name = f"sweep_N{N}" + ("" if precision == "fp64" else "_fp32")
+    name = f"sweep_N{N}" + {"fp64": "", "fp32": "_fp32", "fp64ff": "_ff"}[precision]
     cfg = wl.get_config(name)
     g = wl.generate(cfg, device="cuda")
     got_full, op, _ = hz.run_gpu(cfg, g)
@@ -125,7 +128,7 @@ def test_order_sweep_sampled(N, precision):
 # ----------------------------------------------------------------------------
 # properties: determinism, element-range split, status flag, errors
 
-@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+@pytest.mark.parametrize("precision", PRECISIONS)
 def test_bitwise_deterministic_and_range_split(precision):
     cfg = wl.small_config(5, K=(5, 3, 2), warp=True, precision=precision)
     g = hz.to_device(wl.generate(cfg))

@@ -123,7 +123,7 @@ def test_fig1_counts_and_library_schedule_N3(lib):
     assert antipodal == sorted(tuple(map(int, s.split(","))) for s in g["antipodal_pairs"])
 
 
-@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+@pytest.mark.parametrize("precision", ["fp64", "fp32", "fp64ff"])
 @pytest.mark.parametrize("N", range(1, 9))
 def test_library_schedule_covers_each_ordered_pair_once(lib, N, precision):
     """Each node receives exactly one contribution from every other node of its line.
@@ -138,7 +138,7 @@ def test_library_schedule_covers_each_ordered_pair_once(lib, N, precision):
         for d in range(H):
             antipodal = Nq % 2 == 0 and d + 1 == H
             if sides[p, d] == 0:
-                assert partner[p, d] == -1 and antipodal and p >= H and precision == "fp64"
+                assert partner[p, d] == -1 and antipodal and p >= H and precision != "fp32"
                 continue
             m = int(partner[p, d])
             assert m == (p + d + 1) % Nq
@@ -149,7 +149,7 @@ def test_library_schedule_covers_each_ordered_pair_once(lib, N, precision):
                 assert sides[p, d] == 1 and antipodal and precision == "fp32"
             evals[p] += 1
     assert np.array_equal(got, 1 - np.eye(Nq, dtype=int))
-    if precision == "fp64":
+    if precision != "fp32":
         assert list(evals) == [len(_eq6_pairs(N, i)) for i in range(1, Nq + 1)]
     else:
         assert list(evals) == [H] * Nq
@@ -160,7 +160,7 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(lib):
     assert lib.esdg_create(None, 1, 1, 1, 3, 0, 0) == fd.ESDG_ERR_ARG
     assert lib.esdg_create(ctypes.byref(h), 1, 1, 1, 0, 0, 0) == fd.ESDG_ERR_UNSUPPORTED
     assert lib.esdg_create(ctypes.byref(h), 1, 1, 1, 9, 0, 0) == fd.ESDG_ERR_UNSUPPORTED
-    assert lib.esdg_create(ctypes.byref(h), 1, 1, 1, 3, 2, 0) == fd.ESDG_ERR_UNSUPPORTED
+    assert lib.esdg_create(ctypes.byref(h), 1, 1, 1, 3, 3, 0) == fd.ESDG_ERR_UNSUPPORTED
     assert lib.esdg_create(ctypes.byref(h), 1, 1, 1, 3, 0, 5) == fd.ESDG_ERR_UNSUPPORTED
     assert lib.esdg_create(ctypes.byref(h), 0, 1, 1, 3, 0, 0) == fd.ESDG_ERR_ARG
     assert lib.esdg_create(ctypes.byref(h), 1 << 20, 1 << 20, 1, 3, 0, 0) == fd.ESDG_ERR_ARG

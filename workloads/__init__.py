@@ -104,10 +104,13 @@ def _make_configs() -> dict:
     cfgs["channel_N7_fp32"] = dataclasses.replace(
         cfgs["channel_N7"], name="channel_N7_fp32", precision="fp32",
         description="channel_N7 with FP32 state, metrics and geopotential")
+    cfgs["channel_N7_ff"] = dataclasses.replace(
+        cfgs["channel_N7"], name="channel_N7_ff", precision="fp64ff",
+        description="channel_N7 with FP64 buffers and float-float pair arithmetic")
     for N in range(2, 9):
         k = _sweep_K(N)
-        for prec in ("fp64", "fp32"):
-            nm = f"sweep_N{N}" + ("" if prec == "fp64" else "_fp32")
+        for prec in ("fp64", "fp32", "fp64ff"):
+            nm = f"sweep_N{N}" + {"fp64": "", "fp32": "_fp32", "fp64ff": "_ff"}[prec]
             cfgs[nm] = Config(
                 nm, N, k, k, k, prec, "random", (1.0e4, 1.0e4, 1.0e4), True, _seed(5, N),
                 f"warped periodic 10 km cube, {k}^3 elements, N={N}, about 6.4e7 nodes")
