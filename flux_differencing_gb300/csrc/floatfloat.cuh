@@ -128,6 +128,48 @@ __device__ __forceinline__ ff ff_rcp(ff x) {
     return ff(r, 0.0f) + ff(r, 0.0f) * e;
 }
 
+// Natural logarithm of a positive float-float x, with no FP64 instruction.
+// Argument reduction by the binary exponent of x.hi: x = 2^e m with m in
+// [sqrt(1/2), sqrt(2)), then ln m = 2 atanh(s) = 2 s (1 + s^2/3 + s^4/5 + ...)
+// with s = (m - 1)/(m + 1), |s| <= 0.1716 (the series of Abramowitz & Stegun
+// 4.1.27).  Terms up to s^8/9 are summed in float-float, the rest (each below
+// 2^-26 relative) in FP32; ln 2 enters as a three-part constant so that e ln 2
+// is exact to float-float precision.  Absolute error about 2^-48 |ln x|.
+__device__ __forceinline__ ff ff_log(ff x) {
+    const unsigned hb = __float_as_uint(x.hi);
+    int e = static_cast<int>((hb >> 23) & 0xFFu) - 127;
+    unsigned mb = (hb & 0x007FFFFFu) | 0x3F800000u;  // m in [1, 2)
+    if (mb > 0x3FB504F3u) {                           // m > sqrt(2): use m/2, e + 1
+        mb -= 0x00800000u;
+        e += 1;
+    }
+    const float scale = __uint_as_float(static_cast<unsigned>(127 - e) << 23);  // 2^-e, exact
+    const ff m(__uint_as_float(mb), x.lo * scale);
+    const ff num = m + ff(-1.0f, 0.0f);
+    const ff den = m + ff(1.0f, 0.0f);
+    const ff s = num * ff_rcp(den);
+    const ff z = s * s;
+    // tail 1/11 + z/13 + z^2/15 + z^3/17 + z^4/19 in FP32
+    const float zf = z.hi;
+    float tail = __fmaf_rn(zf, 1.0f / 19.0f, 1.0f / 17.0f);
+    tail = __fmaf_rn(zf, tail, 1.0f / 15.0f);
+    tail = __fmaf_rn(zf, tail, 1.0f / 13.0f);
+    tail = __fmaf_rn(zf, tail, 1.0f / 11.0f);
+    ff P = fma(z, ff(tail, 0.0f), ff(1.0 / 9.0));
+    P = fma(z, P, ff(1.0 / 7.0));
+    P = fma(z, P, ff(1.0 / 5.0));
+    P = fma(z, P, ff(1.0 / 3.0));
+    P = fma(z, P, ff(1.0f, 0.0f));
+    const ff lnm = (s + s) * P;
+    // e ln 2 with ln 2 = L1 + L2 + L3: L1 has 16 significant bits, so e L1 is exact
+    const float ef = static_cast<float>(e);
+    constexpr float L1 = 0.693145751953125f;      // 0x3F317200, 45426 * 2^-16
+    constexpr float L2 = 1.428606765330187e-06f;  // ln 2 - L1 rounded to float
+    constexpr float L3 = 5.497923148104107e-14f;  // ln 2 - L1 - L2 rounded to float
+    const ff eln2 = ff(ef * L1, 0.0f) + (ff(ef, 0.0f) * ff(L2, L3));
+    return eln2 + lnm;
+}
+
 __device__ __forceinline__ ff shfl_ff(ff v, int src) {
     return ff(__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src));
 }

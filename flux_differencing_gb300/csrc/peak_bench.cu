@@ -69,14 +69,15 @@ __global__ void ff_selftest(int op, const double* __restrict__ x, const double* 
         case 1: r = a - b; break;
         case 2: r = a * b; break;
         case 3: r = esdg::fma(a, b, a); break;
-        default: r = esdg::ff_rcp(a); break;
+        case 4: r = esdg::ff_rcp(a); break;
+        default: r = esdg::ff_log(a); break;
     }
     out[k] = esdg::ff_join(r);
 }
 }  // namespace
 
 extern "C" int esdg_selftest_ff(int op, long n, const double* x, const double* y, double* out, void* stream) {
-    if (n < 1 || op < 0 || op > 4 || !x || !y || !out) return 1;
+    if (n < 1 || op < 0 || op > 5 || !x || !y || !out) return 1;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ff_selftest<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(op, x, y, out, n);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;

@@ -56,6 +56,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "esdg_internal.h"
 #include "floatfloat.cuh"
 
@@ -158,7 +160,13 @@ struct Num<ff> {
     static __device__ __forceinline__ bool close(ff d) {
         return (__float_as_uint(d.hi) & 0x7fffffffu) < 0x3CA3D70Au;  // |d| < 0.02
     }
+    static __device__ __forceinline__ ff log_(ff x) { return ff_log(x); }
 };
+
+// x > 0 (false for NaN), for the non-physical-state check
+__device__ __forceinline__ bool positive(double x) { return x > 0.0; }
+__device__ __forceinline__ bool positive(float x) { return x > 0.0f; }
+__device__ __forceinline__ bool positive(ff x) { return x.hi > 0.0f; }
 
 template <typename C>
 struct IsFF {
@@ -488,76 +496,87 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     const int e_count = rem < S::EPB ? (int)rem : S::EPB;
     const long long node0 = e0 * NP3;
 
-    // ---- load phase: one node per thread, coalesced plane reads -> derived values
+    // ---- load phase: one node per thread, coalesced plane reads -> derived values.
+    // The per-node arithmetic runs in P: the I/O type for FP64 and FP32, and
+    // float-float for FP64_FF, where the doubles are split on the integer
+    // pipe and the divisions and logarithms stay off the FP64 pipe.
+    using P = typename std::conditional<IsFF<C>::value, ff, T>::type;
+    using PV = Conv<T, P>;
     bool bad = false;
     for (int t = threadIdx.x; t < S::NODES; t += Launch<N, C>::THREADS) {
         const int el = t / NP3;
         const int nd = t - el * NP3;
         const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
         const int sl = SL::at(el, na, nb, nc);
-        T rho = T(1), m1 = T(0), m2 = T(0), m3 = T(0), E = T(1), phi = T(0);
-        T ja[9];
+        T rho_t = T(1), m1_t = T(0), m2_t = T(0), m3_t = T(0), E_t = T(1), phi_t = T(0);
+        T ja_t[9];
 #pragma unroll
-        for (int k = 0; k < 9; ++k) ja[k] = T(0);
+        for (int k = 0; k < 9; ++k) ja_t[k] = T(0);
         const bool real = t < e_count * NP3;
         if (real) {
             const long long g = node0 + t;
             const long long n = a.n;
-            rho = __ldg(a.q + g);
-            m1 = __ldg(a.q + n + g);
-            m2 = __ldg(a.q + 2 * n + g);
-            m3 = __ldg(a.q + 3 * n + g);
-            E = __ldg(a.q + 4 * n + g);
-            phi = __ldg(a.phi + g);
+            rho_t = __ldg(a.q + g);
+            m1_t = __ldg(a.q + n + g);
+            m2_t = __ldg(a.q + 2 * n + g);
+            m3_t = __ldg(a.q + 3 * n + g);
+            E_t = __ldg(a.q + 4 * n + g);
+            phi_t = __ldg(a.phi + g);
 #pragma unroll
-            for (int k = 0; k < 9; ++k) ja[k] = __ldg(a.Ja + k * n + g);
+            for (int k = 0; k < 9; ++k) ja_t[k] = __ldg(a.Ja + k * n + g);
         }
-        const T irho = Num<T>::rcp(rho);
-        const T u1 = m1 * irho, u2 = m2 * irho, u3 = m3 * irho;
-        const T uu = fma(u3, u3, fma(u2, u2, u1 * u1));
-        T pr = a.gm1 * (E - rho * fma(T(0.5), uu, phi));
-        if (!real) pr = T(0.5) * a.gm1;  // padding node: finite values, never stored
-        bad |= !(rho > T(0)) || !(pr > T(0));
-        const T ipr = Num<T>::rcp(pr);
-        const T b = T(0.5) * rho * ipr;
-        const T ib = T(2) * pr * irho;
-        const T h = fma(T(-0.25), uu, T(0.5) * phi);
-        sm[F_RHO * FS + sl] = CV::in(rho);
-        sm[F_U1 * FS + sl] = CV::in(u1);
-        sm[F_U2 * FS + sl] = CV::in(u2);
-        sm[F_U3 * FS + sl] = CV::in(u3);
-        sm[F_B * FS + sl] = CV::in(b);
-        sm[F_INVB * FS + sl] = CV::in(ib);
-        sm[F_LNRHO * FS + sl] = CV::in(Num<T>::log_(rho));
-        sm[F_LNB * FS + sl] = CV::in(Num<T>::log_(b));
-        sm[F_PHI * FS + sl] = CV::in(phi);
-        sm[F_H * FS + sl] = CV::in(h);
+        const P rho = PV::in(rho_t), m1 = PV::in(m1_t), m2 = PV::in(m2_t), m3 = PV::in(m3_t);
+        const P E = PV::in(E_t), phi = PV::in(phi_t);
+        P ja[9];
 #pragma unroll
-        for (int k = 0; k < 9; ++k) sm[(F_JA0 + k) * FS + sl] = CV::in(ja[k]);
+        for (int k = 0; k < 9; ++k) ja[k] = PV::in(ja_t[k]);
+        const P gm1 = PV::in(a.gm1);
+        const P irho = Num<P>::rcp(rho);
+        const P u1 = m1 * irho, u2 = m2 * irho, u3 = m3 * irho;
+        const P uu = fma(u3, u3, fma(u2, u2, u1 * u1));
+        P pr = gm1 * (E - rho * fma(P(0.5), uu, phi));
+        if (!real) pr = P(0.5) * gm1;  // padding node: finite values, never stored
+        bad |= !positive(rho) || !positive(pr);
+        const P ipr = Num<P>::rcp(pr);
+        const P b = P(0.5) * rho * ipr;
+        const P ib = P(2.0) * pr * irho;
+        const P h = fma(P(-0.25), uu, P(0.5) * phi);
+        sm[F_RHO * FS + sl] = rho;
+        sm[F_U1 * FS + sl] = u1;
+        sm[F_U2 * FS + sl] = u2;
+        sm[F_U3 * FS + sl] = u3;
+        sm[F_B * FS + sl] = b;
+        sm[F_INVB * FS + sl] = ib;
+        sm[F_LNRHO * FS + sl] = Num<P>::log_(rho);
+        sm[F_LNB * FS + sl] = Num<P>::log_(b);
+        sm[F_PHI * FS + sl] = phi;
+        sm[F_H * FS + sl] = h;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) sm[(F_JA0 + k) * FS + sl] = ja[k];
 
         // diagonal pairs of the 2D form: sum_r 2 D_{a_r a_r} Ja^r(i) . f(q_i), nonzero
         // only where a_r is 0 or N; f is the physical flux of Eq. 1
-        T f0 = T(0), f1 = T(0), f2 = T(0), f3 = T(0), f4 = T(0);
+        P f0 = P(0.0), f1 = P(0.0), f2 = P(0.0), f3 = P(0.0), f4 = P(0.0);
         if (a.form == 0) {
-            const T dA = (na == 0 || na == N) ? a.ops.Q2[na * NQ + na] * a.ops.invw[na] : T(0);
-            const T dB = (nb == 0 || nb == N) ? a.ops.Q2[nb * NQ + nb] * a.ops.invw[nb] : T(0);
-            const T dC = (nc == 0 || nc == N) ? a.ops.Q2[nc * NQ + nc] * a.ops.invw[nc] : T(0);
-            const T V0 = fma(dC, ja[6], fma(dB, ja[3], dA * ja[0]));
-            const T V1 = fma(dC, ja[7], fma(dB, ja[4], dA * ja[1]));
-            const T V2 = fma(dC, ja[8], fma(dB, ja[5], dA * ja[2]));
-            const T rU = rho * fma(u3, V2, fma(u2, V1, u1 * V0));
-            const T pp = T(0.5) * rho * ib;
+            const P dA = PV::in((na == 0 || na == N) ? a.ops.Q2[na * NQ + na] * a.ops.invw[na] : T(0));
+            const P dB = PV::in((nb == 0 || nb == N) ? a.ops.Q2[nb * NQ + nb] * a.ops.invw[nb] : T(0));
+            const P dC = PV::in((nc == 0 || nc == N) ? a.ops.Q2[nc * NQ + nc] * a.ops.invw[nc] : T(0));
+            const P V0 = fma(dC, ja[6], fma(dB, ja[3], dA * ja[0]));
+            const P V1 = fma(dC, ja[7], fma(dB, ja[4], dA * ja[1]));
+            const P V2 = fma(dC, ja[8], fma(dB, ja[5], dA * ja[2]));
+            const P rU = rho * fma(u3, V2, fma(u2, V1, u1 * V0));
+            const P pp = P(0.5) * rho * ib;
             f0 = rU;
             f1 = fma(rU, u1, pp * V0);
             f2 = fma(rU, u2, pp * V1);
             f3 = fma(rU, u3, pp * V2);
-            f4 = rU * fma(a.c_h, ib, T(2) * (phi - h));  // (E + p) U
+            f4 = rU * fma(PV::in(a.c_h), ib, P(2.0) * (phi - h));  // (E + p) U
         }
-        sm[(F_ACC0 + 0) * FS + sl] = CV::in(f0);
-        sm[(F_ACC0 + 1) * FS + sl] = CV::in(f1);
-        sm[(F_ACC0 + 2) * FS + sl] = CV::in(f2);
-        sm[(F_ACC0 + 3) * FS + sl] = CV::in(f3);
-        sm[(F_ACC0 + 4) * FS + sl] = CV::in(f4);
+        sm[(F_ACC0 + 0) * FS + sl] = f0;
+        sm[(F_ACC0 + 1) * FS + sl] = f1;
+        sm[(F_ACC0 + 2) * FS + sl] = f2;
+        sm[(F_ACC0 + 3) * FS + sl] = f3;
+        sm[(F_ACC0 + 4) * FS + sl] = f4;
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(a.status, 1u);
 

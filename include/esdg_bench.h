@@ -33,10 +33,11 @@ int esdg_selftest_rcp(int fp64, long n, const void* x, void* y, void* stream);
 
 /* Self-test of the float-float arithmetic of ESDG_FP64_FF: x[k] and y[k]
  * (doubles) are split into float-float, combined by operation `op`
- * (0: x + y, 1: x - y, 2: x * y, 3: x * y + x, 4: 1 / x) in float-float, and
+ * (0: x + y, 1: x - y, 2: x * y, 3: x * y + x, 4: 1 / x, 5: log x for x > 0) in
+ * float-float, and
  * the result is written back as a double to out[k], so the test suite can
  * compare it with FP64.  x, y, out: device arrays of n doubles (y unused for
- * op 4).  Asynchronous on `stream`.  Returns 0, 1 (bad argument) or 4 (CUDA
+ * ops 4 and 5).  Asynchronous on `stream`.  Returns 0, 1 (bad argument) or 4 (CUDA
  * launch error). */
 int esdg_selftest_ff(int op, long n, const double* x, const double* y, double* out, void* stream);
 

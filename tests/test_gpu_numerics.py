@@ -101,3 +101,18 @@ def test_float_float_arithmetic_error_bounds(cuda_ok, op):
     assert rel.max() < bound, (op, rel.max())
     # and the pair arithmetic really carries more than FP32 precision
     assert np.median(rel) < 2.0 ** -40
+
+
+def test_float_float_log(cuda_ok):
+    """Float-float logarithm (no FP64 instruction) against FP64 log: absolute error
+    <= 2^-46 max(1, |ln x|) on positive inputs across 1e-20 .. 1e20."""
+    lib = fd.load_library(build_if_missing=True)
+    rng = np.random.default_rng(41)
+    n = 1 << 18
+    x = np.exp(rng.uniform(np.log(1e-20), np.log(1e20), n))
+    x[:1000] = 1.0 + rng.uniform(-1e-6, 1e-6, 1000)   # near 1: ln x tiny
+    x[1000:2000] = np.sqrt(2.0) * (1.0 + rng.uniform(-1e-7, 1e-7, 1000))  # reduction boundary
+    got = _ff(lib, 5, x, x)
+    ref = np.log(x)
+    err = np.abs(got - ref) / np.maximum(1.0, np.abs(ref))
+    assert err.max() < 2.0 ** -46, err.max()
