@@ -67,7 +67,7 @@ NOMINAL_FP64_TFLOPS = 1.25  # GB300 FP64 vector, nominal
 
 
 KERNEL_SOURCES = [os.path.join(ROOT, "flux_differencing_gb300", "csrc", f)
-                  for f in ("volume_kernel.cuh", "esdg_internal.h", "volume_inst.cu")]
+                  for f in ("volume_kernel.cuh", "floatfloat.cuh", "esdg_internal.h", "volume_inst.cu")]
 
 
 def kernel_source_sha() -> str:

@@ -13,6 +13,12 @@
 // FP64.  The volume kernel uses this type for its pair arithmetic in the
 // ESDG_FP64_FF precision (FP64 inputs and outputs).
 //
+// The algorithms are written for a component type F (float here).  Carrying
+// two float-float values per thread in Blackwell's packed FP32 registers
+// (add/mul/fma on float2) was measured slower for the volume kernel: the
+// packed instructions hold the FMA pipe twice as long, so they only save
+// issue slots, and the doubled register footprint spills.
+//
 // Range: the FP32 exponent range, about 1e-38 .. 3e38; magnitudes below
 // about 1e-30 lose relative precision in lo.  Values are assumed finite.
 #pragma once
@@ -21,62 +27,100 @@
 
 namespace esdg {
 
-struct ff {
-    float hi, lo;
-    ff() = default;
-    __host__ __device__ constexpr ff(float h, float l) : hi(h), lo(l) {}
-    // exact split of a compile-time or host constant; on the device use from_double()
-    __host__ __device__ constexpr explicit ff(double d)
+// the float and double overloads stay visible next to the ones below
+using ::fma;
+
+__device__ __forceinline__ float sel(bool c, float a, float b) { return c ? a : b; }
+__device__ __forceinline__ double sel(bool c, double a, double b) { return c ? a : b; }
+
+// hardware reciprocal estimate
+__device__ __forceinline__ float rcp_estimate(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// float-float over component type F
+template <typename F>
+struct ffv {
+    F hi, lo;
+    ffv() = default;
+    __host__ __device__ constexpr ffv(F h, F l) : hi(h), lo(l) {}
+    // exact split of a compile-time or host constant
+    __host__ __device__ constexpr explicit ffv(double d)
         : hi(static_cast<float>(d)), lo(static_cast<float>(d - static_cast<double>(static_cast<float>(d)))) {}
 };
+using ff = ffv<float>;
 
-__device__ __forceinline__ void ff_two_sum(float a, float b, float& s, float& e) {
+__device__ __forceinline__ float ffma_(float a, float b, float c) { return __fmaf_rn(a, b, c); }
+
+template <typename F>
+__device__ __forceinline__ void ff_two_sum(F a, F b, F& s, F& e) {
     s = a + b;
-    const float bb = s - a;
+    const F bb = s - a;
     e = (a - (s - bb)) + (b - bb);
 }
 
-__device__ __forceinline__ ff ff_fast(float s, float e) {  // renormalise, |s| >= |e|
-    const float h = s + e;
-    return ff(h, e - (h - s));
+template <typename F>
+__device__ __forceinline__ ffv<F> ff_fast(F s, F e) {  // renormalise, |s| >= |e|
+    const F h = s + e;
+    return ffv<F>(h, e - (h - s));
 }
 
-__device__ __forceinline__ ff operator+(ff x, ff y) {
-    float s, e;
+template <typename F>
+__device__ __forceinline__ ffv<F> operator+(ffv<F> x, ffv<F> y) {
+    F s, e;
     ff_two_sum(x.hi, y.hi, s, e);
-    e += x.lo + y.lo;
+    e = e + (x.lo + y.lo);
     return ff_fast(s, e);
 }
 
-__device__ __forceinline__ ff operator-(ff x) { return ff(-x.hi, -x.lo); }
-__device__ __forceinline__ ff operator-(ff x, ff y) { return x + (-y); }
+template <typename F>
+__device__ __forceinline__ ffv<F> operator-(ffv<F> x) { return ffv<F>(-x.hi, -x.lo); }
+template <typename F>
+__device__ __forceinline__ ffv<F> operator-(ffv<F> x, ffv<F> y) { return x + (-y); }
 
-__device__ __forceinline__ ff operator*(ff x, ff y) {
-    const float p = x.hi * y.hi;
-    float e = __fmaf_rn(x.hi, y.hi, -p);
-    e = __fmaf_rn(x.hi, y.lo, e);
-    e = __fmaf_rn(x.lo, y.hi, e);
+template <typename F>
+__device__ __forceinline__ ffv<F> operator*(ffv<F> x, ffv<F> y) {
+    const F p = x.hi * y.hi;
+    F e = ffma_(x.hi, y.hi, -p);
+    e = ffma_(x.hi, y.lo, e);
+    e = ffma_(x.lo, y.hi, e);
     return ff_fast(p, e);
 }
 
-__device__ __forceinline__ ff& operator+=(ff& x, ff y) { return x = x + y; }
-__device__ __forceinline__ ff& operator-=(ff& x, ff y) { return x = x - y; }
-
-// the float and double overloads stay visible next to the float-float one
-using ::fma;
+template <typename F>
+__device__ __forceinline__ ffv<F>& operator+=(ffv<F>& x, ffv<F> y) { return x = x + y; }
+template <typename F>
+__device__ __forceinline__ ffv<F>& operator-=(ffv<F>& x, ffv<F> y) { return x = x - y; }
 
 // x*y + z with the product's rounding error kept and one renormalisation
-__device__ __forceinline__ ff fma(ff x, ff y, ff z) {
-    const float p = x.hi * y.hi;
-    float e = __fmaf_rn(x.hi, y.hi, -p);
-    e = __fmaf_rn(x.hi, y.lo, e);
-    e = __fmaf_rn(x.lo, y.hi, e);
-    float s, t;
+template <typename F>
+__device__ __forceinline__ ffv<F> fma(ffv<F> x, ffv<F> y, ffv<F> z) {
+    const F p = x.hi * y.hi;
+    F e = ffma_(x.hi, y.hi, -p);
+    e = ffma_(x.hi, y.lo, e);
+    e = ffma_(x.lo, y.hi, e);
+    F s, t;
     ff_two_sum(p, z.hi, s, t);
-    t += e + z.lo;
+    t = t + (e + z.lo);
     return ff_fast(s, t);
 }
 
+// 1/x: FP32 estimate r of x.hi, then one Newton-Raphson step in float-float,
+// r' = r + r (1 - x r); the estimate's error (about 2^-23) squares.
+template <typename F>
+__device__ __forceinline__ ffv<F> ff_rcp(ffv<F> x) {
+    const F r = rcp_estimate(x.hi);
+    const F z = F(0.0f);
+    const ffv<F> e = ffv<F>(F(1.0f), z) - x * ffv<F>(r, z);
+    return ffv<F>(r, z) + ffv<F>(r, z) * e;
+}
+
+__device__ __forceinline__ ff sel(bool c, ff a, ff b) { return c ? a : b; }
+
+// ---------------------------------------------------------------------------
 // conversions from and to FP64 with the conversion instructions (FP64 pipe)
 __device__ __forceinline__ ff ff_from_double(double d) {
     const float h = __double2float_rn(d);
@@ -118,23 +162,14 @@ __device__ __forceinline__ double ff_widen(float f) {
 }
 __device__ __forceinline__ double ff_join(ff x) { return ff_widen(x.hi) + ff_widen(x.lo); }
 
-// 1/x: FP32 hardware estimate r, then one Newton-Raphson step in float-float,
-// r' = r + r (1 - x r); the estimate's error (about 2^-23) squares.
-__device__ __forceinline__ ff ff_rcp(ff x) {
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x.hi));
-    const ff xr = x * ff(r, 0.0f);
-    const ff e = ff(1.0f, 0.0f) - xr;
-    return ff(r, 0.0f) + ff(r, 0.0f) * e;
-}
-
 // Natural logarithm of a positive float-float x, with no FP64 instruction.
 // Argument reduction by the binary exponent of x.hi: x = 2^e m with m in
 // [sqrt(1/2), sqrt(2)), then ln m = 2 atanh(s) = 2 s (1 + s^2/3 + s^4/5 + ...)
 // with s = (m - 1)/(m + 1), |s| <= 0.1716 (the series of Abramowitz & Stegun
 // 4.1.27).  Terms up to s^8/9 are summed in float-float, the rest (each below
 // 2^-26 relative) in FP32; ln 2 enters as a three-part constant so that e ln 2
-// is exact to float-float precision.  Absolute error about 2^-48 |ln x|.
+// is exact to float-float precision.  Absolute error about 2^-48 |ln x|;
+// x.hi must be a positive normal float.
 __device__ __forceinline__ ff ff_log(ff x) {
     const unsigned hb = __float_as_uint(x.hi);
     int e = static_cast<int>((hb >> 23) & 0xFFu) - 127;

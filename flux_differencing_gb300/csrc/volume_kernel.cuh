@@ -162,7 +162,6 @@ struct Num<ff> {
     }
     static __device__ __forceinline__ ff log_(ff x) { return ff_log(x); }
 };
-
 // x > 0 (false for NaN), for the non-physical-state check
 __device__ __forceinline__ bool positive(double x) { return x > 0.0; }
 __device__ __forceinline__ bool positive(float x) { return x > 0.0f; }
@@ -268,26 +267,26 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
     const T rsum = I.rho + M.rho;
     const T drho = M.rho - I.rho;
     const T dlr = M.lr - I.lr;
-    const bool cr = Num<T>::close(dlr);
-    const T rr = Num<T>::rcp(cr ? rsum : dlr);
+    const auto cr = Num<T>::close(dlr);
+    const T rr = Num<T>::rcp(sel(cr, rsum, dlr));
     const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
     const T ur = tr * tr;
     // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945)
     const T polr = fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
-    const T rho_ln = cr ? rsum * polr : tr;
+    const T rho_ln = sel(cr, rsum * polr, tr);
 
     // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
     const T bsum = I.b + M.b;
     const T db = M.b - I.b;
     const T dlb = M.lb - I.lb;
-    const bool cb = Num<T>::close(dlb);
-    const T rb = Num<T>::rcp(cb ? bsum : db * bsum);
-    const T inv_bsum = cb ? rb : db * rb;
+    const auto cb = Num<T>::close(dlb);
+    const T rb = Num<T>::rcp(sel(cb, bsum, db * bsum));
+    const T inv_bsum = sel(cb, rb, db * rb);
     const T fb = db * inv_bsum;
     const T ub = fb * fb;
     // (2/bsum) atanh(f)/f = (2/bsum)(1 + u/3 + u^2/5 + u^3/7)
     const T polb = fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
-    const T inv_bln = cb ? inv_bsum * polb : dlb * (bsum * rb);
+    const T inv_bln = sel(cb, inv_bsum * polb, dlb * (bsum * rb));
 
     // flux scalars, already multiplied by 2Q_{pp'}
     const T cr8 = c8 * rho_ln;
@@ -409,13 +408,14 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
 
 // Threads per CTA and line sets per warp.  A warp walks REPS sets of lines in
 // each direction phase: 2 for float-float, which gives 256-thread CTAs at
-// N = 7 and lets two CTAs share an SM, so that one CTA's load phase (FP64
-// logarithms and divisions) overlaps the other's pair arithmetic on the FP32
-// pipes; 1 otherwise.
+// N = 7 and lets two CTAs share an SM, so that one CTA's load phase overlaps
+// the other's pair arithmetic; 1 otherwise
 template <int N, typename C>
 struct Launch {
     using S = Shape<N>;
-    static constexpr int REPS = IsFF<C>::value ? 2 : 1;
+    // (also 2 at N = 8, where one element's 81 lines would need 864 threads,
+    // which caps registers at 72 per thread and made the FP64 kernel spill)
+    static constexpr int REPS = (IsFF<C>::value || N == 8) ? 2 : 1;
     static constexpr int VWARPS = (S::LINES + S::LPW - 1) / S::LPW;  // warps' worth of lines
     static constexpr int WARPS = (VWARPS + REPS - 1) / REPS;
     static constexpr int THREADS = WARPS * 32;
