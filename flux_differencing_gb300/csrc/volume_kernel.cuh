@@ -407,21 +407,27 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
 }
 
 // Threads per CTA and line sets per warp.  A warp walks REPS sets of lines in
-// each direction phase: 2 for float-float, which gives 256-thread CTAs at
-// N = 7 and lets two CTAs share an SM, so that one CTA's load phase overlaps
-// the other's pair arithmetic; 1 otherwise
+// each direction phase.  Two sets halve the CTA, so that two CTAs can share an
+// SM and one CTA's load phase overlaps the other's pair arithmetic.  Chosen
+// per precision and order from the order sweep (about 6.4e7 nodes per order)
+// on GB300:
+//  * float-float: always 2 (256-thread CTAs at N = 7);
+//  * FP64: 2 only at N = 7 (111.2 -> 109.4 ms); at N = 2, 4, 5, 6, 8 the
+//    halved CTA was 2-7 % slower;
+//  * FP32: 2 only at N = 8, where one element's 81 lines would otherwise need
+//    an 864-thread CTA (5.05 -> 5.00 ms).
 template <int N, typename C>
 struct Launch {
     using S = Shape<N>;
-    // (also 2 at N = 8, where one element's 81 lines would need 864 threads,
-    // which caps registers at 72 per thread and made the FP64 kernel spill)
-    static constexpr int REPS = (IsFF<C>::value || N == 8) ? 2 : 1;
     static constexpr int VWARPS = (S::LINES + S::LPW - 1) / S::LPW;  // warps' worth of lines
+    static constexpr bool FP64 = sizeof(C) == 8;
+    static constexpr int REPS = IsFF<C>::value ? 2 : FP64 ? (N == 7 ? 2 : 1) : (N == 8 ? 2 : 1);
     static constexpr int WARPS = (VWARPS + REPS - 1) / REPS;
     static constexpr int THREADS = WARPS * 32;
     static constexpr size_t SMEM = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
     static constexpr bool TWO_FIT = 2 * SMEM <= 227 * 1024;
-    static constexpr int MIN_BLOCKS = ((sizeof(C) == 4 && THREADS <= 512) || IsFF<C>::value) && TWO_FIT ? 2 : 1;
+    static constexpr int MIN_BLOCKS =
+        ((sizeof(C) == 4 && THREADS <= 512) || IsFF<C>::value || (FP64 && REPS == 2)) && TWO_FIT ? 2 : 1;
 };
 
 template <typename T, typename C, int N, int R, bool FINAL>
@@ -429,7 +435,7 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, C* __res
                                                 long long node0, const C (&c8)[Shape<N>::H], C iw, C c_g) {
     using LA = Launch<N, C>;
     const int warp = threadIdx.x >> 5;
-#pragma unroll
+#pragma unroll 1
     for (int rep = 0; rep < LA::REPS; ++rep)
         direction_lines<T, C, N, FINAL>(a, sm, e_count, node0, c8, iw, c_g, warp + rep * LA::WARPS, R);
 }
