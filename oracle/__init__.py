@@ -5,7 +5,8 @@ Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 two share no code: the oracle is plain C (``esdg_oracle.c``), written from
 "GPU Performance of an Entropy-Stable Discontinuous Galerkin Euler Solver with
 Non-Conservative Terms" (Sec. 3 Eq. 2, Sec. 4.1 Eqs. 3-5), compiled with gcc
--O2 and no fast-math.
+-O2 and no fast-math.  It covers the volume term and the surface term (the
+entropy-conserving flux plus matrix dissipation at element faces).
 
 Functions take and return numpy arrays.  ``real='d'`` uses the double build,
 ``real='ld'`` the long-double build (80-bit on x86-64, binary128 on aarch64).
@@ -55,6 +56,12 @@ def _load():
                 getattr(lib, "ora_flux" + sfx).argtypes = [P, real, P, real, P, real, P]
                 getattr(lib, "ora_volume" + sfx).argtypes = [
                     ctypes.c_int, ctypes.c_long, P, P, P, real, ctypes.c_int, P, P, ctypes.c_int]
+                getattr(lib, "ora_roe_matrices" + sfx).argtypes = [P, real, P, real, P, real, P, P, P]
+                getattr(lib, "ora_dissipation" + sfx).argtypes = [P, real, P, real, P, real, P]
+                getattr(lib, "ora_surface_flux" + sfx).argtypes = [P, real, P, real, P, real, ctypes.c_int, P]
+                getattr(lib, "ora_surface" + sfx).argtypes = [
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, real,
+                    ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int]
             lib.ora_max_threads.restype = ctypes.c_int
             lib.ora_sizeof_long_double.restype = ctypes.c_int
             _lib = lib
@@ -129,4 +136,59 @@ def volume(N: int, K: int, q, Ja, phi, gamma=1.4, form: int = 0, real: str = "d"
     nt = nthreads if nthreads is not None else max_threads()
     getattr(lib, "ora_volume_" + real)(N, K, _ptr(q), _ptr(Ja), _ptr(phi), gamma, form,
                                        _ptr(out), _ptr(scale) if with_scale else None, nt)
+    return (out, scale) if with_scale else out
+
+
+def roe_matrices(qm, phim, qp, phip, nvec, gamma=1.4, real: str = "d"):
+    """Right eigenvectors R (columns), eigenvalues (unit normal) and scaling T at the averaged state."""
+    lib = _load()
+    qm, qp, nvec = _arr(qm, real), _arr(qp, real), _arr(nvec, real)
+    R = np.zeros((5, 5), dtype=_dt(real))
+    lam = np.zeros(5, dtype=_dt(real))
+    T = np.zeros(5, dtype=_dt(real))
+    getattr(lib, "ora_roe_matrices_" + real)(_ptr(qm), phim, _ptr(qp), phip, _ptr(nvec), gamma,
+                                             _ptr(R), _ptr(lam), _ptr(T))
+    return R, lam, T
+
+
+def dissipation(qm, phim, qp, phip, nvec, gamma=1.4, real: str = "d"):
+    """Matrix dissipation 1/2 |n| R |Lambda| T R^T [[w]] of the surface flux."""
+    lib = _load()
+    qm, qp, nvec = _arr(qm, real), _arr(qp, real), _arr(nvec, real)
+    D = np.zeros(5, dtype=_dt(real))
+    getattr(lib, "ora_dissipation_" + real)(_ptr(qm), phim, _ptr(qp), phip, _ptr(nvec), gamma, _ptr(D))
+    return D
+
+
+def surface_flux(qm, phim, qp, phip, nvec, gamma=1.4, dissipation: bool = True, real: str = "d"):
+    """Surface flux F*(q-, q+; n): entropy-conserving flux with gravity, minus the dissipation."""
+    lib = _load()
+    qm, qp, nvec = _arr(qm, real), _arr(qp, real), _arr(nvec, real)
+    F = np.zeros(5, dtype=_dt(real))
+    getattr(lib, "ora_surface_flux_" + real)(_ptr(qm), phim, _ptr(qp), phip, _ptr(nvec), gamma,
+                                             int(bool(dissipation)), _ptr(F))
+    return F
+
+
+def surface(N: int, K, q, Ja, phi, bc=(0, 0, 0), gamma=1.4, form: int = 0, dissipation: bool = True,
+            real: str = "d", with_scale: bool = False, nthreads: int | None = None):
+    """Surface term (5, n) on a Kx x Ky x Kz brick; bc[r] = 0 periodic, 1 slip wall.
+
+    form 0 pairs with the strong (2D) volume form and subtracts the physical
+    flux at the face nodes; form 1 (skew) adds F* alone.  with_scale also
+    returns sum (|F*| + |f.n|)/w_0 per node and variable.
+    """
+    lib = _load()
+    Kx, Ky, Kz = (int(k) for k in K)
+    n = Kx * Ky * Kz * (N + 1) ** 3
+    q = _arr(q, real).reshape(5, n)
+    Ja = _arr(Ja, real).reshape(9, n)
+    phi = _arr(phi, real).reshape(n)
+    bcs = np.ascontiguousarray(np.asarray(bc, dtype=np.int32).reshape(3))
+    out = np.zeros((5, n), dtype=_dt(real))
+    scale = np.zeros((5, n), dtype=_dt(real)) if with_scale else None
+    nt = nthreads if nthreads is not None else max_threads()
+    getattr(lib, "ora_surface_" + real)(N, Kx, Ky, Kz, _ptr(bcs), _ptr(q), _ptr(Ja), _ptr(phi), gamma,
+                                        form, int(bool(dissipation)), _ptr(out),
+                                        _ptr(scale) if with_scale else None, nt)
     return (out, scale) if with_scale else out

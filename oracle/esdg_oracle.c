@@ -1,5 +1,5 @@
 /*
- * CPU ORACLE for the flux-differencing volume term of the entropy-stable DG
+ * CPU ORACLE for the flux-differencing volume term and the surface term of the entropy-stable DG
  * Euler-with-gravity solver in "GPU Performance of an Entropy-Stable
  * Discontinuous Galerkin Euler Solver with Non-Conservative Terms"
  * (Sec. 3 Eq. 2; Sec. 4.1 Eqs. 3-5).
@@ -18,6 +18,13 @@
  * entropy-conservation condition, per-element conservation and SBP entropy
  * identity, free-stream preservation on curved meshes, a hydrostatic closed
  * form, metric identities and closed forms, and LGL operator identities.
+ *
+ * The surface term (Eq. 2's M^-1 M^s G^s F*, with F* the entropy-conserving
+ * flux plus matrix dissipation) is pinned in tests/test_oracle_surface_pins.py:
+ * the eigen-structure and entropy Jacobian against complex-step derivatives
+ * of the physical flux and entropy variables, the Roe small-jump limit,
+ * entropy stability, conservation, free stream, and the global entropy
+ * balance of volume + surface.
  */
 #include <stdlib.h>
 #include <tgmath.h>

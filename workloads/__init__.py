@@ -67,6 +67,8 @@ class Config:
     warp: bool
     seed: int
     description: str = ""
+    # surface term only: per reference direction 0 = periodic, 1 = slip wall
+    bc: tuple = (0, 0, 0)
 
     @property
     def Nq(self) -> int:
@@ -97,10 +99,12 @@ def _make_configs() -> dict:
         "4x4x4 affine periodic box, N=3, constant state plus 1% smooth perturbations")
     cfgs["bubble_N4"] = Config(
         "bubble_N4", 4, 16, 16, 16, "fp64", "bubble", (1000.0, 1000.0, 1000.0), False, _seed(2, 4),
-        "1000 m box, 16^3 affine elements, N=4, hydrostatic background + 0.5 K cosine bubble")
+        "1000 m box, 16^3 affine elements, N=4, hydrostatic background + 0.5 K cosine bubble",
+        (1, 1, 1))
     cfgs["channel_N7"] = Config(
         "channel_N7", 7, 64, 16, 8, "fp64", "channel", (4.0e7, 6.0e6, 3.0e4), True, _seed(3, 7),
-        "40000x6000x30 km channel, 64x16x8 warped elements, N=7, balanced jet + 1 K bump")
+        "40000x6000x30 km channel, 64x16x8 warped elements, N=7, balanced jet + 1 K bump",
+        (0, 1, 1))
     cfgs["channel_N7_fp32"] = dataclasses.replace(
         cfgs["channel_N7"], name="channel_N7_fp32", precision="fp32",
         description="channel_N7 with FP32 state, metrics and geopotential")
@@ -125,12 +129,12 @@ def get_config(name: str) -> Config:
 
 
 def small_config(N: int, K=(2, 2, 2), warp=True, state="random", seed=None,
-                 precision="fp64", domain=(1.0e4, 1.0e4, 1.0e4)) -> Config:
+                 precision="fp64", domain=(1.0e4, 1.0e4, 1.0e4), bc=(0, 0, 0)) -> Config:
     """A small mesh of any order for parity sweeps (several tiles, ragged counts)."""
     Kx, Ky, Kz = K
     s = seed if seed is not None else _seed(9, N) + 1000 * (Kx + 7 * Ky + 49 * Kz)
     return Config(f"small_N{N}_{Kx}x{Ky}x{Kz}_{state}{'_warp' if warp else ''}",
-                  N, Kx, Ky, Kz, precision, state, tuple(domain), warp, s)
+                  N, Kx, Ky, Kz, precision, state, tuple(domain), warp, s, "", tuple(bc))
 
 
 # ----------------------------------------------------------------------------
