@@ -43,6 +43,9 @@ _SIGS = {
     "esdg_set_geometry": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     "esdg_volume_rhs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "esdg_volume_rhs_range": (ctypes.c_int, [_P, ctypes.c_long, ctypes.c_long, _P, _P, _P, _P, _P]),
+    "esdg_set_boundary": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "esdg_set_dissipation": (ctypes.c_int, [_P, ctypes.c_int]),
+    "esdg_surface_rhs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "esdg_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint), _P]),
     "esdg_last_error": (ctypes.c_char_p, [_P]),
     "esdg_get_operators": (ctypes.c_int, [ctypes.c_int, _P, _P, _P]),
@@ -135,13 +138,15 @@ class VolumeOperator:
     """A handle for one mesh shape, order and precision.
 
     precision: "fp64", "fp32" or "fp64ff" (FP64 buffers, float-float pair
-    arithmetic); form: "2d" (diagonal kept) or "skew".
+    arithmetic); form: "2d" (diagonal kept) or "skew"; bc: surface-term
+    boundary kind per reference direction (0 periodic, 1 slip wall);
+    dissipation: matrix dissipation in the surface flux.
     Tensors passed in must be contiguous CUDA tensors of the handle's dtype
     (node coordinates are always float64), laid out as described in esdg.h.
     """
 
     def __init__(self, Kx: int, Ky: int, Kz: int, N: int, precision: str = "fp64", form: str = "2d",
-                 gamma: float = 1.4):
+                 gamma: float = 1.4, bc=(0, 0, 0), dissipation: bool = True):
         import torch
         self.lib = load_library()
         self.Kx, self.Ky, self.Kz, self.N = int(Kx), int(Ky), int(Kz), int(N)
@@ -156,6 +161,18 @@ class VolumeOperator:
         self.h = h
         if gamma != 1.4:
             _check(self.lib.esdg_set_params(self.h, float(gamma)), self.h)
+        self.set_boundary(*bc)
+        self.set_dissipation(dissipation)
+
+    def set_boundary(self, bc_xi: int = 0, bc_eta: int = 0, bc_zeta: int = 0):
+        """Surface-term boundary kind per reference direction: 0 periodic, 1 slip wall."""
+        _check(self.lib.esdg_set_boundary(self.h, int(bc_xi), int(bc_eta), int(bc_zeta)), self.h)
+        self.bc = (int(bc_xi), int(bc_eta), int(bc_zeta))
+
+    def set_dissipation(self, on: bool = True):
+        """Surface flux with (default) or without the matrix dissipation."""
+        _check(self.lib.esdg_set_dissipation(self.h, int(bool(on))), self.h)
+        self.dissipation = bool(on)
 
     def close(self):
         if getattr(self, "h", None):
@@ -209,6 +226,21 @@ class VolumeOperator:
                                                 _dptr(out), sp)
         _check(rc, self.h)
         return out
+
+    def surface_rhs(self, q, metrics, phi, out, stream=None):
+        """Add the surface term into out (5, n): out = volume + surface after volume_rhs."""
+        self._req(q, 5 * self.n, name="q")
+        self._req(metrics, 9 * self.n, name="metrics")
+        self._req(phi, self.n, name="phi")
+        self._req(out, 5 * self.n, name="out")
+        _check(self.lib.esdg_surface_rhs(self.h, _dptr(q), _dptr(metrics), _dptr(phi), _dptr(out),
+                                         _stream_ptr(stream)), self.h)
+        return out
+
+    def rhs(self, q, metrics, phi, out=None, stream=None):
+        """Volume + surface term (5, n): dq/dt = -rhs/J."""
+        out = self.volume_rhs(q, metrics, phi, out=out, stream=stream)
+        return self.surface_rhs(q, metrics, phi, out, stream=stream)
 
     def status(self, stream=None) -> int:
         """Read and clear the status word (synchronises the stream)."""

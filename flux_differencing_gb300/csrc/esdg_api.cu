@@ -15,6 +15,8 @@ struct esdg_ctx {
     long long Kx = 0, Ky = 0, Kz = 0, K = 0, n = 0;
     int N = 0, Nq = 0, precision = 0, form = 0;
     double gamma = 1.4;
+    int bc[3] = {ESDG_BC_PERIODIC, ESDG_BC_PERIODIC, ESDG_BC_PERIODIC};
+    int dissipation = 1;
     int device = 0;
     unsigned* d_status = nullptr;
     double nodes[esdg::kMaxNq];
@@ -145,6 +147,33 @@ esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja
     a.form = h->form;
     a.status = h->d_status;
     a.ops = ops;
+    return a;
+}
+
+template <typename T>
+esdg::SurfaceArgs<T> surface_args(const esdg_ctx* h, const void* q, const void* Ja, const void* phi, void* out) {
+    esdg::SurfaceArgs<T> a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = static_cast<const T*>(q);
+    a.Ja = static_cast<const T*>(Ja);
+    a.phi = static_cast<const T*>(phi);
+    a.out = static_cast<T*>(out);
+    a.n = h->n;
+    a.Kx = h->Kx;
+    a.Ky = h->Ky;
+    a.Kz = h->Kz;
+    for (int r = 0; r < 3; ++r) a.bc[r] = h->bc[r];
+    a.form = h->form;
+    a.dissipation = h->dissipation;
+    a.inv_w0 = (T)(1.0L / (long double)h->weights[0]);
+    const long double g = h->gamma;
+    a.k.gm1 = (T)(g - 1);
+    a.k.igm1 = (T)(1 / (g - 1));
+    a.k.c_g = (T)(1 / (2 * (g - 1)));
+    a.k.gamma = (T)g;
+    a.k.c_ac = (T)(1 / (2 * g));
+    a.k.c_en = (T)((g - 1) / g);
+    a.status = h->d_status;
     return a;
 }
 
@@ -342,6 +371,42 @@ int esdg_volume_rhs_range(esdg_handle h, long e_begin, long e_count, const void*
 int esdg_volume_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream) {
     if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
     return esdg_volume_rhs_range(h, 0, (long)h->K, q, metrics, phi, out, stream);
+}
+
+int esdg_set_boundary(esdg_handle h, int bc_xi, int bc_eta, int bc_zeta) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    const int b[3] = {bc_xi, bc_eta, bc_zeta};
+    for (int r = 0; r < 3; ++r)
+        if (b[r] != ESDG_BC_PERIODIC && b[r] != ESDG_BC_WALL)
+            return fail(h, ESDG_ERR_ARG, "boundary kind must be ESDG_BC_PERIODIC or ESDG_BC_WALL");
+    for (int r = 0; r < 3; ++r) h->bc[r] = b[r];
+    return ESDG_OK;
+}
+
+int esdg_set_dissipation(esdg_handle h, int on) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    h->dissipation = on ? 1 : 0;
+    return ESDG_OK;
+}
+
+int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (!q || !metrics || !phi || !out) return fail(h, ESDG_ERR_ARG, "null device pointer");
+    if (!aligned16(q) || !aligned16(metrics) || !aligned16(phi) || !aligned16(out))
+        return fail(h, ESDG_ERR_ALIGN, "device pointers must be 16-byte aligned");
+    const size_t es = h->precision == ESDG_FP32 ? sizeof(float) : sizeof(double);
+    const size_t nb = es * (size_t)h->n;
+    if (overlaps(out, 5 * nb, q, 5 * nb) || overlaps(out, 5 * nb, metrics, 9 * nb) || overlaps(out, 5 * nb, phi, nb))
+        return fail(h, ESDG_ERR_ARG, "out overlaps an input");
+    if (int rc = check_device(h)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (h->precision == ESDG_FP32)
+        e = esdg::launch_surface_fp32(surface_args<float>(h, q, metrics, phi, out), h->N, s);
+    else
+        e = esdg::launch_surface_fp64(surface_args<double>(h, q, metrics, phi, out), h->N, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "surface kernel launch");
+    return ESDG_OK;
 }
 
 int esdg_get_status(esdg_handle h, unsigned* flags, void* stream) {

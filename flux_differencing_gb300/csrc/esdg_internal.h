@@ -54,6 +54,37 @@ ESDG_DECLARE_LAUNCH(7)
 ESDG_DECLARE_LAUNCH(8)
 #undef ESDG_DECLARE_LAUNCH
 
+// Surface term: constants derived from gamma.
+template <typename T>
+struct SurfaceConsts {
+    T gm1;     // gamma - 1
+    T igm1;    // 1/(gamma - 1)
+    T c_g;     // 1/(2 (gamma - 1))
+    T gamma;
+    T c_ac;    // 1/(2 gamma): acoustic-wave entry of the eigenvector scaling
+    T c_en;    // (gamma - 1)/gamma: entropy-wave entry of the eigenvector scaling
+};
+
+template <typename T>
+struct SurfaceArgs {
+    const T* q;        // 5 planes
+    const T* Ja;       // 9 planes
+    const T* phi;      // 1 plane
+    T* out;            // 5 planes, accumulated into
+    long long n;       // plane stride
+    long long Kx, Ky, Kz;
+    int bc[3];         // per direction: 0 periodic, 1 slip wall
+    int form;          // 0: 2D form (subtract the physical flux), 1: skew form
+    int dissipation;   // 0: entropy-conserving flux only
+    T inv_w0;          // 1 / (LGL end weight)
+    SurfaceConsts<T> k;
+    unsigned* status;
+};
+
+// Launch the three direction passes of the surface term (one per launch).
+cudaError_t launch_surface_fp64(const SurfaceArgs<double>& a, int N, cudaStream_t s);
+cudaError_t launch_surface_fp32(const SurfaceArgs<float>& a, int N, cudaStream_t s);
+
 // Geometry: curl-form metrics in FP64 from node coordinates.
 struct GeometryArgs {
     const double* x;

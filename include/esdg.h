@@ -128,6 +128,48 @@ int esdg_volume_rhs(esdg_handle h, const void* q, const void* metrics, const voi
 int esdg_volume_rhs_range(esdg_handle h, long e_begin, long e_count, const void* q,
                           const void* metrics, const void* phi, void* out, void* stream);
 
+/* Boundary kinds of the surface term, per reference direction of the brick
+ * of elements (element e = ex + Kx (ey + Ky ez)). */
+enum { ESDG_BC_PERIODIC = 0, ESDG_BC_WALL = 1 };
+
+/* Boundary kind of each reference direction for esdg_surface_rhs (default
+ * periodic in all three).  ESDG_BC_WALL is a slip wall: the state outside
+ * the face is the mirror image (rho, m - 2 (m.n^) n^, E) of the inside state
+ * with the same phi, so no mass or energy crosses it.
+ * Errors: ESDG_ERR_ARG (null handle or unknown kind). */
+int esdg_set_boundary(esdg_handle h, int bc_xi, int bc_eta, int bc_zeta);
+
+/* on != 0 (default): the surface flux is the entropy-conserving flux minus
+ * the matrix dissipation; on == 0: the entropy-conserving flux alone (the
+ * semi-discrete scheme then conserves entropy, which tests use). */
+int esdg_set_dissipation(esdg_handle h, int on);
+
+/* The surface term of Eq. 2 (Sec. 3 of the ESDG GPU paper: the surface flux
+ * F* is the entropy-conserving flux plus matrix dissipation, "akin to a Roe
+ * Riemann solver"; the paper leaves the formula to its reference), ADDED
+ * into out.  At every face node i of every element, with j the node of the
+ * neighbouring element at the same position (or the wall's mirror state):
+ *     out_i += (1/w_0) [ F*(q_i, q_j; n) - f(q_i) . n_own ]     (ESDG_FORM_2D)
+ *     out_i += (1/w_0) F*(q_i, q_j; n)                          (ESDG_FORM_SKEW)
+ * with w_0 the LGL end weight, n = +-(Ja^r(i) + Ja^r(j))/2 the outward
+ * averaged normal (n = n_own = +-Ja^r(i) at a wall), f the physical flux and
+ *     F* = F_ec(q_i, q_j; n) + G(i, j; n) - 1/2 |n| R |Lambda| T R^T [[w]],
+ * F_ec + G the volume term's two-point flux (Eqs. 3-5), [[w]] = w_j - w_i the
+ * jump of the entropy variables, and R, Lambda, T the eigenvectors,
+ * eigenvalues (unit normal) and entropy scaling (R T R^T = dq/dw) of the
+ * flux Jacobian at the averaged state rho_ln, {{u}}, {{rho}}/(2{{b}}),
+ * {{phi}}.  So out = volume + surface after esdg_volume_rhs then this call
+ * on the same stream, and dq/dt = -out/J.
+ *   q, metrics, phi  device, as esdg_volume_rhs (read).
+ *   out              device, 5*n values (read and written); must not overlap
+ *                    an input.
+ * Enqueues three kernel launches (one per reference direction) on `stream`;
+ * no synchronisation and no allocation.  ESDG_FP64_FF handles run the FP64
+ * surface kernel.  Non-physical states set ESDG_STATUS_NONPHYSICAL.
+ * Errors: ESDG_ERR_ARG, ESDG_ERR_ALIGN, ESDG_ERR_CUDA (launch failure). */
+int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi,
+                     void* out, void* stream);
+
 /* Copy the status word to *flags and clear it.  Synchronises `stream`.
  * Errors: ESDG_ERR_ARG, ESDG_ERR_CUDA. */
 int esdg_get_status(esdg_handle h, unsigned* flags, void* stream);

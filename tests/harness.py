@@ -49,3 +49,29 @@ def errors(got, ref, scale):
     e = np.array([np.max(np.abs(got[c] - ref[c])) / np.max(scale[c]) for c in range(5)])
     plain = np.array([np.max(np.abs(got[c] - ref[c])) / max(np.max(np.abs(ref[c])), 1e-300) for c in range(5)])
     return e, plain
+
+
+def run_gpu_surface(cfg, g, form="2d", precision=None, dissipation=True, bc=None, with_volume=False):
+    """Surface term alone (or volume + surface) on the GPU; returns (out float64 numpy, op)."""
+    prec = precision or cfg.precision
+    bc = cfg.bc if bc is None else bc
+    op = fd.VolumeOperator(cfg.Kx, cfg.Ky, cfg.Kz, cfg.N, prec, form, bc=bc, dissipation=dissipation)
+    dg = g if g["q"].is_cuda else to_device(g)
+    Ja = op.set_geometry(dg["x"].contiguous(), dg["y"].contiguous(), dg["z"].contiguous())
+    q = dg["q"].to(op.dtype).contiguous()
+    phi = dg["phi"].to(op.dtype).contiguous()
+    if with_volume:
+        res = op.rhs(q, Ja, phi)
+    else:
+        res = torch.zeros((5, cfg.n), dtype=op.dtype, device=q.device)
+        op.surface_rhs(q, Ja, phi, res)
+    torch.cuda.synchronize()
+    return res.double().cpu().numpy(), op
+
+
+def run_oracle_surface(cfg, g, form=0, dissipation=True, bc=None, nthreads=None):
+    gc = {k: v.cpu().numpy() for k, v in g.items()}
+    bc = cfg.bc if bc is None else bc
+    Ja, _ = oracle.metrics(cfg.N, cfg.K, gc["x"], gc["y"], gc["z"])
+    return oracle.surface(cfg.N, (cfg.Kx, cfg.Ky, cfg.Kz), gc["q"], Ja, gc["phi"], bc, form=form,
+                          dissipation=dissipation, with_scale=True, nthreads=nthreads)

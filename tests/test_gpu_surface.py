@@ -1,0 +1,151 @@
+"""Parity of the CUDA surface term with the CPU oracle (GPU required).
+
+The surface term alone (added into a zeroed output) is compared with the
+oracle's, normalised per conserved variable by the magnitude of the summed
+face terms, sum (|F*| + |f.n|)/w_0 (tests/harness.py): 1e-11 for FP64 and
+1e-4 for FP32 against the FP64 oracle on the original FP64 inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import flux_differencing_gb300 as fd
+import oracle
+import workloads as wl
+from tests import harness as hz
+from tests import physics as ph
+
+pytestmark = pytest.mark.gpu
+
+BCS = [(0, 0, 0), (1, 1, 1), (0, 1, 1), (1, 0, 0)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_ok):
+    fd.load_library(build_if_missing=True)
+
+
+@pytest.mark.parametrize("N", list(range(1, 9)))
+@pytest.mark.parametrize("bc", BCS)
+@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+def test_surface_small_meshes(N, bc, precision):
+    cfg = wl.small_config(N, K=(3, 2, 2), warp=True, precision=precision, bc=bc)
+    g = wl.generate(cfg)
+    got, op = hz.run_gpu_surface(cfg, g)
+    assert op.status() == 0
+    ref, scale = hz.run_oracle_surface(cfg, g)
+    e, _ = hz.errors(got, ref, scale)
+    assert e.max() < hz.TOL[precision], e
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8])
+@pytest.mark.parametrize("form,dissipation", [("skew", True), ("2d", False), ("skew", False)])
+@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+def test_surface_forms_and_dissipation(N, form, dissipation, precision):
+    cfg = wl.small_config(N, K=(2, 3, 2), warp=True, precision=precision, bc=(0, 1, 1))
+    g = wl.generate(cfg)
+    got, _ = hz.run_gpu_surface(cfg, g, form=form, dissipation=dissipation)
+    ref, scale = hz.run_oracle_surface(cfg, g, form=1 if form == "skew" else 0, dissipation=dissipation)
+    e, _ = hz.errors(got, ref, scale)
+    assert e.max() < hz.TOL[precision], e
+
+
+@pytest.mark.parametrize("K", [(1, 1, 1), (1, 4, 1), (5, 1, 2), (1, 1, 3)])
+@pytest.mark.parametrize("bc", [(0, 0, 0), (1, 1, 1)])
+def test_surface_degenerate_meshes(K, bc):
+    """One element along a direction: periodic faces meet the same element."""
+    cfg = wl.small_config(3, K=K, warp=True, bc=bc)
+    g = wl.generate(cfg)
+    got, _ = hz.run_gpu_surface(cfg, g)
+    ref, scale = hz.run_oracle_surface(cfg, g)
+    e, _ = hz.errors(got, ref, scale)
+    assert e.max() < hz.TOL["fp64"], e
+
+
+def test_surface_fp64ff_handle_runs_fp64_surface():
+    cfg = wl.small_config(4, K=(2, 2, 2), warp=True, precision="fp64ff", bc=(0, 1, 1))
+    g = wl.generate(cfg)
+    got, _ = hz.run_gpu_surface(cfg, g)
+    ref, scale = hz.run_oracle_surface(cfg, g)
+    e, _ = hz.errors(got, ref, scale)
+    assert e.max() < hz.TOL["fp64"], e
+
+
+@pytest.mark.parametrize("name", ["tiny_box_N3", "bubble_N4", "channel_N7", "channel_N7_fp32"])
+def test_surface_named_workloads(name):
+    """The surface term of each workload at full size, with its boundary kinds."""
+    cfg = wl.get_config(name)
+    g = wl.generate(cfg)
+    got, op = hz.run_gpu_surface(cfg, g)
+    assert op.status() == 0
+    ref, scale = hz.run_oracle_surface(cfg, g)
+    e, plain = hz.errors(got, ref, scale)
+    assert e.max() < hz.TOL[cfg.precision], (e, plain)
+
+
+@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+def test_rhs_is_volume_plus_surface(precision):
+    cfg = wl.small_config(5, K=(2, 2, 3), warp=True, precision=precision, bc=(0, 1, 1))
+    g = wl.generate(cfg)
+    got, _ = hz.run_gpu_surface(cfg, g, with_volume=True)
+    vref, vscale = hz.run_oracle(cfg, g)
+    sref, sscale = hz.run_oracle_surface(cfg, g)
+    e, _ = hz.errors(got, vref + sref, vscale + sscale)
+    assert e.max() < hz.TOL[precision], e
+
+
+def test_surface_is_deterministic():
+    cfg = wl.small_config(7, K=(3, 3, 2), warp=True, bc=(0, 1, 1))
+    g = wl.generate(cfg)
+    a, _ = hz.run_gpu_surface(cfg, g)
+    b, _ = hz.run_gpu_surface(cfg, g)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("N", [2, 4, 7])
+def test_gpu_rhs_free_stream_and_conservation(N):
+    """Properties of the GPU result alone: a constant state is steady on a warped
+    periodic mesh, and the global integrals of mass and energy do not change."""
+    cfg = wl.small_config(N, K=(3, 2, 2), warp=True, bc=(0, 0, 0))
+    g = wl.generate(cfg)
+    n = cfg.n
+    _, w = oracle.lgl(N)
+    idx = np.arange((N + 1) ** 3)
+    om = np.tile(w[idx % (N + 1)] * w[(idx // (N + 1)) % (N + 1)] * w[idx // (N + 1) ** 2], cfg.K)
+    qc = ph.conserved(np.full(n, 1.1), np.tile(np.array([[12.0], [-7.0], [4.0]]), (1, n)),
+                      np.full(n, 9.0e4), 0.0)
+    gc = dict(g)
+    gc["q"] = torch.from_numpy(qc)
+    gc["phi"] = torch.zeros(n, dtype=torch.float64)
+    tot, _ = hz.run_gpu_surface(cfg, gc, with_volume=True)
+    _, fvs = hz.run_oracle(cfg, gc)
+    _, fss = hz.run_oracle_surface(cfg, gc)
+    free_scale = (fvs + fss).max(axis=1)
+    assert np.max(np.abs(tot).max(axis=1) / free_scale) < 1e3 * np.finfo(float).eps
+    got, _ = hz.run_gpu_surface(cfg, g, with_volume=True)
+    _, vscale = hz.run_oracle(cfg, g)
+    _, sscale = hz.run_oracle_surface(cfg, g)
+    mag = (vscale + sscale) @ om
+    sums = got @ om
+    for c in (0, 4):
+        assert abs(sums[c]) < 1e-12 * mag[c]
+
+
+def test_surface_status_flags_nonphysical_state():
+    cfg = wl.small_config(3, K=(2, 2, 2), warp=False, bc=(0, 0, 0))
+    g = wl.generate(cfg)
+    g["q"][4, 0] = -1.0  # p < 0 at a corner node of element 0
+    _, op = hz.run_gpu_surface(cfg, g)
+    assert op.status() & 1
+
+
+def test_surface_argument_errors():
+    op = fd.VolumeOperator(2, 2, 2, 3)
+    with pytest.raises(fd.EsdgError):
+        op.set_boundary(0, 2, 0)
+    n = op.n
+    q = torch.ones((5, n), dtype=torch.float64, device="cuda")
+    Ja = torch.ones((9, n), dtype=torch.float64, device="cuda")
+    phi = torch.zeros(n, dtype=torch.float64, device="cuda")
+    with pytest.raises(fd.EsdgError):
+        op.surface_rhs(q, Ja, phi, q)  # out aliases q
