@@ -176,7 +176,9 @@ def surface(N: int, K, q, Ja, phi, bc=(0, 0, 0), gamma=1.4, form: int = 0, dissi
 
     form 0 pairs with the strong (2D) volume form and subtracts the physical
     flux at the face nodes; form 1 (skew) adds F* alone.  with_scale also
-    returns sum (|F*| + |f.n|)/w_0 per node and variable.
+    returns sum (|F*| + |f.n| + M)/w_0 per node and variable, M the magnitude
+    bound 1/2 |n| |R| |Lambda| T |R|^T (|w-| + |w+|) of the dissipation's
+    terms (its rounding scale: [[w]] is a difference of O(|w|) numbers).
     """
     lib = _load()
     Kx, Ky, Kz = (int(k) for k in K)

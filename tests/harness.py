@@ -3,7 +3,10 @@ same seeded inputs and measure the normalised error.
 
 Error measure (per conserved variable c):
     e_c = max_i |gpu_c,i - oracle_c,i| / S_c,   S_c = max_i sum_r sum_m |2 D_im F^r_c(i, m)|
-S_c is the magnitude of the terms the volume sum adds up; the plain relative
+S_c is the magnitude of the terms the volume sum adds up (for the surface
+term: sum over the node's faces of (|F*_c| + |f_c.n| + M_c)/w_0, M the
+magnitude of the dissipation's terms, which carry rounding relative to |w|
+because [[w]] is a difference of O(|w|) numbers); the plain relative
 error max|diff| / max|oracle| is also returned because for nearly hydrostatic
 states the momentum sum is a near-cancellation of pressure terms and its
 plain relative error reflects that conditioning, not the kernel.

@@ -29,7 +29,8 @@ def _lib(cuda_ok):
 @pytest.mark.parametrize("bc", BCS)
 @pytest.mark.parametrize("precision", ["fp64", "fp32"])
 def test_surface_small_meshes(N, bc, precision):
-    cfg = wl.small_config(N, K=(3, 2, 2), warp=True, precision=precision, bc=bc)
+    """States with jumps across faces, so that the dissipation is exercised."""
+    cfg = wl.small_config(N, K=(3, 2, 2), warp=True, precision=precision, bc=bc, state="noisy")
     g = wl.generate(cfg)
     got, op = hz.run_gpu_surface(cfg, g)
     assert op.status() == 0
@@ -38,11 +39,22 @@ def test_surface_small_meshes(N, bc, precision):
     assert e.max() < hz.TOL[precision], e
 
 
+def test_noisy_state_makes_the_dissipation_count():
+    """The dissipation must be a sizeable part of the surface term for the parity
+    tests above to check it: with jumps of a few percent across faces it is."""
+    cfg = wl.small_config(3, K=(2, 2, 2), warp=True, bc=(0, 1, 1), state="noisy")
+    g = wl.generate(cfg)
+    with_d, scale = hz.run_oracle_surface(cfg, g, dissipation=True)
+    without, _ = hz.run_oracle_surface(cfg, g, dissipation=False)
+    rel = np.abs(with_d - without).max(axis=1) / scale.max(axis=1)
+    assert rel.min() > 1e-4, rel
+
+
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8])
 @pytest.mark.parametrize("form,dissipation", [("skew", True), ("2d", False), ("skew", False)])
 @pytest.mark.parametrize("precision", ["fp64", "fp32"])
 def test_surface_forms_and_dissipation(N, form, dissipation, precision):
-    cfg = wl.small_config(N, K=(2, 3, 2), warp=True, precision=precision, bc=(0, 1, 1))
+    cfg = wl.small_config(N, K=(2, 3, 2), warp=True, precision=precision, bc=(0, 1, 1), state="noisy")
     g = wl.generate(cfg)
     got, _ = hz.run_gpu_surface(cfg, g, form=form, dissipation=dissipation)
     ref, scale = hz.run_oracle_surface(cfg, g, form=1 if form == "skew" else 0, dissipation=dissipation)
@@ -54,7 +66,7 @@ def test_surface_forms_and_dissipation(N, form, dissipation, precision):
 @pytest.mark.parametrize("bc", [(0, 0, 0), (1, 1, 1)])
 def test_surface_degenerate_meshes(K, bc):
     """One element along a direction: periodic faces meet the same element."""
-    cfg = wl.small_config(3, K=K, warp=True, bc=bc)
+    cfg = wl.small_config(3, K=K, warp=True, bc=bc, state="noisy")
     g = wl.generate(cfg)
     got, _ = hz.run_gpu_surface(cfg, g)
     ref, scale = hz.run_oracle_surface(cfg, g)
@@ -63,7 +75,7 @@ def test_surface_degenerate_meshes(K, bc):
 
 
 def test_surface_fp64ff_handle_runs_fp64_surface():
-    cfg = wl.small_config(4, K=(2, 2, 2), warp=True, precision="fp64ff", bc=(0, 1, 1))
+    cfg = wl.small_config(4, K=(2, 2, 2), warp=True, precision="fp64ff", bc=(0, 1, 1), state="noisy")
     g = wl.generate(cfg)
     got, _ = hz.run_gpu_surface(cfg, g)
     ref, scale = hz.run_oracle_surface(cfg, g)
@@ -85,7 +97,7 @@ def test_surface_named_workloads(name):
 
 @pytest.mark.parametrize("precision", ["fp64", "fp32"])
 def test_rhs_is_volume_plus_surface(precision):
-    cfg = wl.small_config(5, K=(2, 2, 3), warp=True, precision=precision, bc=(0, 1, 1))
+    cfg = wl.small_config(5, K=(2, 2, 3), warp=True, precision=precision, bc=(0, 1, 1), state="noisy")
     g = wl.generate(cfg)
     got, _ = hz.run_gpu_surface(cfg, g, with_volume=True)
     vref, vscale = hz.run_oracle(cfg, g)
@@ -95,7 +107,7 @@ def test_rhs_is_volume_plus_surface(precision):
 
 
 def test_surface_is_deterministic():
-    cfg = wl.small_config(7, K=(3, 3, 2), warp=True, bc=(0, 1, 1))
+    cfg = wl.small_config(7, K=(3, 3, 2), warp=True, bc=(0, 1, 1), state="noisy")
     g = wl.generate(cfg)
     a, _ = hz.run_gpu_surface(cfg, g)
     b, _ = hz.run_gpu_surface(cfg, g)

@@ -62,7 +62,7 @@ class Config:
     Ky: int
     Kz: int
     precision: str          # "fp64" or "fp32"
-    state: str              # "box", "bubble", "channel", "random"
+    state: str              # "box", "bubble", "channel", "random", "noisy" (random + per-node jumps)
     domain: tuple           # (Lx, Ly, Lz), origin at 0
     warp: bool
     seed: int
@@ -237,12 +237,23 @@ def _state(cfg: Config, X, Y, Z, draws: dict, elems: torch.Tensor):
         u2 = u0[1] + 0.01 * umag * _smooth_field(f[2], X, Y, Z, dom)
         u3 = u0[2] + 0.01 * umag * _smooth_field(f[3], X, Y, Z, dom)
         p = 1.0e5 * (1.0 + 0.01 * _smooth_field(f[4], X, Y, Z, dom))
-    elif cfg.state == "random":
+    elif cfg.state in ("random", "noisy"):
         rho = 1.0 + 0.05 * _smooth_field(f[0], X, Y, Z, dom)
         p = 1.0e5 * (1.0 + 0.05 * _smooth_field(f[1], X, Y, Z, dom))
         u1 = 20.0 * _smooth_field(f[2], X, Y, Z, dom)
         u2 = 20.0 * _smooth_field(f[3], X, Y, Z, dom)
         u3 = 20.0 * _smooth_field(f[4], X, Y, Z, dom)
+        if cfg.state == "noisy":
+            # independent per-node perturbations: states jump across element faces
+            g = torch.Generator(device="cpu")
+            g.manual_seed(draws["noise_seed"])
+            full = 2.0 * torch.rand((5, cfg.K, cfg.Nq ** 3), generator=g, dtype=torch.float64) - 1.0
+            xi = full[:, elems.cpu(), :].to(X.device)
+            rho = rho * (1.0 + 0.02 * xi[0])
+            p = p * (1.0 + 0.02 * xi[1])
+            u1 = u1 + 2.0 * xi[2]
+            u2 = u2 + 2.0 * xi[3]
+            u3 = u3 + 2.0 * xi[4]
     elif cfg.state == "bubble":
         theta0 = 300.0
         exner = 1.0 - GRAV * Z / (C_P * theta0)
