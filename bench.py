@@ -63,33 +63,73 @@ def flops_per_dof(N: int, form2d: bool = True) -> float:
 
 BYTES_PER_DOF = {"fp64": 20 * 8, "fp32": 20 * 4, "fp64ff": 20 * 8}  # 15 planes read + 5 written
 
-NOMINAL_FP64_TFLOPS = 1.25  # GB300 FP64 vector, nominal (see DESIGN.md)
+# Surface term, algorithmic operations per face node (same counting rules),
+# from the formulas of the surface kernel:
+#   interior face node (evaluated once for both sides): two node states
+#     (1/rho, u, |u|^2, p, b, two logarithms) 38, entropy-conserving flux
+#     with gravity 69, matrix dissipation (averaged state, sound speed,
+#     entropy-variable jumps, wave strengths, projections) 128, both sides'
+#     fluxes 31, the physical flux subtracted on both sides (2D form) 54,
+#     1/w_0 accumulation into both nodes 20                   -> 340
+#   slip-wall face node: one node state 19, mirror state 24, flux 69,
+#     dissipation 128, fluxes 31, physical flux 27, accumulation 10 -> 308
+# Values moved per face node: interior 2 x (5 + 1 + 3) read + 2 x 5
+# read-modify-written = 38; wall 9 + 5 + 5 = 19.
+SURF_IFACE_OPS = 340
+SURF_WALL_OPS = 308
+SURF_IFACE_VALUES = 38
+SURF_WALL_VALUES = 19
 
 
-KERNEL_SOURCES = [os.path.join(ROOT, "flux_differencing_gb300", "csrc", f)
-                  for f in ("volume_kernel.cuh", "floatfloat.cuh", "esdg_internal.h", "volume_inst.cu")]
+def surface_counts(cfg):
+    """(interior face nodes, wall face nodes) over the three direction passes."""
+    Nq2 = (cfg.N + 1) ** 2
+    K = cfg.K
+    Kd = (cfg.Kx, cfg.Ky, cfg.Kz)
+    inner = walls = 0
+    for r in range(3):
+        plane = (K // Kd[r]) * Nq2
+        if cfg.bc[r]:
+            inner += K * Nq2 - plane
+            walls += 2 * plane
+        else:
+            inner += K * Nq2
+    return inner, walls
+
+NOMINAL_FP64_TFLOPS = 1.25  # GB300 FP64 vector, nominal
 
 
-def kernel_source_sha() -> str:
+_CSRC = os.path.join(ROOT, "flux_differencing_gb300", "csrc")
+KERNEL_SOURCES = {
+    "volume": [os.path.join(_CSRC, f) for f in ("volume_kernel.cuh", "floatfloat.cuh", "esdg_internal.h",
+                                                 "volume_inst.cu")],
+}
+KERNEL_SOURCES["surface"] = KERNEL_SOURCES["volume"] + [os.path.join(_CSRC, "surface_kernel.cu")]
+
+
+def kernel_source_sha(kind: str = "volume") -> str:
     import hashlib
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in KERNEL_SOURCES[kind]:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, only if the kernel source is unchanged."""
+def recorded_traffic(kernel: str, workload: str, kind: str = "volume"):
+    """DRAM bytes per launch (volume) or per three-launch call (surface) from a
+    committed ncu summary, only if the kernel source is unchanged."""
     import glob
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(kind)
+    key = "dram_bytes_per_launch" if kind == "volume" else "dram_bytes_per_call"
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         with open(path) as f:
             for line in f:
                 if line.startswith("traffic_record:"):
                     rec = json.loads(line.split(":", 1)[1])
-                    if rec["kernel"] == kernel and rec["workload"] == workload and rec["source_sha"] == sha:
-                        return rec["dram_bytes_per_launch"]
+                    if (rec["kernel"] == kernel and rec["workload"] == workload and rec["source_sha"] == sha
+                            and key in rec):
+                        return rec[key]
     return None
 
 
@@ -203,7 +243,7 @@ def _setup(cfg, device):
     import workloads as wl
 
     g = wl.generate(cfg, device=device)
-    op = fd.VolumeOperator(cfg.Kx, cfg.Ky, cfg.Kz, cfg.N, cfg.precision)
+    op = fd.VolumeOperator(cfg.Kx, cfg.Ky, cfg.Kz, cfg.N, cfg.precision, bc=cfg.bc)
     Ja = op.set_geometry(g["x"], g["y"], g["z"])
     q = g["q"].to(op.dtype).contiguous()
     phi = g["phi"].to(op.dtype).contiguous()
@@ -213,19 +253,30 @@ def _setup(cfg, device):
     return op, q, Ja, phi, out
 
 
-def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier):
-    """Per-launch times of the volume kernel with CUDA events on its stream."""
+def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier, what="volume"):
+    """Per-call times with CUDA events on the launching stream.
+
+    what: "volume" (one launch), "surface" (three launches, accumulating into
+    out) or "rhs" (volume then surface: four launches)."""
     import torch
+
+    def call():
+        if what == "volume":
+            op.volume_rhs(q, Ja, phi, out=out, stream=stream)
+        elif what == "surface":
+            op.surface_rhs(q, Ja, phi, out, stream=stream)
+        else:
+            op.rhs(q, Ja, phi, out=out, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            op.volume_rhs(q, Ja, phi, out=out, stream=stream)
+            call()
         torch.cuda.synchronize()
         barrier()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
         ev[0].record(stream)
         for k in range(steps):
-            op.volume_rhs(q, Ja, phi, out=out, stream=stream)
+            call()
             ev[k + 1].record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -405,6 +456,14 @@ def run_ours(args):
         res = {"cfg": cfg, "ms": ms, "gdof": gdof, "per": per,
                "flops_per_launch": fl, "achieved_tflops": fl / (statistics.mean(per) * 1e-3) / 1e12,
                "bytes_per_launch": BYTES_PER_DOF[cfg.precision] * cfg.n}
+        if not args.no_surface:
+            s_total, s_per = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier,
+                                          what="surface")
+            r_total, r_per = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier,
+                                          what="rhs")
+            assert op.status() == 0, "non-physical state in the bench inputs"
+            res["surface"] = {"ms": slowest(s_total) / args.steps, "per": s_per,
+                              "rhs_ms": slowest(r_total) / args.steps}
         if not args.no_e2e:
             e2e_steps = max(3, min(args.steps, 20))
             e_ms, h2d, d2h = _time_e2e(op, q, Ja, phi, out, e2e_steps, 1, stream, barrier)
@@ -487,12 +546,58 @@ def run_ours(args):
         if "e2e" in rf:
             line["fp64ff"]["e2e"] = {k: v for k, v in rf["e2e"].items() if k != "ms_per_step"}
         line["gpu_launches"] += args.steps + (max(3, min(args.steps, 20)) if "e2e" in rf else 0)
+    if "surface" in main:
+        line["surface"] = _surface_report(cfg, main["surface"], ws, peak64, "FP64 vector", peaks.get("hbm_gbs"))
+        line["gpu_launches"] += 7 * args.steps
+    if args.fp32_workload and "surface" in results[args.fp32_workload]:
+        r32 = results[args.fp32_workload]
+        line["fp32"]["surface"] = _surface_report(r32["cfg"], r32["surface"], ws, fp32_meas, "FP32 vector",
+                                                  peaks.get("hbm_gbs"))
+        line["gpu_launches"] += 7 * args.steps
+    if args.ff_workload and "surface" in results[args.ff_workload]:
+        rf = results[args.ff_workload]
+        line["fp64ff"]["surface"] = _surface_report(rf["cfg"], rf["surface"], ws, peak64, "FP64 vector",
+                                                    peaks.get("hbm_gbs"))
+        line["gpu_launches"] += 7 * args.steps
     line["peaks_measured"] = {"fp64_tflops": fp64_meas, "fp32_tflops": fp32_meas}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(cfg, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def _surface_report(cfg, sres, ws, alu_peak_tflops, alu_peak_name, hbm_peak_gbs):
+    """Surface-term and volume+surface lines for one workload (three direction
+    launches per surface call, accumulated into the volume output)."""
+    inner, walls = surface_counts(cfg)
+    es = 4 if cfg.precision == "fp32" else 8
+    flops = SURF_IFACE_OPS * inner + SURF_WALL_OPS * walls
+    nbytes = es * (SURF_IFACE_VALUES * inner + SURF_WALL_VALUES * walls)
+    t = statistics.mean(sres["per"]) * 1e-3
+    tfl = flops / t / 1e12
+    gbs = nbytes / t / 1e9
+    f_alu = tfl / alu_peak_tflops if alu_peak_tflops == alu_peak_tflops else None
+    f_hbm = gbs / hbm_peak_gbs if hbm_peak_gbs else None
+    bound = "hbm" if (f_hbm or 0) >= (f_alu or 0) else "alu"
+    kname = {"fp64": "surface_kernel<double>", "fp32": "surface_kernel<float>",
+             "fp64ff": "surface_kernel<double, ff>"}[cfg.precision]
+    traffic = recorded_traffic(kname, cfg.name, kind="surface")
+    return {
+        "workload": cfg.name, "bc": list(cfg.bc),
+        "surface": {"ms_per_call": sres["ms"], "launches_per_call": 3,
+                    "GDOF/s": ws * cfg.n / (sres["ms"] * 1e-3) / 1e9,
+                    "face_nodes": {"interior": inner, "wall": walls},
+                    "roofline": {"bound": bound,
+                                 "achieved_GB/s": gbs, "hbm_peak_GB/s": hbm_peak_gbs, "hbm_frac": f_hbm,
+                                 "achieved_TFLOP/s": tfl, "alu_peak_TFLOP/s": alu_peak_tflops,
+                                 "alu_peak": alu_peak_name, "alu_frac": f_alu,
+                                 "algorithmic_bytes_per_call": nbytes, "algorithmic_flops_per_call": flops,
+                                 "traffic": traffic,
+                                 "traffic_unit": "bytes per call (ncu dram read + write, three launches)"}},
+        "rhs": {"what": "volume + surface", "ms_per_step": sres["rhs_ms"], "launches_per_step": 4,
+                "GDOF/s": ws * cfg.n / (sres["rhs_ms"] * 1e-3) / 1e9},
+    }
 
 
 def run_sweep(args):
@@ -552,6 +657,7 @@ def main():
                     help="FP64 buffers with float-float pair arithmetic, reported under \"fp64ff\"")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-surface", action="store_true", help="skip the surface-term and full-RHS timings")
     ap.add_argument("--no-peaks", action="store_true", help="skip the FMA-throughput peak measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=int, default=256)

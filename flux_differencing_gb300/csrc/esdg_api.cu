@@ -403,6 +403,8 @@ int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const vo
     cudaError_t e;
     if (h->precision == ESDG_FP32)
         e = esdg::launch_surface_fp32(surface_args<float>(h, q, metrics, phi, out), h->N, s);
+    else if (h->precision == ESDG_FP64_FF)
+        e = esdg::launch_surface_fp64ff(surface_args<double>(h, q, metrics, phi, out), h->N, s);
     else
         e = esdg::launch_surface_fp64(surface_args<double>(h, q, metrics, phi, out), h->N, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "surface kernel launch");

@@ -84,6 +84,8 @@ struct SurfaceArgs {
 // Launch the three direction passes of the surface term (one per launch).
 cudaError_t launch_surface_fp64(const SurfaceArgs<double>& a, int N, cudaStream_t s);
 cudaError_t launch_surface_fp32(const SurfaceArgs<float>& a, int N, cudaStream_t s);
+// FP64 buffers, float-float arithmetic
+cudaError_t launch_surface_fp64ff(const SurfaceArgs<double>& a, int N, cudaStream_t s);
 
 // Geometry: curl-form metrics in FP64 from node coordinates.
 struct GeometryArgs {

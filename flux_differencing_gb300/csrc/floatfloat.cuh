@@ -29,6 +29,7 @@ namespace esdg {
 
 // the float and double overloads stay visible next to the ones below
 using ::fma;
+using ::fabs;
 
 __device__ __forceinline__ float sel(bool c, float a, float b) { return c ? a : b; }
 __device__ __forceinline__ double sel(bool c, double a, double b) { return c ? a : b; }
@@ -119,6 +120,20 @@ __device__ __forceinline__ ffv<F> ff_rcp(ffv<F> x) {
 }
 
 __device__ __forceinline__ ff sel(bool c, ff a, ff b) { return c ? a : b; }
+__device__ __forceinline__ ff fabs(ff x) { return x.hi < 0.0f ? -x : x; }
+
+// sqrt(x) for x > 0: FP32 square root y of x.hi, then one correction
+// y + (x - y^2)/(2y) with the residual x - y^2 formed exactly (FMA product
+// error); relative error about 2^-47 (Karp and Markstein's method).
+__device__ __forceinline__ ff ff_sqrt(ff x) {
+    const float y = sqrtf(x.hi);
+    const float p = y * y;
+    const float pe = __fmaf_rn(y, y, -p);
+    const float r = ((x.hi - p) - pe) + x.lo;
+    const float c = r * (0.5f * rcp_estimate(y));
+    const float h = y + c;
+    return ff(h, c - (h - y));
+}
 
 // ---------------------------------------------------------------------------
 // conversions from and to FP64 with the conversion instructions (FP64 pipe)

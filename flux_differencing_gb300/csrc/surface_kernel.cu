@@ -23,11 +23,18 @@
 //  * Consecutive threads take consecutive face nodes of one element face, so
 //    zeta faces read contiguous runs of (N+1)^2 nodes and eta faces runs of
 //    N+1; xi faces gather with stride N+1.
+//  * No logarithm in the common case: closeness of the two states is tested
+//    on f = (a+ - a-)/(a+ + a-), and when every lane of a warp is close the
+//    log means and the log jumps [[ln a]] = 2 atanh(f) of the entropy
+//    variables come from their series in f^2.  Only warps holding a far pair
+//    take the four logarithms.
 //  * The dissipation is formed without tangent vectors: the two shear waves
 //    share the eigenvalue u.n, so together they are the projection
 //    (I - n^ n^T) onto the face, and the acoustic pair enters through the
 //    sum and difference of its two wave strengths.
-//  * Reciprocals, logarithms and log means use the volume kernel's numerics.
+//  * Arithmetic type C: the I/O type, or float-float for FP64 buffers
+//    (ESDG_FP64_FF), which moves the arithmetic from GB300's narrow FP64 pipe
+//    to the FP32 pipes.
 #include <cuda_runtime.h>
 
 #include "esdg_internal.h"
@@ -37,137 +44,153 @@ namespace esdg {
 
 __device__ __forceinline__ double sqrt_(double x) { return sqrt(x); }
 __device__ __forceinline__ float sqrt_(float x) { return sqrtf(x); }
+__device__ __forceinline__ ff sqrt_(ff x) { return ff_sqrt(x); }
 
 namespace {
 
-template <typename T>
+template <typename C>
 struct FaceNode {
-    T rho, u1, u2, u3, uu, E, p, b, lr, lb, phi;
+    C rho, u1, u2, u3, uu, E, p, b, ib, phi;
 };
 
-template <typename T>
-__device__ __forceinline__ FaceNode<T> node_state(T rho, T m1, T m2, T m3, T E, T phi, T gm1) {
-    FaceNode<T> s;
-    const T irho = Num<T>::rcp(rho);
+template <typename C>
+__device__ __forceinline__ FaceNode<C> node_state(C rho, C m1, C m2, C m3, C E, C phi, C gm1) {
+    FaceNode<C> s;
+    const C irho = Num<C>::rcp(rho);
     s.rho = rho;
     s.u1 = m1 * irho;
     s.u2 = m2 * irho;
     s.u3 = m3 * irho;
     s.uu = fma(s.u3, s.u3, fma(s.u2, s.u2, s.u1 * s.u1));
     s.E = E;
-    s.p = gm1 * (E - rho * fma(T(0.5), s.uu, phi));
-    s.b = T(0.5) * rho * Num<T>::rcp(s.p);
-    s.lr = Num<T>::log_(rho);
-    s.lb = Num<T>::log_(s.b);
+    s.p = gm1 * (E - rho * fma(C(0.5), s.uu, phi));
+    s.b = C(0.5) * rho * Num<C>::rcp(s.p);
+    s.ib = C(2.0) * s.p * irho;  // 1/b
     s.phi = phi;
     return s;
 }
 
-// physical flux f(q) . n of Eq. 1, accumulated with weight c into o
-template <typename T>
-__device__ __forceinline__ void add_phys_flux(const FaceNode<T>& s, T n0, T n1, T n2, T c, T (&o)[5]) {
-    const T un = fma(s.u3, n2, fma(s.u2, n1, s.u1 * n0));
-    const T ru = c * s.rho * un;
-    const T cp = c * s.p;
-    o[0] = fma(c, s.rho * un, o[0]);
+// physical flux f(q) . n of Eq. 1, accumulated with sign c (+-1) into o
+template <typename C>
+__device__ __forceinline__ void add_phys_flux(const FaceNode<C>& s, C n0, C n1, C n2, C c, C (&o)[5]) {
+    const C un = c * fma(s.u3, n2, fma(s.u2, n1, s.u1 * n0));
+    const C ru = s.rho * un;
+    const C cp = c * s.p;
+    o[0] = o[0] + ru;
     o[1] = fma(ru, s.u1, fma(cp, n0, o[1]));
     o[2] = fma(ru, s.u2, fma(cp, n1, o[2]));
     o[3] = fma(ru, s.u3, fma(cp, n2, o[3]));
-    o[4] = fma(c * un, s.E + s.p, o[4]);
+    o[4] = fma(un, s.E + s.p, o[4]);
+}
+
+template <typename C>
+struct Consts {
+    C gm1, igm1, c_g, gamma, c_ac, c_en;
+};
+
+// 2 atanh(f)/f = 2 (1 + u/3 + u^2/5 + u^3/7) + O(u^4), u = f^2
+template <typename C>
+__device__ __forceinline__ C atanh_ratio(C u) {
+    return fma(u, fma(u, fma(u, C(2.0 / 7.0), C(2.0 / 5.0)), C(2.0 / 3.0)), C(2.0));
 }
 
 // The interface flux between node i ("-", owning the normal n) and node j
 // ("+").  Returns F_ec + G(i,j) - D for node i in fi and the far node's
 // -F_ec + D + G(i,j) b_i/b_j in fj (its flux with the normal -n).
-template <typename T>
-__device__ __forceinline__ void interface_flux(const FaceNode<T>& I, const FaceNode<T>& J, T n0, T n1, T n2,
-                                               const SurfaceConsts<T>& k, bool dissipation,
-                                               T (&fi)[5], T (&fj)[5]) {
-    // averages
-    const T a1 = T(0.5) * (I.u1 + J.u1), a2 = T(0.5) * (I.u2 + J.u2), a3 = T(0.5) * (I.u3 + J.u3);
-    const T U = fma(a3, n2, fma(a2, n1, a1 * n0));
-    const T rsum = I.rho + J.rho;
-    const T bsum = I.b + J.b;
-    const T phib = T(0.5) * (I.phi + J.phi);
+template <typename C>
+__device__ __forceinline__ void interface_flux(const FaceNode<C>& I, const FaceNode<C>& J, C n0, C n1, C n2,
+                                               const Consts<C>& k, bool dissipation, C (&fi)[5], C (&fj)[5]) {
+    const C a1 = C(0.5) * (I.u1 + J.u1), a2 = C(0.5) * (I.u2 + J.u2), a3 = C(0.5) * (I.u3 + J.u3);
+    const C U = fma(a3, n2, fma(a2, n1, a1 * n0));
+    const C phib = C(0.5) * (I.phi + J.phi);
 
-    // {{rho}}_log: (rho+ - rho-)/(ln rho+ - ln rho-), or the series when close
-    const T dlr = J.lr - I.lr;
-    const bool cr = Num<T>::close(dlr);
-    const T rr = Num<T>::rcp(sel(cr, rsum, dlr));
-    const T tr = (J.rho - I.rho) * rr;
-    const T ur = tr * tr;
-    const T polr = fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
-    const T rho_ln = sel(cr, rsum * polr, tr);
-
-    // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
-    const T db = J.b - I.b;
-    const T dlb = J.lb - I.lb;
-    const bool cb = Num<T>::close(dlb);
-    const T rb = Num<T>::rcp(sel(cb, bsum, db * bsum));
-    const T inv_bsum = sel(cb, rb, db * rb);
-    const T fb = db * inv_bsum;
-    const T ub = fb * fb;
-    const T polb = fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
-    const T inv_bln = sel(cb, inv_bsum * polb, dlb * (bsum * rb));
+    // log means and log jumps of rho and b, with f = (a+ - a-)/(a+ + a-), u = f^2:
+    //   {{a}}_log = {{a}} (1 - u/3 - 4u^2/45 - 44u^3/945) + O(u^4),
+    //   [[ln a]] = 2 atanh(f),  1/{{a}}_log = [[ln a]]/[[a]] = atanh_ratio(u)/(a+ + a-)
+    const C rsum = I.rho + J.rho, drho = J.rho - I.rho;
+    const C irs = Num<C>::rcp(rsum);
+    const C fr = drho * irs;
+    const C ur = fr * fr;
+    const C bsum = I.b + J.b, db = J.b - I.b;
+    const C ibs = Num<C>::rcp(bsum);
+    const C fb = db * ibs;
+    const C ub = fb * fb;
+    const bool cr = Num<C>::close_ratio(fr), cb = Num<C>::close_ratio(fb);
+    const C polr = fma(ur, fma(ur, fma(ur, C(-22.0 / 945.0), C(-2.0 / 45.0)), C(-1.0 / 6.0)), C(0.5));
+    const C polb = atanh_ratio(ub);
+    C rho_ln = rsum * polr;
+    C inv_bln = ibs * polb;
+    C dlr = fr * atanh_ratio(ur);
+    C dlb = fb * polb;
+    if (!__all_sync(__activemask(), cr && cb)) {
+        // a far pair in this warp: logarithms for all its lanes, selected per lane
+        const C lr = Num<C>::log_(J.rho) - Num<C>::log_(I.rho);
+        const C lb = Num<C>::log_(J.b) - Num<C>::log_(I.b);
+        rho_ln = sel(cr, rho_ln, drho * Num<C>::rcp(sel(cr, C(1.0), lr)));
+        inv_bln = sel(cb, inv_bln, lb * Num<C>::rcp(sel(cb, C(1.0), db)));
+        dlr = sel(cr, dlr, lr);
+        dlb = sel(cb, dlb, lb);
+    }
 
     // entropy-conserving flux (Eqs. 3-4) and the gravity term (Eq. 5)
-    const T p_hat = T(0.5) * rsum * inv_bsum;  // {{rho}}/(2{{b}})
-    const T Fr = rho_ln * U;
-    const T aa = fma(a3, a3, fma(a2, a2, a1 * a1));
-    const T uu_avg = T(0.5) * (I.uu + J.uu);
-    const T FE = fma(Fr, fma(k.c_g, inv_bln, fma(T(-0.5), uu_avg, phib + aa)), U * p_hat);
-    // G(i,j) = 1/2 rho_ln {{b}} (phi_j - phi_i)/b_i n
-    const T gq = T(0.25) * rho_ln * bsum * (J.phi - I.phi);
-    const T gi = gq * Num<T>::rcp(I.b);
-    const T gj = gq * Num<T>::rcp(J.b);
+    const C p_hat = C(0.5) * rsum * ibs;  // {{rho}}/(2{{b}})
+    const C Fr = rho_ln * U;
+    const C aa = fma(a3, a3, fma(a2, a2, a1 * a1));
+    const C uu_avg = C(0.5) * (I.uu + J.uu);
+    const C FE = fma(Fr, fma(k.c_g, inv_bln, fma(C(-0.5), uu_avg, phib + aa)), U * p_hat);
+    // G(i,j) = 1/2 rho_ln {{b}} (phi_j - phi_i)/b_i n;  the far side's is G(i,j) b_i/b_j
+    const C gq = C(0.25) * rho_ln * bsum * (J.phi - I.phi);
+    const C gi = gq * I.ib;
+    const C gj = gq * J.ib;
 
-    T D0 = T(0), D1 = T(0), D2 = T(0), D3 = T(0), D4 = T(0);
+    C D0 = C(0.0), D1 = C(0.0), D2 = C(0.0), D3 = C(0.0), D4 = C(0.0);
     if (dissipation) {
-        // averaged state and its sound speed and total enthalpy
-        const T a_sq = k.gamma * p_hat * Num<T>::rcp(rho_ln);
-        const T a = sqrt_(a_sq);
-        const T a_sq_g = a_sq * k.igm1;                  // a^2/(gamma-1)
-        const T ke = fma(T(0.5), aa, phib);              // |u|^2/2 + phi
-        const T H = a_sq_g + ke;
-        // jump of the entropy variables w = ((gamma-s)/(gamma-1) - b|u|^2 + 2 b phi, 2 b u, -2 b),
-        // with [[s]] = (1 - gamma)[[ln rho]] - [[ln b]]
-        const T d1 = fma(dlb, k.igm1, dlr) - (J.b * fma(T(-2.0), J.phi, J.uu) - I.b * fma(T(-2.0), I.phi, I.uu));
-        const T dm1 = T(2.0) * (J.b * J.u1 - I.b * I.u1);
-        const T dm2 = T(2.0) * (J.b * J.u2 - I.b * I.u2);
-        const T dm3 = T(2.0) * (J.b * J.u3 - I.b * I.u3);
-        const T d5 = T(-2.0) * db;
+        // averaged state: sound speed and total enthalpy
+        const C a_sq = k.gamma * p_hat * Num<C>::rcp(rho_ln);
+        const C a = sqrt_(a_sq);
+        const C a_sq_g = a_sq * k.igm1;  // a^2/(gamma-1)
+        const C ke = fma(C(0.5), aa, phib);  // |u|^2/2 + phi
+        const C H = a_sq_g + ke;
+        // [[w]] for w = ((gamma-s)/(gamma-1) - b|u|^2 + 2 b phi, 2 b u, -2 b),
+        // [[s]] = (1 - gamma)[[ln rho]] - [[ln b]]
+        const C d1 = fma(dlb, k.igm1, dlr) - (J.b * fma(C(-2.0), J.phi, J.uu) - I.b * fma(C(-2.0), I.phi, I.uu));
+        const C dm1 = C(2.0) * (J.b * J.u1 - I.b * I.u1);
+        const C dm2 = C(2.0) * (J.b * J.u2 - I.b * I.u2);
+        const C dm3 = C(2.0) * (J.b * J.u3 - I.b * I.u3);
+        const C d5 = C(-2.0) * db;
         // shear input v = [[w_m]] + u [[w_5]] and its normal part
-        const T v1 = fma(a1, d5, dm1), v2 = fma(a2, d5, dm2), v3 = fma(a3, d5, dm3);
-        const T vn = fma(v3, n2, fma(v2, n1, v1 * n0));  // n . v (n unnormalised)
-        const T nsq = fma(n2, n2, fma(n1, n1, n0 * n0));
-        const T inn = Num<T>::rcp(sqrt_(nsq));
-        const T nn = nsq * inn;
-        const T inn2 = inn * inn;
-        // wave strengths: beta = r_acoustic-common . [[w]]
-        const T beta = fma(H, d5, fma(a3, dm3, fma(a2, dm2, fma(a1, dm1, d1))));
-        const T alpha_e = fma(-a_sq_g, d5, beta);
-        const T anu = a * vn * inn;
-        const T lam_p = fabs(fma(a, nn, U)) * rho_ln * k.c_ac;
-        const T lam_m = fabs(fma(-a, nn, U)) * rho_ln * k.c_ac;
-        const T aU = fabs(U);
-        const T cp_ = lam_p * (beta + anu);
-        const T cm_ = lam_m * (beta - anu);
-        const T ce = aU * rho_ln * k.c_en * alpha_e;
-        const T ls = aU * p_hat;
-        const T csum = cp_ + cm_;
-        const T cdif = (cp_ - cm_) * a * inn;
-        const T c0 = csum + ce;
-        const T svn = ls * vn * inn2;
-        D0 = T(0.5) * c0;
-        D1 = T(0.5) * (fma(c0, a1, fma(cdif, n0, ls * v1)) - svn * n0);
-        D2 = T(0.5) * (fma(c0, a2, fma(cdif, n1, ls * v2)) - svn * n1);
-        D3 = T(0.5) * (fma(c0, a3, fma(cdif, n2, ls * v3)) - svn * n2);
-        const T uv = fma(a3, v3, fma(a2, v2, a1 * v1));
-        D4 = T(0.5) * (fma(csum, H, fma(cdif, U, fma(ce, ke, ls * uv))) - svn * U);
+        const C v1 = fma(a1, d5, dm1), v2 = fma(a2, d5, dm2), v3 = fma(a3, d5, dm3);
+        const C vn = fma(v3, n2, fma(v2, n1, v1 * n0));  // n . v (n unnormalised)
+        const C nsq = fma(n2, n2, fma(n1, n1, n0 * n0));
+        const C nn = sqrt_(nsq);
+        const C inn = Num<C>::rcp(nn);
+        const C inn2 = inn * inn;
+        // wave strengths
+        const C beta = fma(H, d5, fma(a3, dm3, fma(a2, dm2, fma(a1, dm1, d1))));
+        const C alpha_e = fma(-a_sq_g, d5, beta);
+        const C anu = a * vn * inn;
+        const C rc = rho_ln * k.c_ac;
+        const C lam_p = fabs(fma(a, nn, U)) * rc;
+        const C lam_m = fabs(fma(-a, nn, U)) * rc;
+        const C aU = fabs(U);
+        const C cp_ = lam_p * (beta + anu);
+        const C cm_ = lam_m * (beta - anu);
+        const C ce = aU * rho_ln * k.c_en * alpha_e;
+        const C ls = aU * p_hat;
+        const C csum = cp_ + cm_;
+        const C cdif = (cp_ - cm_) * a * inn;
+        const C c0 = csum + ce;
+        const C svn = ls * vn * inn2;
+        D0 = C(0.5) * c0;
+        D1 = C(0.5) * (fma(c0, a1, fma(cdif, n0, ls * v1)) - svn * n0);
+        D2 = C(0.5) * (fma(c0, a2, fma(cdif, n1, ls * v2)) - svn * n1);
+        D3 = C(0.5) * (fma(c0, a3, fma(cdif, n2, ls * v3)) - svn * n2);
+        const C uv = fma(a3, v3, fma(a2, v2, a1 * v1));
+        D4 = C(0.5) * (fma(csum, H, fma(cdif, U, fma(ce, ke, ls * uv))) - svn * U);
     }
 
     // momentum: F_rho {{u}} + p_hat n (+ gravity, scaled per side)
-    const T m1 = fma(Fr, a1, p_hat * n0), m2 = fma(Fr, a2, p_hat * n1), m3 = fma(Fr, a3, p_hat * n2);
+    const C m1 = fma(Fr, a1, p_hat * n0), m2 = fma(Fr, a2, p_hat * n1), m3 = fma(Fr, a3, p_hat * n2);
     fi[0] = Fr - D0;
     fi[1] = fma(gi, n0, m1) - D1;
     fi[2] = fma(gi, n1, m2) - D2;
@@ -190,7 +213,8 @@ __device__ __forceinline__ int face_node(int A, int s1, int s2) {
 }
 
 template <typename T>
-__device__ __forceinline__ void load_node(const SurfaceArgs<T>& a, long long g, int dir, T (&q)[5], T& phi, T (&n)[3]) {
+__device__ __forceinline__ void load_node(const SurfaceArgs<T>& a, long long g, int dir, T (&q)[5], T& phi,
+                                          T (&n)[3]) {
     const long long st = a.n;
 #pragma unroll
     for (int v = 0; v < 5; ++v) q[v] = __ldg(a.q + v * st + g);
@@ -199,21 +223,29 @@ __device__ __forceinline__ void load_node(const SurfaceArgs<T>& a, long long g, 
     for (int s = 0; s < 3; ++s) n[s] = __ldg(a.Ja + (3 * dir + s) * st + g);
 }
 
-template <typename T>
-__device__ __forceinline__ void add_out(const SurfaceArgs<T>& a, long long g, const T (&f)[5]) {
+template <typename T, typename C>
+__device__ __forceinline__ FaceNode<C> node_from(const T (&q)[5], T phi, C gm1) {
+    using CV = Conv<T, C>;
+    return node_state<C>(CV::in(q[0]), CV::in(q[1]), CV::in(q[2]), CV::in(q[3]), CV::in(q[4]), CV::in(phi), gm1);
+}
+
+template <typename T, typename C>
+__device__ __forceinline__ void add_out(const SurfaceArgs<T>& a, long long g, const C (&f)[5]) {
     const long long st = a.n;
 #pragma unroll
-    for (int v = 0; v < 5; ++v) a.out[v * st + g] = fma(a.inv_w0, f[v], a.out[v * st + g]);
+    for (int v = 0; v < 5; ++v)
+        a.out[v * st + g] = fma(a.inv_w0, Conv<T, C>::out(f[v]), a.out[v * st + g]);
 }
 
 // One thread per slot.  Slots [0, K (N+1)^2): the +xi_DIR face of element e
 // (an interface with the next element, wrapped when periodic, or a wall).
 // Slots beyond: the -xi_DIR faces of the first layer of elements when the
 // direction has walls.
-template <typename T, int N, int DIR>
+template <typename T, typename C, int N, int DIR>
 __global__ void __launch_bounds__(256) surface_kernel(const __grid_constant__ SurfaceArgs<T> a) {
     constexpr int NQ = N + 1;
     constexpr int NF = NQ * NQ;
+    using CV = Conv<T, C>;
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long K = a.Kx * a.Ky * a.Kz;
     const long long Kd[3] = {a.Kx, a.Ky, a.Kz};
@@ -242,13 +274,19 @@ __global__ void __launch_bounds__(256) surface_kernel(const __grid_constant__ Su
     }
     const int s1 = f % NQ, s2 = f / NQ;
     const long long er = (DIR == 0) ? e % a.Kx : (DIR == 1) ? (e / a.Kx) % a.Ky : e / (a.Kx * a.Ky);
-    const SurfaceConsts<T> k = a.k;
     const long long NP3 = (long long)NQ * NQ * NQ;
+    Consts<C> k;
+    k.gm1 = CV::in(a.k.gm1);
+    k.igm1 = CV::in(a.k.igm1);
+    k.c_g = CV::in(a.k.c_g);
+    k.gamma = CV::in(a.k.gamma);
+    k.c_ac = CV::in(a.k.c_ac);
+    k.c_en = CV::in(a.k.c_en);
 
     T qi[5], phii, ni[3];
     const long long gi = e * NP3 + face_node<N, DIR>(plus_face ? N : 0, s1, s2);
     load_node(a, gi, DIR, qi, phii, ni);
-    const FaceNode<T> I = node_state(qi[0], qi[1], qi[2], qi[3], qi[4], phii, k.gm1);
+    const FaceNode<C> I = node_from<T, C>(qi, phii, k.gm1);
     bool bad = !positive(I.rho) || !positive(I.p);
 
     const bool interior = plus_face && (er + 1 < Kd[DIR] || !wall_dir);
@@ -257,38 +295,39 @@ __global__ void __launch_bounds__(256) surface_kernel(const __grid_constant__ Su
         const long long gj = ej * NP3 + face_node<N, DIR>(0, s1, s2);
         T qj[5], phij, nj[3];
         load_node(a, gj, DIR, qj, phij, nj);
-        const FaceNode<T> J = node_state(qj[0], qj[1], qj[2], qj[3], qj[4], phij, k.gm1);
+        const FaceNode<C> J = node_from<T, C>(qj, phij, k.gm1);
         bad |= !positive(J.rho) || !positive(J.p);
-        const T n0 = T(0.5) * (ni[0] + nj[0]), n1 = T(0.5) * (ni[1] + nj[1]), n2 = T(0.5) * (ni[2] + nj[2]);
-        T fi[5], fj[5];
+        const C n0 = CV::in(T(0.5) * (ni[0] + nj[0]));
+        const C n1 = CV::in(T(0.5) * (ni[1] + nj[1]));
+        const C n2 = CV::in(T(0.5) * (ni[2] + nj[2]));
+        C fi[5], fj[5];
         interface_flux(I, J, n0, n1, n2, k, a.dissipation != 0, fi, fj);
         if (a.form == 0) {
-            add_phys_flux(I, ni[0], ni[1], ni[2], T(-1), fi);
-            add_phys_flux(J, nj[0], nj[1], nj[2], T(1), fj);
+            add_phys_flux(I, CV::in(ni[0]), CV::in(ni[1]), CV::in(ni[2]), C(-1.0), fi);
+            add_phys_flux(J, CV::in(nj[0]), CV::in(nj[1]), CV::in(nj[2]), C(1.0), fj);
         }
-        add_out(a, gi, fi);
-        add_out(a, gj, fj);
+        add_out<T, C>(a, gi, fi);
+        add_out<T, C>(a, gj, fj);
     } else {
         // slip wall: mirror ghost (rho, m - 2 (m.n^) n^, E), same phi, outward normal
         const T sg = plus_face ? T(1) : T(-1);
-        const T n0 = sg * ni[0], n1 = sg * ni[1], n2 = sg * ni[2];
-        const T inn = Num<T>::rcp(sqrt_(fma(n2, n2, fma(n1, n1, n0 * n0))));
-        const T h0 = n0 * inn, h1 = n1 * inn, h2 = n2 * inn;
-        const T mn = T(2.0) * fma(qi[3], h2, fma(qi[2], h1, qi[1] * h0));
-        FaceNode<T> G = I;
-        const T un2 = mn * Num<T>::rcp(qi[0]);
+        const C n0 = CV::in(sg * ni[0]), n1 = CV::in(sg * ni[1]), n2 = CV::in(sg * ni[2]);
+        const C inn = Num<C>::rcp(sqrt_(fma(n2, n2, fma(n1, n1, n0 * n0))));
+        const C h0 = n0 * inn, h1 = n1 * inn, h2 = n2 * inn;
+        const C un2 = C(2.0) * fma(I.u3, h2, fma(I.u2, h1, I.u1 * h0));
+        FaceNode<C> G = I;
         G.u1 = fma(-un2, h0, I.u1);
         G.u2 = fma(-un2, h1, I.u2);
         G.u3 = fma(-un2, h2, I.u3);
-        T fi[5], fg[5];
+        C fi[5], fg[5];
         interface_flux(I, G, n0, n1, n2, k, a.dissipation != 0, fi, fg);
-        if (a.form == 0) add_phys_flux(I, n0, n1, n2, T(-1), fi);
-        add_out(a, gi, fi);
+        if (a.form == 0) add_phys_flux(I, n0, n1, n2, C(-1.0), fi);
+        add_out<T, C>(a, gi, fi);
     }
     if (bad) atomicOr(a.status, 1u);
 }
 
-template <typename T, int N>
+template <typename T, typename C, int N>
 cudaError_t launch_surface_n(const SurfaceArgs<T>& a, cudaStream_t s) {
     constexpr int NF = (N + 1) * (N + 1);
     const long long K = a.Kx * a.Ky * a.Kz;
@@ -297,26 +336,26 @@ cudaError_t launch_surface_n(const SurfaceArgs<T>& a, cudaStream_t s) {
         const long long slots = K * NF + (a.bc[dir] ? (K / Kd[dir]) * NF : 0);
         const long long blocks = (slots + 255) / 256;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        if (dir == 0) surface_kernel<T, N, 0><<<(unsigned)blocks, 256, 0, s>>>(a);
-        else if (dir == 1) surface_kernel<T, N, 1><<<(unsigned)blocks, 256, 0, s>>>(a);
-        else surface_kernel<T, N, 2><<<(unsigned)blocks, 256, 0, s>>>(a);
+        if (dir == 0) surface_kernel<T, C, N, 0><<<(unsigned)blocks, 256, 0, s>>>(a);
+        else if (dir == 1) surface_kernel<T, C, N, 1><<<(unsigned)blocks, 256, 0, s>>>(a);
+        else surface_kernel<T, C, N, 2><<<(unsigned)blocks, 256, 0, s>>>(a);
         const cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
 }
 
-template <typename T>
+template <typename T, typename C>
 cudaError_t launch_surface_any(const SurfaceArgs<T>& a, int N, cudaStream_t s) {
     switch (N) {
-        case 1: return launch_surface_n<T, 1>(a, s);
-        case 2: return launch_surface_n<T, 2>(a, s);
-        case 3: return launch_surface_n<T, 3>(a, s);
-        case 4: return launch_surface_n<T, 4>(a, s);
-        case 5: return launch_surface_n<T, 5>(a, s);
-        case 6: return launch_surface_n<T, 6>(a, s);
-        case 7: return launch_surface_n<T, 7>(a, s);
-        case 8: return launch_surface_n<T, 8>(a, s);
+        case 1: return launch_surface_n<T, C, 1>(a, s);
+        case 2: return launch_surface_n<T, C, 2>(a, s);
+        case 3: return launch_surface_n<T, C, 3>(a, s);
+        case 4: return launch_surface_n<T, C, 4>(a, s);
+        case 5: return launch_surface_n<T, C, 5>(a, s);
+        case 6: return launch_surface_n<T, C, 6>(a, s);
+        case 7: return launch_surface_n<T, C, 7>(a, s);
+        case 8: return launch_surface_n<T, C, 8>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -325,11 +364,15 @@ cudaError_t launch_surface_any(const SurfaceArgs<T>& a, int N, cudaStream_t s) {
 
 #if ESDG_SURF_PREC == 0
 cudaError_t launch_surface_fp64(const SurfaceArgs<double>& a, int N, cudaStream_t s) {
-    return launch_surface_any<double>(a, N, s);
+    return launch_surface_any<double, double>(a, N, s);
+}
+#elif ESDG_SURF_PREC == 1
+cudaError_t launch_surface_fp32(const SurfaceArgs<float>& a, int N, cudaStream_t s) {
+    return launch_surface_any<float, float>(a, N, s);
 }
 #else
-cudaError_t launch_surface_fp32(const SurfaceArgs<float>& a, int N, cudaStream_t s) {
-    return launch_surface_any<float>(a, N, s);
+cudaError_t launch_surface_fp64ff(const SurfaceArgs<double>& a, int N, cudaStream_t s) {
+    return launch_surface_any<double, ff>(a, N, s);
 }
 #endif
 

@@ -139,6 +139,11 @@ struct Num<double> {
         return (static_cast<unsigned>(__double2hiint(d)) & 0x7fffffffu) < 0x3F947AE1u;
     }
     static __device__ __forceinline__ double log_(double x) { return log(x); }
+    // |f| < 0.01 (high word of 0.01 = 0x3F847AE1): for f = (a+ - a-)/(a+ + a-)
+    // this is |ln a+ - ln a-| < 2 atanh(0.01), the same closeness as close()
+    static __device__ __forceinline__ bool close_ratio(double f) {
+        return (static_cast<unsigned>(__double2hiint(f)) & 0x7fffffffu) < 0x3F847AE1u;
+    }
 };
 template <>
 struct Num<float> {
@@ -152,6 +157,10 @@ struct Num<float> {
         return (__float_as_uint(d) & 0x7fffffffu) < 0x3E4CCCCDu;
     }
     static __device__ __forceinline__ float log_(float x) { return logf(x); }
+    // |f| < 0.1 (0x3DCCCCCD), i.e. |ln a+ - ln a-| < 2 atanh(0.1) ~ 0.2
+    static __device__ __forceinline__ bool close_ratio(float f) {
+        return (__float_as_uint(f) & 0x7fffffffu) < 0x3DCCCCCDu;
+    }
 };
 // float-float pair arithmetic (ESDG_FP64_FF): thresholds as in FP64, tested on hi
 template <>
@@ -161,6 +170,9 @@ struct Num<ff> {
         return (__float_as_uint(d.hi) & 0x7fffffffu) < 0x3CA3D70Au;  // |d| < 0.02
     }
     static __device__ __forceinline__ ff log_(ff x) { return ff_log(x); }
+    static __device__ __forceinline__ bool close_ratio(ff f) {
+        return (__float_as_uint(f.hi) & 0x7fffffffu) < 0x3C23D70Au;  // |f| < 0.01
+    }
 };
 // x > 0 (false for NaN), for the non-physical-state check
 __device__ __forceinline__ bool positive(double x) { return x > 0.0; }

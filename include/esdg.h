@@ -164,8 +164,9 @@ int esdg_set_dissipation(esdg_handle h, int on);
  *   out              device, 5*n values (read and written); must not overlap
  *                    an input.
  * Enqueues three kernel launches (one per reference direction) on `stream`;
- * no synchronisation and no allocation.  ESDG_FP64_FF handles run the FP64
- * surface kernel.  Non-physical states set ESDG_STATUS_NONPHYSICAL.
+ * no synchronisation and no allocation.  ESDG_FP64_FF handles run the
+ * surface arithmetic in float-float, like their volume term.  Non-physical
+ * states set ESDG_STATUS_NONPHYSICAL.
  * Errors: ESDG_ERR_ARG, ESDG_ERR_ALIGN, ESDG_ERR_CUDA (launch failure). */
 int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi,
                      void* out, void* stream);
