@@ -75,6 +75,9 @@ BYTES_PER_DOF = {"fp64": 20 * 8, "fp32": 20 * 4, "fp64ff": 20 * 8}  # 15 planes 
 #     dissipation 128, fluxes 31, physical flux 27, accumulation 10 -> 308
 # Values moved per face node: interior 2 x (5 + 1 + 3) read + 2 x 5
 # read-modify-written = 38; wall 9 + 5 + 5 = 19.
+STEP_DT = 1.0e-3  # s; stable on every workload here (timing does not depend on it)
+RK_STAGE_VALUES = 26  # per node: q, rhs, dq read (5 each), J, dq and q written (5 each)
+
 SURF_IFACE_OPS = 340
 SURF_WALL_OPS = 308
 SURF_IFACE_VALUES = 38
@@ -244,7 +247,8 @@ def _setup(cfg, device):
 
     g = wl.generate(cfg, device=device)
     op = fd.VolumeOperator(cfg.Kx, cfg.Ky, cfg.Kz, cfg.N, cfg.precision, bc=cfg.bc)
-    Ja = op.set_geometry(g["x"], g["y"], g["z"])
+    op.J = torch.empty(cfg.n, dtype=op.dtype, device=device)
+    Ja = op.set_geometry(g["x"], g["y"], g["z"], J_out=op.J)
     q = g["q"].to(op.dtype).contiguous()
     phi = g["phi"].to(op.dtype).contiguous()
     del g
@@ -257,16 +261,26 @@ def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier, what="volu
     """Per-call times with CUDA events on the launching stream.
 
     what: "volume" (one launch), "surface" (three launches, accumulating into
-    out) or "rhs" (volume then surface: four launches)."""
+    out), "rhs" (volume then surface: four launches), "step" (one five-stage
+    Runge-Kutta step: 25 launches, on a copy of q) or "stage" (one
+    Runge-Kutta stage update)."""
     import torch
+
+    if what in ("step", "stage"):
+        qs = q.clone()
+        dq = torch.zeros_like(q)
 
     def call():
         if what == "volume":
             op.volume_rhs(q, Ja, phi, out=out, stream=stream)
         elif what == "surface":
             op.surface_rhs(q, Ja, phi, out, stream=stream)
-        else:
+        elif what == "rhs":
             op.rhs(q, Ja, phi, out=out, stream=stream)
+        elif what == "step":
+            op.lsrk_step(qs, dq, out, Ja, phi, op.J, STEP_DT, stream=stream)
+        else:  # one Runge-Kutta stage update (dt = 0 leaves the state unchanged)
+            op.rk_stage(qs, dq, out, op.J, 0.5, 0.5, 0.0, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -464,6 +478,13 @@ def run_ours(args):
             assert op.status() == 0, "non-physical state in the bench inputs"
             res["surface"] = {"ms": slowest(s_total) / args.steps, "per": s_per,
                               "rhs_ms": slowest(r_total) / args.steps}
+            if not args.no_step:
+                st_total, _ = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier,
+                                           what="step")
+                k_total, k_per = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier,
+                                              what="stage")
+                res["step"] = {"ms": slowest(st_total) / args.steps, "stage_ms": slowest(k_total) / args.steps,
+                               "stage_per": k_per}
         if not args.no_e2e:
             e2e_steps = max(3, min(args.steps, 20))
             e_ms, h2d, d2h = _time_e2e(op, q, Ja, phi, out, e2e_steps, 1, stream, barrier)
@@ -549,6 +570,11 @@ def run_ours(args):
     if "surface" in main:
         line["surface"] = _surface_report(cfg, main["surface"], ws, peak64, "FP64 vector", peaks.get("hbm_gbs"))
         line["gpu_launches"] += 7 * args.steps
+    for key, wname in (("main", args.workload), ("fp32", args.fp32_workload), ("fp64ff", args.ff_workload)):
+        if wname and "step" in results[wname]:
+            rep = _step_report(results[wname]["cfg"], results[wname], ws, peaks.get("hbm_gbs"))
+            (line if key == "main" else line[key])["step"] = rep
+            line["gpu_launches"] += 26 * args.steps
     if args.fp32_workload and "surface" in results[args.fp32_workload]:
         r32 = results[args.fp32_workload]
         line["fp32"]["surface"] = _surface_report(r32["cfg"], r32["surface"], ws, fp32_meas, "FP32 vector",
@@ -598,6 +624,24 @@ def _surface_report(cfg, sres, ws, alu_peak_tflops, alu_peak_name, hbm_peak_gbs)
         "rhs": {"what": "volume + surface", "ms_per_step": sres["rhs_ms"], "launches_per_step": 4,
                 "GDOF/s": ws * cfg.n / (sres["rhs_ms"] * 1e-3) / 1e9},
     }
+
+
+def _step_report(cfg, res, ws, hbm_peak_gbs):
+    """One five-stage Runge-Kutta step: time, throughput and per-kernel shares."""
+    st = res["step"]
+    es = 4 if cfg.precision == "fp32" else 8
+    stage_t = statistics.mean(st["stage_per"]) * 1e-3
+    gbs = RK_STAGE_VALUES * es * cfg.n / stage_t / 1e9
+    vol = 5 * res["ms"]
+    srf = 5 * res["surface"]["ms"]
+    rk = 5 * st["stage_ms"]
+    return {"what": "five-stage low-storage Runge-Kutta step (volume + surface + stage update per stage)",
+            "ms_per_step": st["ms"], "launches_per_step": 25,
+            "GDOF/s": ws * cfg.n / (st["ms"] * 1e-3) / 1e9,
+            "shares": {"volume": vol / st["ms"], "surface": srf / st["ms"], "rk_stage": rk / st["ms"]},
+            "rk_stage": {"ms": st["stage_ms"], "bound": "hbm", "achieved_GB/s": gbs, "peak_GB/s": hbm_peak_gbs,
+                         "frac": gbs / hbm_peak_gbs if hbm_peak_gbs else None,
+                         "algorithmic_bytes_per_node": RK_STAGE_VALUES * es}}
 
 
 def run_sweep(args):
@@ -658,6 +702,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-surface", action="store_true", help="skip the surface-term and full-RHS timings")
+    ap.add_argument("--no-step", action="store_true", help="skip the Runge-Kutta step timing")
     ap.add_argument("--no-peaks", action="store_true", help="skip the FMA-throughput peak measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=int, default=256)

@@ -46,6 +46,11 @@ _SIGS = {
     "esdg_set_boundary": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "esdg_set_dissipation": (ctypes.c_int, [_P, ctypes.c_int]),
     "esdg_surface_rhs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
+    "esdg_lsrk_coefficients": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), _P, _P, _P]),
+    "esdg_set_coriolis": (ctypes.c_int, [_P, ctypes.c_double]),
+    "esdg_rk_stage": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_double, ctypes.c_double, ctypes.c_double, _P]),
+    "esdg_lsrk_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_double, _P]),
+    "esdg_diagnostics": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "esdg_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint), _P]),
     "esdg_last_error": (ctypes.c_char_p, [_P]),
     "esdg_get_operators": (ctypes.c_int, [ctypes.c_int, _P, _P, _P]),
@@ -121,6 +126,17 @@ def pair_schedule(N: int, precision: str = "fp64"):
     prec = _PRECISIONS[precision]
     _check(lib.esdg_pair_schedule(N, prec, ctypes.byref(H), partner.ctypes.data, sides.ctypes.data))
     return H.value, partner.reshape(N + 1, -1), sides.reshape(N + 1, -1)
+
+
+def lsrk_coefficients():
+    """(A, B, C) of the library's five-stage low-storage Runge-Kutta scheme (host call)."""
+    lib = load_library()
+    st = ctypes.c_int(0)
+    A = (ctypes.c_double * 5)()
+    B = (ctypes.c_double * 5)()
+    C = (ctypes.c_double * 5)()
+    _check(lib.esdg_lsrk_coefficients(ctypes.byref(st), A, B, C))
+    return list(A)[:st.value], list(B)[:st.value], list(C)[:st.value]
 
 
 def _stream_ptr(stream):
@@ -234,6 +250,40 @@ class VolumeOperator:
         self._req(phi, self.n, name="phi")
         self._req(out, 5 * self.n, name="out")
         _check(self.lib.esdg_surface_rhs(self.h, _dptr(q), _dptr(metrics), _dptr(phi), _dptr(out),
+                                         _stream_ptr(stream)), self.h)
+        return out
+
+    def set_coriolis(self, f: float = 0.0):
+        """f-plane Coriolis parameter (s^-1) of the time-stepping source h."""
+        _check(self.lib.esdg_set_coriolis(self.h, float(f)), self.h)
+        self.coriolis = float(f)
+
+    def rk_stage(self, q, dq, rhs, J, a: float, b: float, dt: float, stream=None):
+        """dq <- a dq + dt (h - rhs/J); q <- q + b dq (in place)."""
+        for t, nm, k in ((q, "q", 5), (dq, "dq", 5), (rhs, "rhs", 5), (J, "J", 1)):
+            self._req(t, k * self.n, name=nm)
+        _check(self.lib.esdg_rk_stage(self.h, _dptr(q), _dptr(dq), _dptr(rhs), _dptr(J), float(a), float(b),
+                                      float(dt), _stream_ptr(stream)), self.h)
+
+    def lsrk_step(self, q, dq, rhs, metrics, phi, J, dt: float, stream=None):
+        """One five-stage step of size dt, in place on q (dq and rhs are scratch)."""
+        for t, nm, k in ((q, "q", 5), (dq, "dq", 5), (rhs, "rhs", 5), (metrics, "metrics", 9),
+                         (phi, "phi", 1), (J, "J", 1)):
+            self._req(t, k * self.n, name=nm)
+        _check(self.lib.esdg_lsrk_step(self.h, _dptr(q), _dptr(dq), _dptr(rhs), _dptr(metrics), _dptr(phi),
+                                       _dptr(J), float(dt), _stream_ptr(stream)), self.h)
+
+    def diagnostics(self, q, J, phi, out=None, stream=None):
+        """(mass, energy, entropy) integrals as a CUDA float64 tensor of 3 values."""
+        import torch
+        self._req(q, 5 * self.n, name="q")
+        self._req(J, self.n, name="J")
+        self._req(phi, self.n, name="phi")
+        if out is None:
+            out = torch.empty(3, dtype=torch.float64, device=q.device)
+        if not (out.is_cuda and out.dtype == torch.float64 and out.numel() >= 3):
+            raise ValueError("out: need a CUDA float64 tensor of at least 3 values")
+        _check(self.lib.esdg_diagnostics(self.h, _dptr(q), _dptr(J), _dptr(phi), _dptr(out),
                                          _stream_ptr(stream)), self.h)
         return out
 

@@ -17,8 +17,10 @@ struct esdg_ctx {
     double gamma = 1.4;
     int bc[3] = {ESDG_BC_PERIODIC, ESDG_BC_PERIODIC, ESDG_BC_PERIODIC};
     int dissipation = 1;
+    double coriolis = 0.0;
     int device = 0;
     unsigned* d_status = nullptr;
+    double* d_partials = nullptr;  // diagnostics scratch, 3 * kDiagBlocks doubles
     double nodes[esdg::kMaxNq];
     double weights[esdg::kMaxNq];
     double D[esdg::kMaxNq * esdg::kMaxNq];
@@ -177,6 +179,42 @@ esdg::SurfaceArgs<T> surface_args(const esdg_ctx* h, const void* q, const void* 
     return a;
 }
 
+// Carpenter & Kennedy (1994), five-stage fourth-order 2N-storage Runge-Kutta
+// scheme: numerator and denominator of A_k, B_k, c_k (exact integers).
+const long double kLsrkA[5][2] = {{0.0L, 1.0L},
+                                  {-567301805773.0L, 1357537059087.0L},
+                                  {-2404267990393.0L, 2016746695238.0L},
+                                  {-3550918686646.0L, 2091501179385.0L},
+                                  {-1275806237668.0L, 842570457699.0L}};
+const long double kLsrkB[5][2] = {{1432997174477.0L, 9575080441755.0L},
+                                  {5161836677717.0L, 13612068292357.0L},
+                                  {1720146321549.0L, 2090206949498.0L},
+                                  {3134564353537.0L, 4481467310338.0L},
+                                  {2277821191437.0L, 14882151754819.0L}};
+const long double kLsrkC[5][2] = {{0.0L, 1.0L},
+                                  {1432997174477.0L, 9575080441755.0L},
+                                  {2526269341429.0L, 6820363962896.0L},
+                                  {2006345519317.0L, 3224310063776.0L},
+                                  {2802321613138.0L, 2924317926251.0L}};
+double lsrk_coef(const long double (&r)[2]) { return (double)(r[0] / r[1]); }
+
+template <typename T>
+esdg::DiagArgs<T> diag_args(const esdg_ctx* h, const void* q, const void* J, const void* phi) {
+    esdg::DiagArgs<T> a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = static_cast<const T*>(q);
+    a.J = static_cast<const T*>(J);
+    a.phi = static_cast<const T*>(phi);
+    a.n = h->n;
+    a.Nq = h->Nq;
+    a.np3 = h->Nq * h->Nq * h->Nq;
+    a.gamma = h->gamma;
+    a.gm1 = h->gamma - 1.0;
+    for (int k = 0; k < h->Nq; ++k) a.w[k] = h->weights[k];
+    a.partials = h->d_partials;
+    return a;
+}
+
 cudaError_t dispatch_fp64(int N, const esdg::VolumeArgs<double>& a, cudaStream_t s) {
     switch (N) {
         case 1: return esdg::launch_volume_fp64_n1(a, s);
@@ -298,9 +336,11 @@ int esdg_create(esdg_handle* out, long Kx, long Ky, long Kz, int N, int precisio
     cudaError_t e = cudaGetDevice(&h->device);
     if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_partials, sizeof(double) * 3 * esdg::kDiagBlocks);
     if (e != cudaSuccess) {
         std::string msg = std::string("device status word: ") + cudaGetErrorString(e);
         if (h->d_status) cudaFree(h->d_status);
+        if (h->d_partials) cudaFree(h->d_partials);
         delete h;
         return fail(nullptr, ESDG_ERR_CUDA, msg);
     }
@@ -311,6 +351,7 @@ int esdg_create(esdg_handle* out, long Kx, long Ky, long Kz, int N, int precisio
 int esdg_destroy(esdg_handle h) {
     if (!h) return ESDG_OK;
     if (h->d_status) cudaFree(h->d_status);
+    if (h->d_partials) cudaFree(h->d_partials);
     delete h;
     return ESDG_OK;
 }
@@ -408,6 +449,80 @@ int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const vo
     else
         e = esdg::launch_surface_fp64(surface_args<double>(h, q, metrics, phi, out), h->N, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "surface kernel launch");
+    return ESDG_OK;
+}
+
+int esdg_lsrk_coefficients(int* stages, double* A, double* B, double* C) {
+    if (!stages) return fail(nullptr, ESDG_ERR_ARG, "stages is NULL");
+    *stages = 5;
+    for (int k = 0; k < 5; ++k) {
+        if (A) A[k] = lsrk_coef(kLsrkA[k]);
+        if (B) B[k] = lsrk_coef(kLsrkB[k]);
+        if (C) C[k] = lsrk_coef(kLsrkC[k]);
+    }
+    return ESDG_OK;
+}
+
+int esdg_set_coriolis(esdg_handle h, double f) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (!(f == f) || f > 1.0 || f < -1.0) return fail(h, ESDG_ERR_ARG, "|f| must be at most 1 s^-1");
+    h->coriolis = f;
+    return ESDG_OK;
+}
+
+int esdg_rk_stage(esdg_handle h, void* q, void* dq, const void* rhs, const void* J, double a, double b, double dt,
+                  void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (!q || !dq || !rhs || !J) return fail(h, ESDG_ERR_ARG, "null device pointer");
+    if (!aligned16(q) || !aligned16(dq) || !aligned16(rhs) || !aligned16(J))
+        return fail(h, ESDG_ERR_ALIGN, "device pointers must be 16-byte aligned");
+    const size_t es = h->precision == ESDG_FP32 ? sizeof(float) : sizeof(double);
+    const size_t nb = es * (size_t)h->n;
+    if (overlaps(q, 5 * nb, dq, 5 * nb) || overlaps(q, 5 * nb, rhs, 5 * nb) || overlaps(dq, 5 * nb, rhs, 5 * nb) ||
+        overlaps(q, 5 * nb, J, nb) || overlaps(dq, 5 * nb, J, nb))
+        return fail(h, ESDG_ERR_ARG, "q, dq, rhs and J must not overlap");
+    if (int rc = check_device(h)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (h->precision == ESDG_FP32) {
+        esdg::RkArgs<float> r{static_cast<float*>(q), static_cast<float*>(dq), static_cast<const float*>(rhs),
+                              static_cast<const float*>(J), h->n, (float)a, (float)b, (float)dt,
+                              (float)h->coriolis};
+        e = esdg::launch_rk_stage(r, s);
+    } else {
+        esdg::RkArgs<double> r{static_cast<double*>(q), static_cast<double*>(dq), static_cast<const double*>(rhs),
+                               static_cast<const double*>(J), h->n, a, b, dt, h->coriolis};
+        e = esdg::launch_rk_stage(r, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "Runge-Kutta stage launch");
+    return ESDG_OK;
+}
+
+int esdg_lsrk_step(esdg_handle h, void* q, void* dq, void* rhs, const void* metrics, const void* phi, const void* J,
+                   double dt, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    for (int k = 0; k < 5; ++k) {
+        if (int rc = esdg_volume_rhs(h, q, metrics, phi, rhs, stream)) return rc;
+        if (int rc = esdg_surface_rhs(h, q, metrics, phi, rhs, stream)) return rc;
+        if (int rc = esdg_rk_stage(h, q, dq, rhs, J, lsrk_coef(kLsrkA[k]), lsrk_coef(kLsrkB[k]), dt, stream))
+            return rc;
+    }
+    return ESDG_OK;
+}
+
+int esdg_diagnostics(esdg_handle h, const void* q, const void* J, const void* phi, double* out3, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (!q || !J || !phi || !out3) return fail(h, ESDG_ERR_ARG, "null device pointer");
+    if (!aligned16(q) || !aligned16(J) || !aligned16(phi))
+        return fail(h, ESDG_ERR_ALIGN, "device pointers must be 16-byte aligned");
+    if (int rc = check_device(h)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (h->precision == ESDG_FP32)
+        e = esdg::launch_diagnostics(diag_args<float>(h, q, J, phi), out3, s);
+    else
+        e = esdg::launch_diagnostics(diag_args<double>(h, q, J, phi), out3, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "diagnostics launch");
     return ESDG_OK;
 }
 

@@ -87,6 +87,38 @@ cudaError_t launch_surface_fp32(const SurfaceArgs<float>& a, int N, cudaStream_t
 // FP64 buffers, float-float arithmetic
 cudaError_t launch_surface_fp64ff(const SurfaceArgs<double>& a, int N, cudaStream_t s);
 
+// One stage of the 2N-storage Runge-Kutta update (all pointers device, planes
+// of stride n): dq <- A dq + dt (h - rhs/J), q <- q + B dq.
+template <typename T>
+struct RkArgs {
+    T* q;              // 5 planes
+    T* dq;             // 5 planes
+    const T* rhs;      // 5 planes: volume + surface
+    const T* J;        // 1 plane
+    long long n;
+    T A, B, dt;
+    T coriolis;        // f of the f-plane source (0, f rho u2, -f rho u1, 0, 0)
+};
+template <typename T>
+cudaError_t launch_rk_stage(const RkArgs<T>& a, cudaStream_t s);
+
+// Global integrals (mass, total energy, entropy) with a fixed two-level
+// reduction over kDiagBlocks CTAs.
+constexpr int kDiagBlocks = 608;
+template <typename T>
+struct DiagArgs {
+    const T* q;
+    const T* J;
+    const T* phi;
+    long long n;
+    int Nq, np3;
+    double gamma, gm1;
+    double w[kMaxNq];  // LGL weights
+    double* partials;  // 3 * kDiagBlocks doubles
+};
+template <typename T>
+cudaError_t launch_diagnostics(const DiagArgs<T>& a, double* out, cudaStream_t s);
+
 // Geometry: curl-form metrics in FP64 from node coordinates.
 struct GeometryArgs {
     const double* x;

@@ -79,8 +79,9 @@ enum {
 
 /* Create a handle for a mesh of Kx*Ky*Kz elements of order N (1..8).
  * Builds the LGL nodes, weights and differentiation matrix (Sec. 3) on the
- * host in long double.  Allocates host memory and one 4-byte device status
- * word on the current device; the handle must be used on that device.
+ * host in long double.  Allocates host memory, one 4-byte device status
+ * word and a 14.6 KB diagnostics scratch buffer on the current device; the
+ * handle must be used on that device.
  * Errors: ESDG_ERR_ARG (out == NULL, K < 1 or K*Nq^3 > 2^40),
  * ESDG_ERR_UNSUPPORTED (N, precision or form), ESDG_ERR_CUDA. */
 int esdg_create(esdg_handle* out, long Kx, long Ky, long Kz, int N, int precision, int form);
@@ -170,6 +171,53 @@ int esdg_set_dissipation(esdg_handle h, int on);
  * Errors: ESDG_ERR_ARG, ESDG_ERR_ALIGN, ESDG_ERR_CUDA (launch failure). */
 int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi,
                      void* out, void* stream);
+
+/* ---- time stepping (the semi-discrete system of Eq. 2) -------------------
+ * dq/dt = h - (volume + surface)/J, advanced with the five-stage fourth-order
+ * 2N-storage Runge-Kutta scheme of Carpenter and Kennedy (1994), which the
+ * ESDG GPU paper (Sec. 3) names as the scheme it used before its fourteen-
+ * stage one (whose coefficients it does not print).  h is the f-plane
+ * Coriolis source of Eq. 2's h term: (0, f rho u2, -f rho u1, 0, 0). */
+
+/* The scheme's coefficients: *stages = 5; A, B, C (5 doubles each, any may
+ * be NULL) receive A_k, B_k and the stage times c_k of
+ *     dq <- A_k dq + dt L(q),   q <- q + B_k dq.
+ * Host only.  Errors: ESDG_ERR_ARG (stages NULL). */
+int esdg_lsrk_coefficients(int* stages, double* A, double* B, double* C);
+
+/* Coriolis parameter f in s^-1 (default 0).  Errors: ESDG_ERR_ARG (|f| > 1). */
+int esdg_set_coriolis(esdg_handle h, double f);
+
+/* One Runge-Kutta stage on every node:
+ *     dq <- a dq + dt (h(q) - rhs/J),   q <- q + b dq.
+ *   q    device, 5*n values (read and written).
+ *   dq   device, 5*n values (written; also read unless a == 0, so a first
+ *        stage needs no initialised dq).
+ *   rhs  device, 5*n values (read): volume + surface at q.
+ *   J    device, n values (read): the Jacobian from esdg_set_geometry.
+ * All of the handle's precision (FP64 for ESDG_FP64_FF); none may overlap.
+ * Enqueues one launch on `stream`.  Errors: ESDG_ERR_ARG, ESDG_ERR_ALIGN,
+ * ESDG_ERR_CUDA. */
+int esdg_rk_stage(esdg_handle h, void* q, void* dq, const void* rhs, const void* J, double a, double b,
+                  double dt, void* stream);
+
+/* One full time step of size dt: five stages of esdg_volume_rhs,
+ * esdg_surface_rhs (boundary kinds, dissipation and form of the handle) and
+ * esdg_rk_stage, i.e. 25 launches on `stream`, no synchronisation, no
+ * allocation (so the call can be captured into a CUDA graph).  rhs is
+ * scratch (5*n values).  Errors: as the three calls. */
+int esdg_lsrk_step(esdg_handle h, void* q, void* dq, void* rhs, const void* metrics, const void* phi,
+                   const void* J, double dt, void* stream);
+
+/* Global integrals of the state, written to out3 (device, 3 doubles):
+ * mass sum_i w_i J_i rho_i, total energy sum_i w_i J_i E_i and entropy
+ * sum_i w_i J_i eta_i with eta = -rho s/(gamma-1), s = ln(p rho^-gamma) and
+ * w_i the product of the node's three LGL weights.  FP64 accumulation with a
+ * fixed reduction order (bitwise reproducible); uses the handle's scratch
+ * (so calls on one handle must not run concurrently).  Two launches on
+ * `stream`.  Errors: ESDG_ERR_ARG, ESDG_ERR_ALIGN, ESDG_ERR_CUDA. */
+int esdg_diagnostics(esdg_handle h, const void* q, const void* J, const void* phi, double* out3,
+                     void* stream);
 
 /* Copy the status word to *flags and clear it.  Synchronises `stream`.
  * Errors: ESDG_ERR_ARG, ESDG_ERR_CUDA. */

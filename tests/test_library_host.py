@@ -178,3 +178,26 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(fd, "library_path", lambda: str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         fd.operators(3)
+
+
+def test_library_lsrk_coefficients_are_fourth_order(lib):
+    """The library's own table (C++), checked against the fourth-order conditions
+    in exact arithmetic after reading its doubles back as rationals, and against
+    the oracle's independent transcription of the published rationals."""
+    from fractions import Fraction
+
+    from oracle import lsrk
+    A, B, C = fd.lsrk_coefficients()
+    assert len(A) == len(B) == len(C) == 5
+    for got, want in zip(A + B + C, lsrk.LSRK_A + lsrk.LSRK_B + lsrk.LSRK_C):
+        assert abs(got - float(want)) <= 1e-16 * max(1.0, abs(float(want)))
+    a, b, c = lsrk.butcher_tableau([Fraction(x) for x in A], [Fraction(x) for x in B])
+    S = 5
+    conds = [(sum(b), 1), (sum(b[i] * c[i] for i in range(S)), Fraction(1, 2)),
+             (sum(b[i] * a[i][j] * c[j] for i in range(S) for j in range(S)), Fraction(1, 6)),
+             (sum(b[i] * a[i][j] * a[j][k] * c[k] for i in range(S) for j in range(S) for k in range(S)),
+              Fraction(1, 24))]
+    for got, want in conds:
+        assert abs(float(got - want)) < 1e-12
+    for got, want in zip(c, C):
+        assert abs(float(got) - want) < 1e-12
