@@ -28,15 +28,19 @@ __global__ void __launch_bounds__(256) rk_stage_kernel(const __grid_constant__ R
     const T A = a.A, B = a.B, dt = a.dt, f = a.coriolis;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
-        const T iJ = T(1) / a.J[i];
+        // reciprocal by estimate + Newton (FP64: within 2 ulp), which keeps the
+        // FP64 stage on the memory roofline rather than on the FP64 pipe
+        const T iJ = -Num<T>::rcp(a.J[i]);
         T qv[5], L[5];
 #pragma unroll
         for (int v = 0; v < 5; ++v) {
             qv[v] = a.q[v * n + i];
-            L[v] = -a.rhs[v * n + i] * iJ;
+            L[v] = a.rhs[v * n + i] * iJ;
         }
-        L[1] = fma(f, qv[2], L[1]);
-        L[2] = fma(-f, qv[1], L[2]);
+        if (f != T(0)) {
+            L[1] = fma(f, qv[2], L[1]);
+            L[2] = fma(-f, qv[1], L[2]);
+        }
         // a first stage (A == 0) neither reads dq nor lets its old contents through
 #pragma unroll
         for (int v = 0; v < 5; ++v) {
