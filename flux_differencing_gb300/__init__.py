@@ -48,6 +48,7 @@ _SIGS = {
     "esdg_surface_rhs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "esdg_lsrk_coefficients": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), _P, _P, _P]),
     "esdg_set_coriolis": (ctypes.c_int, [_P, ctypes.c_double]),
+    "esdg_set_reference": (ctypes.c_int, [_P, _P, _P]),
     "esdg_rk_stage": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_double, ctypes.c_double, ctypes.c_double, _P]),
     "esdg_lsrk_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_double, _P]),
     "esdg_diagnostics": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
@@ -252,6 +253,19 @@ class VolumeOperator:
         _check(self.lib.esdg_surface_rhs(self.h, _dptr(q), _dptr(metrics), _dptr(phi), _dptr(out),
                                          _stream_ptr(stream)), self.h)
         return out
+
+    def set_reference(self, rho_ref=None, p_ref=None):
+        """Switch to perturbation variables about (rho_ref, p_ref) (both (n,) CUDA tensors of
+        the handle's dtype), or back to full-state variables with no arguments.  The handle
+        keeps references to the tensors so they stay alive."""
+        if (rho_ref is None) != (p_ref is None):
+            raise ValueError("rho_ref and p_ref must both be given or both be None")
+        if rho_ref is not None:
+            self._req(rho_ref, self.n, name="rho_ref")
+            self._req(p_ref, self.n, name="p_ref")
+        _check(self.lib.esdg_set_reference(self.h, _dptr(rho_ref) if rho_ref is not None else None,
+                                           _dptr(p_ref) if p_ref is not None else None), self.h)
+        self._reference = (rho_ref, p_ref)
 
     def set_coriolis(self, f: float = 0.0):
         """f-plane Coriolis parameter (s^-1) of the time-stepping source h."""

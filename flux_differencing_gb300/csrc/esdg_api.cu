@@ -18,6 +18,8 @@ struct esdg_ctx {
     int bc[3] = {ESDG_BC_PERIODIC, ESDG_BC_PERIODIC, ESDG_BC_PERIODIC};
     int dissipation = 1;
     double coriolis = 0.0;
+    const void* ref_rho = nullptr;  // perturbation variables: reference density and pressure
+    const void* ref_p = nullptr;
     int device = 0;
     unsigned* d_status = nullptr;
     double* d_partials = nullptr;  // diagnostics scratch, 3 * kDiagBlocks doubles
@@ -148,6 +150,8 @@ esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja
     a.c_h = (T)(h->gamma / (2.0 * (h->gamma - 1.0)));
     a.form = h->form;
     a.status = h->d_status;
+    a.rho_ref = static_cast<const T*>(h->ref_rho);
+    a.p_ref = static_cast<const T*>(h->ref_p);
     a.ops = ops;
     return a;
 }
@@ -176,6 +180,8 @@ esdg::SurfaceArgs<T> surface_args(const esdg_ctx* h, const void* q, const void* 
     a.k.c_ac = (T)(1 / (2 * g));
     a.k.c_en = (T)((g - 1) / g);
     a.status = h->d_status;
+    a.rho_ref = static_cast<const T*>(h->ref_rho);
+    a.p_ref = static_cast<const T*>(h->ref_p);
     return a;
 }
 
@@ -205,6 +211,8 @@ esdg::DiagArgs<T> diag_args(const esdg_ctx* h, const void* q, const void* J, con
     a.q = static_cast<const T*>(q);
     a.J = static_cast<const T*>(J);
     a.phi = static_cast<const T*>(phi);
+    a.rho_ref = static_cast<const T*>(h->ref_rho);
+    a.p_ref = static_cast<const T*>(h->ref_p);
     a.n = h->n;
     a.Nq = h->Nq;
     a.np3 = h->Nq * h->Nq * h->Nq;
@@ -460,6 +468,17 @@ int esdg_lsrk_coefficients(int* stages, double* A, double* B, double* C) {
         if (B) B[k] = lsrk_coef(kLsrkB[k]);
         if (C) C[k] = lsrk_coef(kLsrkC[k]);
     }
+    return ESDG_OK;
+}
+
+int esdg_set_reference(esdg_handle h, const void* rho_ref, const void* p_ref) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if ((rho_ref == nullptr) != (p_ref == nullptr))
+        return fail(h, ESDG_ERR_ARG, "rho_ref and p_ref must both be set or both be NULL");
+    if ((rho_ref && !aligned16(rho_ref)) || (p_ref && !aligned16(p_ref)))
+        return fail(h, ESDG_ERR_ALIGN, "device pointers must be 16-byte aligned");
+    h->ref_rho = rho_ref;
+    h->ref_p = p_ref;
     return ESDG_OK;
 }
 

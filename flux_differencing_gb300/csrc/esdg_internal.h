@@ -35,6 +35,8 @@ struct VolumeArgs {
     T c_h;             // gamma / (2 (gamma - 1))
     int form;          // 0: 2D form (diagonal kept), 1: skew form
     unsigned* status;  // device status word (atomicOr of ESDG_STATUS_* bits)
+    const T* rho_ref;  // reference density (1 plane) or nullptr: q is then the full state
+    const T* p_ref;    // reference pressure (1 plane), with rho_ref
     OpTables<T> ops;
 };
 
@@ -79,6 +81,8 @@ struct SurfaceArgs {
     T inv_w0;          // 1 / (LGL end weight)
     SurfaceConsts<T> k;
     unsigned* status;
+    const T* rho_ref;  // as in VolumeArgs
+    const T* p_ref;
 };
 
 // Launch the three direction passes of the surface term (one per launch).
@@ -110,6 +114,8 @@ struct DiagArgs {
     const T* q;
     const T* J;
     const T* phi;
+    const T* rho_ref;  // as in VolumeArgs
+    const T* p_ref;
     long long n;
     int Nq, np3;
     double gamma, gm1;

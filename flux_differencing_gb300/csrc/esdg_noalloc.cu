@@ -78,6 +78,8 @@ cudaError_t launch_noalloc(long K, int N, int form, double gamma, const void* q,
     a.c_h = (T)(gamma / (2.0 * (gamma - 1.0)));
     a.form = form;
     a.status = status;
+    a.rho_ref = nullptr;  // full-state variables
+    a.p_ref = nullptr;
     fill_ops(a.ops, N);
     if constexpr (sizeof(T) == sizeof(double)) {
         switch (N) {

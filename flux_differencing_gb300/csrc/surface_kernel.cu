@@ -53,17 +53,27 @@ struct FaceNode {
     C rho, u1, u2, u3, uu, E, p, b, ib, phi;
 };
 
+// Node state from the conserved variables; with a reference state (perturbed),
+// rho and E are perturbations from (rho_ref, E_ref = p_ref/(gamma-1) +
+// rho_ref phi) and p = p_ref + (gamma-1)(E' - rho|u|^2/2 - rho' phi).
 template <typename C>
-__device__ __forceinline__ FaceNode<C> node_state(C rho, C m1, C m2, C m3, C E, C phi, C gm1) {
+__device__ __forceinline__ FaceNode<C> node_state(C rho_in, C m1, C m2, C m3, C E_in, C phi, C gm1, bool perturbed,
+                                                  C rho_ref, C p_ref) {
     FaceNode<C> s;
+    const C rho = perturbed ? rho_ref + rho_in : rho_in;
     const C irho = Num<C>::rcp(rho);
     s.rho = rho;
     s.u1 = m1 * irho;
     s.u2 = m2 * irho;
     s.u3 = m3 * irho;
     s.uu = fma(s.u3, s.u3, fma(s.u2, s.u2, s.u1 * s.u1));
-    s.E = E;
-    s.p = gm1 * (E - rho * fma(C(0.5), s.uu, phi));
+    if (perturbed) {
+        s.p = fma(gm1, E_in - fma(C(0.5) * rho, s.uu, rho_in * phi), p_ref);
+        s.E = fma(s.p, Num<C>::rcp(gm1), rho * fma(C(0.5), s.uu, phi));
+    } else {
+        s.E = E_in;
+        s.p = gm1 * (E_in - rho * fma(C(0.5), s.uu, phi));
+    }
     s.b = C(0.5) * rho * Num<C>::rcp(s.p);
     s.ib = C(2.0) * s.p * irho;  // 1/b
     s.phi = phi;
@@ -214,19 +224,22 @@ __device__ __forceinline__ int face_node(int A, int s1, int s2) {
 
 template <typename T>
 __device__ __forceinline__ void load_node(const SurfaceArgs<T>& a, long long g, int dir, T (&q)[5], T& phi,
-                                          T (&n)[3]) {
+                                          T (&n)[3], T (&ref)[2]) {
     const long long st = a.n;
 #pragma unroll
     for (int v = 0; v < 5; ++v) q[v] = __ldg(a.q + v * st + g);
     phi = __ldg(a.phi + g);
 #pragma unroll
     for (int s = 0; s < 3; ++s) n[s] = __ldg(a.Ja + (3 * dir + s) * st + g);
+    ref[0] = a.rho_ref ? __ldg(a.rho_ref + g) : T(0);
+    ref[1] = a.rho_ref ? __ldg(a.p_ref + g) : T(0);
 }
 
 template <typename T, typename C>
-__device__ __forceinline__ FaceNode<C> node_from(const T (&q)[5], T phi, C gm1) {
+__device__ __forceinline__ FaceNode<C> node_from(const T (&q)[5], T phi, const T (&ref)[2], C gm1, bool perturbed) {
     using CV = Conv<T, C>;
-    return node_state<C>(CV::in(q[0]), CV::in(q[1]), CV::in(q[2]), CV::in(q[3]), CV::in(q[4]), CV::in(phi), gm1);
+    return node_state<C>(CV::in(q[0]), CV::in(q[1]), CV::in(q[2]), CV::in(q[3]), CV::in(q[4]), CV::in(phi), gm1,
+                         perturbed, CV::in(ref[0]), CV::in(ref[1]));
 }
 
 template <typename T, typename C>
@@ -283,19 +296,20 @@ __global__ void __launch_bounds__(256) surface_kernel(const __grid_constant__ Su
     k.c_ac = CV::in(a.k.c_ac);
     k.c_en = CV::in(a.k.c_en);
 
-    T qi[5], phii, ni[3];
+    const bool perturbed = a.rho_ref != nullptr;
+    T qi[5], phii, ni[3], ri[2];
     const long long gi = e * NP3 + face_node<N, DIR>(plus_face ? N : 0, s1, s2);
-    load_node(a, gi, DIR, qi, phii, ni);
-    const FaceNode<C> I = node_from<T, C>(qi, phii, k.gm1);
+    load_node(a, gi, DIR, qi, phii, ni, ri);
+    const FaceNode<C> I = node_from<T, C>(qi, phii, ri, k.gm1, perturbed);
     bool bad = !positive(I.rho) || !positive(I.p);
 
     const bool interior = plus_face && (er + 1 < Kd[DIR] || !wall_dir);
     if (interior) {
         const long long ej = (er + 1 < Kd[DIR]) ? e + stride : e - (Kd[DIR] - 1) * stride;
         const long long gj = ej * NP3 + face_node<N, DIR>(0, s1, s2);
-        T qj[5], phij, nj[3];
-        load_node(a, gj, DIR, qj, phij, nj);
-        const FaceNode<C> J = node_from<T, C>(qj, phij, k.gm1);
+        T qj[5], phij, nj[3], rj[2];
+        load_node(a, gj, DIR, qj, phij, nj, rj);
+        const FaceNode<C> J = node_from<T, C>(qj, phij, rj, k.gm1, perturbed);
         bad |= !positive(J.rho) || !positive(J.p);
         const C n0 = CV::in(T(0.5) * (ni[0] + nj[0]));
         const C n1 = CV::in(T(0.5) * (ni[1] + nj[1]));

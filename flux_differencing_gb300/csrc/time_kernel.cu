@@ -69,11 +69,20 @@ __global__ void __launch_bounds__(256) diag_partial_kernel(const __grid_constant
         const int nd = (int)(i % a.np3);
         const double w = a.w[nd % Nq] * a.w[(nd / Nq) % Nq] * a.w[nd / (Nq * Nq)];
         const double wJ = w * (double)a.J[i];
-        const double rho = a.q[i];
         const double m1 = a.q[n + i], m2 = a.q[2 * n + i], m3 = a.q[3 * n + i];
-        const double E = a.q[4 * n + i];
         const double phi = a.phi[i];
-        const double p = a.gm1 * (E - 0.5 * (m1 * m1 + m2 * m2 + m3 * m3) / rho - rho * phi);
+        double rho = a.q[i], E = a.q[4 * n + i], p;
+        if (a.rho_ref) {
+            // perturbation variables: rho = rho_ref + rho', E = E_ref + E',
+            // E_ref = p_ref/(gamma-1) + rho_ref phi
+            const double rr = a.rho_ref[i], pr = a.p_ref[i];
+            const double rp = rho, Ep = E;
+            rho = rr + rp;
+            p = pr + a.gm1 * (Ep - 0.5 * (m1 * m1 + m2 * m2 + m3 * m3) / rho - rp * phi);
+            E = Ep + pr / a.gm1 + rr * phi;
+        } else {
+            p = a.gm1 * (E - 0.5 * (m1 * m1 + m2 * m2 + m3 * m3) / rho - rho * phi);
+        }
         const double ent = -rho * (log(p) - a.gamma * log(rho)) / a.gm1;
         comp_add(s[0], c[0], wJ * rho);
         comp_add(s[1], c[1], wJ * E);

@@ -531,6 +531,8 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
 #pragma unroll
         for (int k = 0; k < 9; ++k) ja_t[k] = T(0);
         const bool real = t < e_count * NP3;
+        const bool perturbed = a.rho_ref != nullptr;
+        T rr_t = T(0), pr_t = T(0);
         if (real) {
             const long long g = node0 + t;
             const long long n = a.n;
@@ -542,9 +544,19 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             phi_t = __ldg(a.phi + g);
 #pragma unroll
             for (int k = 0; k < 9; ++k) ja_t[k] = __ldg(a.Ja + k * n + g);
+            if (perturbed) {
+                rr_t = __ldg(a.rho_ref + g);
+                pr_t = __ldg(a.p_ref + g);
+            }
         }
-        const P rho = PV::in(rho_t), m1 = PV::in(m1_t), m2 = PV::in(m2_t), m3 = PV::in(m3_t);
+        const P m1 = PV::in(m1_t), m2 = PV::in(m2_t), m3 = PV::in(m3_t);
         const P E = PV::in(E_t), phi = PV::in(phi_t);
+        // perturbation variables: q holds q - (rho_ref, 0, 0, 0, E_ref) with
+        // E_ref = p_ref/(gamma-1) + rho_ref phi, so rho = rho_ref + rho' and
+        // p = p_ref + (gamma-1)(E' - rho|u|^2/2 - rho' phi) without the
+        // cancellation of E against rho phi and p_ref/(gamma-1)
+        const P rho_p = PV::in(rho_t);
+        const P rho = perturbed ? PV::in(rr_t) + rho_p : rho_p;
         P ja[9];
 #pragma unroll
         for (int k = 0; k < 9; ++k) ja[k] = PV::in(ja_t[k]);
@@ -552,7 +564,8 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         const P irho = Num<P>::rcp(rho);
         const P u1 = m1 * irho, u2 = m2 * irho, u3 = m3 * irho;
         const P uu = fma(u3, u3, fma(u2, u2, u1 * u1));
-        P pr = gm1 * (E - rho * fma(P(0.5), uu, phi));
+        P pr = perturbed ? fma(gm1, E - fma(P(0.5) * rho, uu, rho_p * phi), PV::in(pr_t))
+                         : gm1 * (E - rho * fma(P(0.5), uu, phi));
         if (!real) pr = P(0.5) * gm1;  // padding node: finite values, never stored
         bad |= !positive(rho) || !positive(pr);
         const P ipr = Num<P>::rcp(pr);

@@ -172,6 +172,25 @@ int esdg_set_dissipation(esdg_handle h, int on);
 int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi,
                      void* out, void* stream);
 
+/* Perturbation variables (Sec. 5.2 of the ESDG GPU paper attributes its FP32
+ * pressure noise to carrying the full state and names perturbation variables
+ * as the remedy).  After this call every q argument of the handle's
+ * entry points (volume, surface, Runge-Kutta stage and step, diagnostics) is
+ * the perturbation q' = q - (rho_ref, 0, 0, 0, E_ref) from a reference state
+ * at rest, E_ref = p_ref/(gamma-1) + rho_ref phi; the kernels form
+ * rho = rho_ref + rho' and p = p_ref + (gamma-1)(E' - rho|u|^2/2 - rho' phi),
+ * which avoids the cancellation of E against rho phi and p/(gamma-1), and the
+ * time step accumulates the small q' rather than the large q.  The output
+ * (volume + surface) is unchanged in meaning: the divergence of the full
+ * state's fluxes (so dq'/dt = dq/dt).  The reference is typically a
+ * hydrostatic background, but any positive state works.
+ *   rho_ref, p_ref  device, n values each of the handle's precision (read
+ *                   by every later call; the caller keeps them alive), or
+ *                   both NULL to return to full-state variables.
+ * esdg_volume_rhs_noalloc always takes full-state variables.
+ * Errors: ESDG_ERR_ARG (only one pointer NULL), ESDG_ERR_ALIGN. */
+int esdg_set_reference(esdg_handle h, const void* rho_ref, const void* p_ref);
+
 /* ---- time stepping (the semi-discrete system of Eq. 2) -------------------
  * dq/dt = h - (volume + surface)/J, advanced with the five-stage fourth-order
  * 2N-storage Runge-Kutta scheme of Carpenter and Kennedy (1994), which the

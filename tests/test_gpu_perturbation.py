@@ -1,0 +1,124 @@
+"""Perturbation variables about a hydrostatic reference (GPU required).
+
+With esdg_set_reference the kernels take q' = q - (rho_ref, 0, 0, 0, E_ref),
+E_ref = p_ref/(gamma-1) + rho_ref phi, and return the same volume + surface
+term as for the full state q: parity is against the oracle on the full FP64
+state.  The point of the variant (the ESDG GPU paper, Sec. 5.2: FP32 noise
+from full-state variables) is checked on the bubble: over several time steps
+the FP32 density and energy stay much closer to an FP64 run when the small
+perturbations are stored instead of the full state.
+"""
+import numpy as np
+import pytest
+import torch
+
+import flux_differencing_gb300 as fd
+import oracle
+import workloads as wl
+from tests import harness as hz
+from tests import physics as ph
+
+pytestmark = pytest.mark.gpu
+
+GAMMA = 1.4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_ok):
+    fd.load_library(build_if_missing=True)
+
+
+def _perturbation(q, phi, ref):
+    qp = q.clone()
+    qp[0] -= ref["rho_ref"]
+    qp[4] -= ref["p_ref"] / (GAMMA - 1.0) + ref["rho_ref"] * phi
+    return qp
+
+
+def _op(cfg, precision, g, ref=None):
+    op = fd.VolumeOperator(cfg.Kx, cfg.Ky, cfg.Kz, cfg.N, precision, bc=cfg.bc)
+    dg = hz.to_device(g)
+    J = torch.empty(cfg.n, dtype=op.dtype, device="cuda")
+    Ja = op.set_geometry(dg["x"], dg["y"], dg["z"], J_out=J)
+    phi = dg["phi"].to(op.dtype).contiguous()
+    if ref is not None:
+        rr = ref["rho_ref"].to("cuda", op.dtype).contiguous()
+        pr = ref["p_ref"].to("cuda", op.dtype).contiguous()
+        op.set_reference(rr, pr)
+    return op, Ja, J, phi
+
+
+@pytest.mark.parametrize("name,precision", [("bubble_N4", "fp64"), ("bubble_N4", "fp32"),
+                                            ("channel_N7", "fp32"), ("channel_N7", "fp64ff"),
+                                            ("small", "fp64"), ("small", "fp32")])
+def test_perturbation_rhs_parity(name, precision):
+    cfg = (wl.small_config(3, K=(3, 2, 2), warp=True, state="noisy", bc=(0, 1, 1)) if name == "small"
+           else wl.get_config(name))
+    g = wl.generate(cfg)
+    ref = wl.reference_state(cfg)
+    qp = _perturbation(g["q"], g["phi"], ref)
+    op, Ja, J, phi = _op(cfg, precision, g, ref)
+    out = op.rhs(qp.to("cuda", op.dtype).contiguous(), Ja, phi)
+    torch.cuda.synchronize()
+    assert op.status() == 0
+    vref, vs = hz.run_oracle(cfg, g)
+    sref, ss = hz.run_oracle_surface(cfg, g)
+    e, plain = hz.errors(out.double().cpu().numpy(), vref + sref, vs + ss)
+    assert e.max() < hz.TOL[precision], (e, plain)
+
+
+def test_reference_off_is_the_full_state_path():
+    cfg = wl.small_config(4, K=(2, 2, 2), warp=True, state="noisy", bc=(0, 1, 1))
+    g = wl.generate(cfg)
+    op, Ja, J, phi = _op(cfg, "fp64", g)
+    q = g["q"].to("cuda").contiguous()
+    a = op.rhs(q, Ja, phi).clone()
+    ref = wl.reference_state(cfg)
+    op.set_reference(ref["rho_ref"].cuda(), ref["p_ref"].cuda())
+    op.set_reference()
+    b = op.rhs(q, Ja, phi)
+    assert torch.equal(a, b)
+
+
+def test_perturbation_diagnostics():
+    cfg = wl.get_config("bubble_N4")
+    g = wl.generate(cfg)
+    ref = wl.reference_state(cfg)
+    op_full, Ja, J, phi = _op(cfg, "fp64", g)
+    full = op_full.diagnostics(g["q"].cuda().contiguous(), J, phi).cpu().numpy()
+    op_p, Ja2, J2, phi2 = _op(cfg, "fp64", g, ref)
+    pert = op_p.diagnostics(_perturbation(g["q"], g["phi"], ref).cuda().contiguous(), J2, phi2).cpu().numpy()
+    for k in range(3):
+        assert abs(full[k] - pert[k]) <= 1e-13 * abs(full[k]), (k, full[k], pert[k])
+
+
+def test_fp32_perturbation_variables_reduce_time_integration_error():
+    cfg = wl.get_config("bubble_N4")
+    g = wl.generate(cfg)
+    ref = wl.reference_state(cfg)
+    rho, u, p = ph.primitives(g["q"].numpy(), g["phi"].numpy())
+    speed = np.max(np.sqrt(np.sum(u * u, axis=0)) + np.sqrt(GAMMA * p / rho))
+    dt = 0.3 * (1000.0 / 16) / speed / (cfg.N + 1) ** 2
+    steps = 20
+
+    def run(precision, perturbed):
+        op, Ja, J, phi = _op(cfg, precision, g, ref if perturbed else None)
+        q0 = _perturbation(g["q"], g["phi"], ref) if perturbed else g["q"]
+        q = q0.to("cuda", op.dtype).contiguous()
+        dq = torch.zeros_like(q)
+        rhs = torch.empty_like(q)
+        for _ in range(steps):
+            op.lsrk_step(q, dq, rhs, Ja, phi, J, dt)
+        qd = q.double().cpu()
+        if perturbed:  # back to the full state in FP64
+            qd[0] += ref["rho_ref"]
+            qd[4] += ref["p_ref"] / (GAMMA - 1.0) + ref["rho_ref"] * g["phi"]
+        return qd.numpy()
+
+    truth = run("fp64", False)
+    full32 = run("fp32", False)
+    pert32 = run("fp32", True)
+    for c in (0, 4):
+        e_full = np.max(np.abs(full32[c] - truth[c]))
+        e_pert = np.max(np.abs(pert32[c] - truth[c]))
+        assert e_pert < 0.1 * e_full, (c, e_pert, e_full)

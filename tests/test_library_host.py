@@ -201,3 +201,16 @@ def test_library_lsrk_coefficients_are_fourth_order(lib):
         assert abs(float(got - want)) < 1e-12
     for got, want in zip(c, C):
         assert abs(float(got) - want) < 1e-12
+
+
+def test_reference_state_is_the_bubble_background():
+    """Outside the bubble the generated state is exactly the hydrostatic background
+    that reference_state() returns (the perturbation variables vanish there)."""
+    import workloads as wl
+    cfg = wl.get_config("bubble_N4")
+    g = wl.generate(cfg)
+    ref = wl.reference_state(cfg)
+    r = np.sqrt((g["x"].numpy() - 500.0) ** 2 + (g["y"].numpy() - 500.0) ** 2 + (g["z"].numpy() - 350.0) ** 2)
+    outside = r > 260.0
+    assert outside.sum() > cfg.n // 2
+    assert np.array_equal(g["q"][0].numpy()[outside], ref["rho_ref"].numpy()[outside])

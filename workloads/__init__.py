@@ -40,7 +40,7 @@ P0 = 1.0e5
 __all__ = [
     "GAMMA", "GRAV", "R_D", "C_P", "P0",
     "Config", "CONFIGS", "get_config", "small_config", "node_positions",
-    "generate", "generate_elements", "element_subset",
+    "generate", "generate_elements", "element_subset", "reference_state",
 ]
 
 
@@ -327,6 +327,42 @@ def generate(cfg: Config, device="cpu", chunk_elems: int = 1 << 16) -> dict:
         for key in ("x", "y", "z", "phi"):
             out[key][sl] = part[key]
         out["q"][:, sl] = part["q"]
+    return out
+
+
+def reference_state(cfg: Config, device="cpu", chunk_elems: int = 1 << 16) -> dict:
+    """The hydrostatic background of a workload at its nodes, float64:
+    {"rho_ref": (n,), "p_ref": (n,)}.
+
+    bubble: the theta0 = 300 K neutral atmosphere the bubble sits in;
+    channel: the stratified background theta_b(z) with its Exner function
+    (no jet, no thermal-wind correction, no bump).  Other states have no
+    hydrostatic background and get rho_ref = 1, p_ref = 1e5."""
+    out = {"rho_ref": torch.empty(cfg.n, dtype=torch.float64, device=device),
+           "p_ref": torch.empty(cfg.n, dtype=torch.float64, device=device)}
+    n_per = cfg.Nq ** 3
+    draws = _draws(cfg)
+    for e0 in range(0, cfg.K, chunk_elems):
+        e1 = min(cfg.K, e0 + chunk_elems)
+        elems = torch.arange(e0, e1, device=device)
+        _, _, Z = _mesh(cfg, elems, device, draws)
+        if cfg.state == "bubble":
+            theta0 = 300.0
+            exner = 1.0 - GRAV * Z / (C_P * theta0)
+            p = P0 * exner ** (C_P / R_D)
+            rho = p / (R_D * theta0 * exner)
+        elif cfg.state == "channel":
+            theta0, nbv = 300.0, 0.01
+            ez = torch.exp(-nbv * nbv * Z / GRAV)
+            exner = 1.0 + GRAV * GRAV / (C_P * theta0 * nbv * nbv) * (ez - 1.0)
+            p = P0 * exner ** (C_P / R_D)
+            rho = p / (R_D * (theta0 / ez) * exner)
+        else:
+            rho = torch.ones_like(Z)
+            p = torch.full_like(Z, 1.0e5)
+        sl = slice(e0 * n_per, e1 * n_per)
+        out["rho_ref"][sl] = rho.reshape(-1)
+        out["p_ref"][sl] = p.reshape(-1)
     return out
 
 
