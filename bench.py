@@ -253,7 +253,7 @@ def _setup(cfg, device):
     q = g["q"].to(op.dtype).contiguous()
     phi = g["phi"].to(op.dtype).contiguous()
     del g
-    out = torch.empty((5, cfg.n), dtype=op.dtype, device=device)
+    out = torch.zeros((5, cfg.n), dtype=op.dtype, device=device)
     torch.cuda.synchronize(device)
     return op, q, Ja, phi, out
 
@@ -270,6 +270,8 @@ def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier, what="volu
     if what in ("step", "stage"):
         qs = q.clone()
         dq = torch.zeros_like(q)
+    # inputs made on the default stream must be complete before the timing stream reads them
+    torch.cuda.synchronize()
 
     def call():
         if what == "volume":
@@ -482,8 +484,10 @@ def run_ours(args):
             if not args.no_step:
                 st_total, _ = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier,
                                            what="step")
+                assert op.status() == 0, "non-physical state during the Runge-Kutta steps"
                 k_total, k_per = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier,
                                               what="stage")
+                assert op.status() == 0, "non-physical state during the Runge-Kutta stages"
                 res["step"] = {"ms": slowest(st_total) / args.steps, "stage_ms": slowest(k_total) / args.steps,
                                "stage_per": k_per}
         if cfg.precision == "fp32" and not args.no_surface:
@@ -496,6 +500,7 @@ def run_ours(args):
             qp[0] = (q[0].double() - ref["rho_ref"]).to(op.dtype)
             qp[4] = (q[4].double() - (ref["p_ref"] / (GAMMA - 1.0) + ref["rho_ref"] * phi.double())).to(op.dtype)
             op.set_reference(rr, pr)
+            torch.cuda.synchronize()
             pv_total, _ = _time_device(op, qp, Ja, phi, out, args.steps, args.warmup, stream, barrier)
             pr_total, _ = _time_device(op, qp, Ja, phi, out, args.steps, args.warmup, stream, barrier, what="rhs")
             assert op.status() == 0, "non-physical state in the perturbation inputs"
