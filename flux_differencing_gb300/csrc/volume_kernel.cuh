@@ -275,60 +275,83 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
     const T s1 = I.u1 + M.u1, s2 = I.u2 + M.u2, s3 = I.u3 + M.u3;
     const T Un = fma(s3, A2, fma(s2, A1, s1 * A0));
 
-    // {{rho}}_log: (rho+ - rho-)/(ln rho+ - ln rho-), or the series when close.
-    // A warp vote skips the branch no lane of the warp needs (lines of one
-    // direction in one warp are usually all close or all far); a mixed warp
-    // evaluates both and selects.  Each lane computes the same formula either
-    // way, so the result does not depend on the vote.
     const T rsum = I.rho + M.rho;
-    const T drho = M.rho - I.rho;
-    const T dlr = M.lr - I.lr;
-    const auto cr = Num<T>::close(dlr);
-    const T bsum = I.b + M.b;
-    const T db = M.b - I.b;
-    const T dlb = M.lb - I.lb;
-    const auto cb = Num<T>::close(dlb);
-    // the vote pays where the arithmetic is expensive (FP64 pipe, float-float);
-    // the FP32 kernel is issue-bound and measured slower with it (0.215 ->
-    // 0.237 ms on the N = 7 channel), so FP32 always selects
-    constexpr bool VOTE = !std::is_same<T, float>::value;
-    const unsigned mask = VOTE ? __activemask() : 0u;
-    // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945), f = drho/rsum
-    auto series_r = [&](T ur) {
-        return fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
-    };
-    // (2/bsum) atanh(f)/f = (2/bsum)(1 + u/3 + u^2/5 + u^3/7), f = db/bsum
-    auto series_b = [&](T ub) {
-        return fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
-    };
-    T rho_ln;
-    if (VOTE && !__any_sync(mask, cr)) {
-        rho_ln = drho * Num<T>::rcp(dlr);
-    } else if (VOTE && __all_sync(mask, cr)) {
-        const T tr = drho * Num<T>::rcp(rsum);
-        rho_ln = rsum * series_r(tr * tr);
-    } else {
+    T rho_ln, inv_bsum, inv_bln, bsum;
+    if constexpr (std::is_same<T, float>::value) {
+        // FP32: per-lane selects in the original statement order (the vote
+        // below was measured slower for this issue-bound kernel: 0.215 ->
+        // 0.237 ms on the N = 7 channel, and a reordering alone cost 4 %)
+        const T drho = M.rho - I.rho;
+        const T dlr = M.lr - I.lr;
+        const auto cr = Num<T>::close(dlr);
         const T rr = Num<T>::rcp(sel(cr, rsum, dlr));
         const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
-        rho_ln = sel(cr, rsum * series_r(tr * tr), tr);
-    }
+        const T ur = tr * tr;
+        // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945)
+        const T polr = fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
+        rho_ln = sel(cr, rsum * polr, tr);
 
-    // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
-    T inv_bsum, inv_bln;
-    if (VOTE && !__any_sync(mask, cb)) {
-        const T rb = Num<T>::rcp(db * bsum);
-        inv_bsum = db * rb;
-        inv_bln = dlb * (bsum * rb);
-    } else if (VOTE && __all_sync(mask, cb)) {
-        const T rb = Num<T>::rcp(bsum);
-        inv_bsum = rb;
-        const T fb = db * rb;
-        inv_bln = rb * series_b(fb * fb);
-    } else {
+        // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
+        bsum = I.b + M.b;
+        const T db = M.b - I.b;
+        const T dlb = M.lb - I.lb;
+        const auto cb = Num<T>::close(dlb);
         const T rb = Num<T>::rcp(sel(cb, bsum, db * bsum));
         inv_bsum = sel(cb, rb, db * rb);
         const T fb = db * inv_bsum;
-        inv_bln = sel(cb, inv_bsum * series_b(fb * fb), dlb * (bsum * rb));
+        const T ub = fb * fb;
+        // (2/bsum) atanh(f)/f = (2/bsum)(1 + u/3 + u^2/5 + u^3/7)
+        const T polb = fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
+        inv_bln = sel(cb, inv_bsum * polb, dlb * (bsum * rb));
+    } else {
+        // {{rho}}_log: (rho+ - rho-)/(ln rho+ - ln rho-), or the series when close.
+        // A warp vote skips the branch no lane of the warp needs (lines of one
+        // direction in one warp are usually all close or all far); a mixed warp
+        // evaluates both and selects.  Each lane computes the same formula either
+        // way, so the result does not depend on the vote.
+        const T drho = M.rho - I.rho;
+        const T dlr = M.lr - I.lr;
+        const auto cr = Num<T>::close(dlr);
+        bsum = I.b + M.b;
+        const T db = M.b - I.b;
+        const T dlb = M.lb - I.lb;
+        const auto cb = Num<T>::close(dlb);
+        const unsigned mask = __activemask();
+        // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945), f = drho/rsum
+        auto series_r = [&](T ur) {
+            return fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
+        };
+        // (2/bsum) atanh(f)/f = (2/bsum)(1 + u/3 + u^2/5 + u^3/7), f = db/bsum
+        auto series_b = [&](T ub) {
+            return fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
+        };
+        if (!__any_sync(mask, cr)) {
+            rho_ln = drho * Num<T>::rcp(dlr);
+        } else if (__all_sync(mask, cr)) {
+            const T tr = drho * Num<T>::rcp(rsum);
+            rho_ln = rsum * series_r(tr * tr);
+        } else {
+            const T rr = Num<T>::rcp(sel(cr, rsum, dlr));
+            const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
+            rho_ln = sel(cr, rsum * series_r(tr * tr), tr);
+        }
+
+        // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
+        if (!__any_sync(mask, cb)) {
+            const T rb = Num<T>::rcp(db * bsum);
+            inv_bsum = db * rb;
+            inv_bln = dlb * (bsum * rb);
+        } else if (__all_sync(mask, cb)) {
+            const T rb = Num<T>::rcp(bsum);
+            inv_bsum = rb;
+            const T fb = db * rb;
+            inv_bln = rb * series_b(fb * fb);
+        } else {
+            const T rb = Num<T>::rcp(sel(cb, bsum, db * bsum));
+            inv_bsum = sel(cb, rb, db * rb);
+            const T fb = db * inv_bsum;
+            inv_bln = sel(cb, inv_bsum * series_b(fb * fb), dlb * (bsum * rb));
+        }
     }
 
     // flux scalars, already multiplied by 2Q_{pp'}
