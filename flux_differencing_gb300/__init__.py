@@ -52,6 +52,13 @@ _SIGS = {
     "esdg_rk_stage": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_double, ctypes.c_double, ctypes.c_double, _P]),
     "esdg_lsrk_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_double, _P]),
     "esdg_diagnostics": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
+    "esdg_describe": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                     ctypes.POINTER(ctypes.c_longlong)]),
+    "esdg_pipeline_create": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(_P)]),
+    "esdg_pipeline_submit": (ctypes.c_int, [_P, _P, _P, _P, _P]),
+    "esdg_pipeline_wait": (ctypes.c_int, [_P]),
+    "esdg_pipeline_last_error": (ctypes.c_char_p, [_P]),
+    "esdg_pipeline_destroy": (ctypes.c_int, [_P]),
     "esdg_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint), _P]),
     "esdg_last_error": (ctypes.c_char_p, [_P]),
     "esdg_get_operators": (ctypes.c_int, [ctypes.c_int, _P, _P, _P]),
@@ -127,6 +134,49 @@ def pair_schedule(N: int, precision: str = "fp64"):
     prec = _PRECISIONS[precision]
     _check(lib.esdg_pair_schedule(N, prec, ctypes.byref(H), partner.ctypes.data, sides.ctypes.data))
     return H.value, partner.reshape(N + 1, -1), sides.reshape(N + 1, -1)
+
+
+class Pipeline:
+    """Pipelined volume-term evaluation from host buffers (esdg_pipeline_*).
+
+    submit() enqueues the copies in, the kernel and the copy out on the next of
+    `depth` slots and returns at once; wait() blocks until every submission
+    has completed.  Host tensors should be pinned; keep them unchanged until
+    their submission completes."""
+
+    def __init__(self, op: "VolumeOperator", depth: int = 2):
+        self.op = op
+        self.lib = op.lib
+        p = ctypes.c_void_p()
+        _check(self.lib.esdg_pipeline_create(op.h, int(depth), ctypes.byref(p)))
+        self.p = p
+        self.depth = int(depth)
+
+    def _err(self, rc):
+        if rc != 0:
+            raise EsdgError(rc, self.lib.esdg_pipeline_last_error(self.p).decode())
+
+    def submit(self, q, metrics, phi, out):
+        for t, nm, k in ((q, "q", 5), (metrics, "metrics", 9), (phi, "phi", 1), (out, "out", 5)):
+            if t.is_cuda or t.dtype != self.op.dtype or not t.is_contiguous() or t.numel() != k * self.op.n:
+                raise ValueError(f"{nm}: need a contiguous host {self.op.dtype} tensor with {k * self.op.n} values")
+        self._err(self.lib.esdg_pipeline_submit(self.p, ctypes.c_void_p(q.data_ptr()),
+                                                ctypes.c_void_p(metrics.data_ptr()),
+                                                ctypes.c_void_p(phi.data_ptr()), ctypes.c_void_p(out.data_ptr())))
+
+    def wait(self):
+        self._err(self.lib.esdg_pipeline_wait(self.p))
+
+    def close(self):
+        if getattr(self, "p", None):
+            self.lib.esdg_pipeline_destroy(self.p)
+            self.p = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def lsrk_coefficients():

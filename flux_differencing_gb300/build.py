@@ -36,7 +36,8 @@ def _units():
              ("geometry", os.path.join(CSRC, "geometry.cu"), []),
              ("peak_bench", os.path.join(CSRC, "peak_bench.cu"), []),
              ("esdg_noalloc", os.path.join(CSRC, "esdg_noalloc.cu"), []),
-             ("time", os.path.join(CSRC, "time_kernel.cu"), [])]
+             ("time", os.path.join(CSRC, "time_kernel.cu"), []),
+             ("pipeline", os.path.join(CSRC, "esdg_pipeline.cu"), [])]
     for prec, tag in ((0, "fp64"), (1, "fp32"), (2, "fp64ff")):
         units.append((f"surface_{tag}", os.path.join(CSRC, "surface_kernel.cu"), [f"-DESDG_SURF_PREC={prec}"]))
     for n in range(1, 9):

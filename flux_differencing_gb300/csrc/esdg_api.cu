@@ -545,6 +545,14 @@ int esdg_diagnostics(esdg_handle h, const void* q, const void* J, const void* ph
     return ESDG_OK;
 }
 
+int esdg_describe(esdg_handle h, int* precision, int* N, long long* n) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (precision) *precision = h->precision;
+    if (N) *N = h->N;
+    if (n) *n = h->n;
+    return ESDG_OK;
+}
+
 int esdg_get_status(esdg_handle h, unsigned* flags, void* stream) {
     if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
     if (!flags) return fail(h, ESDG_ERR_ARG, "flags is NULL");

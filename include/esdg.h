@@ -46,6 +46,7 @@ extern "C" {
 #endif
 
 typedef struct esdg_ctx* esdg_handle;
+typedef struct esdg_pipeline_s* esdg_pipeline;
 
 enum {
     ESDG_OK = 0,
@@ -237,6 +238,46 @@ int esdg_lsrk_step(esdg_handle h, void* q, void* dq, void* rhs, const void* metr
  * `stream`.  Errors: ESDG_ERR_ARG, ESDG_ERR_ALIGN, ESDG_ERR_CUDA. */
 int esdg_diagnostics(esdg_handle h, const void* q, const void* J, const void* phi, double* out3,
                      void* stream);
+
+/* Shape of a handle: *precision (ESDG_FP64, ESDG_FP32, ESDG_FP64_FF), order N
+ * and node count n = K (N+1)^3; any output pointer may be NULL.  Host only.
+ * Errors: ESDG_ERR_ARG (null handle). */
+int esdg_describe(esdg_handle h, int* precision, int* N, long long* n);
+
+/* ---- pipelined evaluation from host buffers ------------------------------
+ * For callers whose state lives in host memory.  A pipeline owns `depth`
+ * slots, each with device buffers for q, metrics, phi and out (of the
+ * handle's precision) and a stream; esdg_pipeline_submit enqueues, on the
+ * next slot, the host-to-device copies of the inputs, esdg_volume_rhs and the
+ * copy of the result to out_host, and returns without waiting, so that the
+ * copies of one submission overlap the kernel of another.  Host buffers
+ * should be pinned (cudaHostAlloc / cudaHostRegister) for the copies to be
+ * asynchronous; the caller keeps them unchanged until the submission has
+ * completed: after esdg_pipeline_wait, or once `depth` later submissions have
+ * been made and waited for.  Submissions on one slot run in order; slots run
+ * concurrently.  Not thread-safe. */
+#define ESDG_PIPELINE_MAX_DEPTH 4
+
+/* Allocate the slots (depth in 1..ESDG_PIPELINE_MAX_DEPTH; 29 * n values of
+ * the handle's precision per slot) on the current device.  The handle must
+ * outlive the pipeline.  Errors: ESDG_ERR_ARG, ESDG_ERR_CUDA. */
+int esdg_pipeline_create(esdg_handle h, int depth, esdg_pipeline* out);
+
+/* Enqueue one volume-term evaluation from host buffers (layouts as in
+ * esdg_volume_rhs): q_host 5*n, metrics_host 9*n, phi_host n values (read),
+ * out_host 5*n values (written when the submission completes).
+ * Errors: ESDG_ERR_ARG, ESDG_ERR_CUDA, and the errors of esdg_volume_rhs. */
+int esdg_pipeline_submit(esdg_pipeline p, const void* q_host, const void* metrics_host, const void* phi_host,
+                         void* out_host);
+
+/* Wait for every submission made so far.  Errors: ESDG_ERR_ARG, ESDG_ERR_CUDA. */
+int esdg_pipeline_wait(esdg_pipeline p);
+
+/* Description of the pipeline's last error (never NULL). */
+const char* esdg_pipeline_last_error(esdg_pipeline p);
+
+/* Wait for outstanding work and free the slots.  Accepts NULL. */
+int esdg_pipeline_destroy(esdg_pipeline p);
 
 /* Copy the status word to *flags and clear it.  Synchronises `stream`.
  * Errors: ESDG_ERR_ARG, ESDG_ERR_CUDA. */

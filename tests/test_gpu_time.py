@@ -156,3 +156,23 @@ def test_lsrk_step_in_a_cuda_graph():
         graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(q_e, q_g)
+
+
+@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+def test_pipeline_from_host_buffers(precision):
+    """esdg_pipeline_*: several submissions from pinned host buffers, overlapping,
+    each giving the same bits as esdg_volume_rhs on device buffers."""
+    cfg = wl.small_config(5, K=(3, 2, 2), warp=True, state="noisy", precision=precision)
+    g, op, Ja, J, q, phi = _setup(cfg)
+    ref = op.volume_rhs(q, Ja, phi).cpu()
+    hq, hJ, hp = q.cpu().pin_memory(), Ja.cpu().pin_memory(), phi.cpu().pin_memory()
+    outs = [torch.zeros(q.shape, dtype=q.dtype).pin_memory() for _ in range(5)]
+    pipe = fd.Pipeline(op, depth=3)
+    for o in outs:
+        pipe.submit(hq, hJ, hp, o)
+    pipe.wait()
+    pipe.close()
+    for o in outs:
+        assert torch.equal(o, ref)
+    with pytest.raises(ValueError):
+        fd.Pipeline(op, 2).submit(q, Ja, phi, outs[0])  # device tensors are refused
