@@ -59,6 +59,7 @@ _SIGS = {
     "esdg_pipeline_wait": (ctypes.c_int, [_P]),
     "esdg_pipeline_last_error": (ctypes.c_char_p, [_P]),
     "esdg_pipeline_destroy": (ctypes.c_int, [_P]),
+    "esdg_rhs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "esdg_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint), _P]),
     "esdg_last_error": (ctypes.c_char_p, [_P]),
     "esdg_get_operators": (ctypes.c_int, [ctypes.c_int, _P, _P, _P]),
@@ -352,9 +353,17 @@ class VolumeOperator:
         return out
 
     def rhs(self, q, metrics, phi, out=None, stream=None):
-        """Volume + surface term (5, n): dq/dt = -rhs/J."""
-        out = self.volume_rhs(q, metrics, phi, out=out, stream=stream)
-        return self.surface_rhs(q, metrics, phi, out, stream=stream)
+        """Volume + surface term (5, n) through esdg_rhs: dq/dt = h - rhs/J."""
+        import torch
+        self._req(q, 5 * self.n, name="q")
+        self._req(metrics, 9 * self.n, name="metrics")
+        self._req(phi, self.n, name="phi")
+        if out is None:
+            out = torch.empty((5, self.n), dtype=self.dtype, device=q.device)
+        self._req(out, 5 * self.n, name="out")
+        _check(self.lib.esdg_rhs(self.h, _dptr(q), _dptr(metrics), _dptr(phi), _dptr(out), _stream_ptr(stream)),
+               self.h)
+        return out
 
     def status(self, stream=None) -> int:
         """Read and clear the status word (synchronises the stream)."""

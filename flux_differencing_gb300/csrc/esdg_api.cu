@@ -136,7 +136,7 @@ void fill_tables(esdg::OpTables<T>& t, int N, const double* w, const double* D) 
 
 template <typename T>
 esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja, const void* phi, void* out,
-                                long long e0, long long e1, const esdg::OpTables<T>& ops) {
+                                long long e0, long long e1, const esdg::OpTables<T>& ops, int form) {
     esdg::VolumeArgs<T> a;
     a.q = static_cast<const T*>(q);
     a.Ja = static_cast<const T*>(Ja);
@@ -148,7 +148,7 @@ esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja
     a.gm1 = (T)(h->gamma - 1.0);
     a.c_g = (T)(1.0 / (2.0 * (h->gamma - 1.0)));
     a.c_h = (T)(h->gamma / (2.0 * (h->gamma - 1.0)));
-    a.form = h->form;
+    a.form = form;
     a.status = h->d_status;
     a.rho_ref = static_cast<const T*>(h->ref_rho);
     a.p_ref = static_cast<const T*>(h->ref_p);
@@ -157,7 +157,8 @@ esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja
 }
 
 template <typename T>
-esdg::SurfaceArgs<T> surface_args(const esdg_ctx* h, const void* q, const void* Ja, const void* phi, void* out) {
+esdg::SurfaceArgs<T> surface_args(const esdg_ctx* h, const void* q, const void* Ja, const void* phi, void* out,
+                                  int form) {
     esdg::SurfaceArgs<T> a;
     std::memset(&a, 0, sizeof(a));
     a.q = static_cast<const T*>(q);
@@ -169,7 +170,7 @@ esdg::SurfaceArgs<T> surface_args(const esdg_ctx* h, const void* q, const void* 
     a.Ky = h->Ky;
     a.Kz = h->Kz;
     for (int r = 0; r < 3; ++r) a.bc[r] = h->bc[r];
-    a.form = h->form;
+    a.form = form;
     a.dissipation = h->dissipation;
     a.inv_w0 = (T)(1.0L / (long double)h->weights[0]);
     const long double g = h->gamma;
@@ -392,8 +393,8 @@ int esdg_set_geometry(esdg_handle h, const double* x, const double* y, const dou
     return ESDG_OK;
 }
 
-int esdg_volume_rhs_range(esdg_handle h, long e_begin, long e_count, const void* q, const void* metrics,
-                          const void* phi, void* out, void* stream) {
+static int volume_range(esdg_handle h, long e_begin, long e_count, const void* q, const void* metrics,
+                        const void* phi, void* out, void* stream, int form) {
     if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
     if (!q || !metrics || !phi || !out) return fail(h, ESDG_ERR_ARG, "null device pointer");
     if (e_begin < 0 || e_count < 1 || e_begin + e_count > h->K)
@@ -408,18 +409,24 @@ int esdg_volume_rhs_range(esdg_handle h, long e_begin, long e_count, const void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (h->precision == ESDG_FP64)
-        e = dispatch_fp64(h->N, volume_args<double>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op64), s);
+        e = dispatch_fp64(h->N, volume_args<double>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op64, form), s);
     else if (h->precision == ESDG_FP64_FF)
-        e = dispatch_fp64ff(h->N, volume_args<double>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op64), s);
+        e = dispatch_fp64ff(h->N, volume_args<double>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op64, form), s);
     else
-        e = dispatch_fp32(h->N, volume_args<float>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op32), s);
+        e = dispatch_fp32(h->N, volume_args<float>(h, q, metrics, phi, out, e_begin, e_begin + e_count, h->op32, form), s);
     if (e != cudaSuccess) return cuda_fail(h, e, "volume kernel launch");
     return ESDG_OK;
 }
 
+int esdg_volume_rhs_range(esdg_handle h, long e_begin, long e_count, const void* q, const void* metrics,
+                          const void* phi, void* out, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    return volume_range(h, e_begin, e_count, q, metrics, phi, out, stream, h->form);
+}
+
 int esdg_volume_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream) {
     if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
-    return esdg_volume_rhs_range(h, 0, (long)h->K, q, metrics, phi, out, stream);
+    return volume_range(h, 0, (long)h->K, q, metrics, phi, out, stream, h->form);
 }
 
 int esdg_set_boundary(esdg_handle h, int bc_xi, int bc_eta, int bc_zeta) {
@@ -438,7 +445,8 @@ int esdg_set_dissipation(esdg_handle h, int on) {
     return ESDG_OK;
 }
 
-int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream) {
+static int surface_form(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream,
+                        int form) {
     if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
     if (!q || !metrics || !phi || !out) return fail(h, ESDG_ERR_ARG, "null device pointer");
     if (!aligned16(q) || !aligned16(metrics) || !aligned16(phi) || !aligned16(out))
@@ -451,13 +459,28 @@ int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const vo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (h->precision == ESDG_FP32)
-        e = esdg::launch_surface_fp32(surface_args<float>(h, q, metrics, phi, out), h->N, s);
+        e = esdg::launch_surface_fp32(surface_args<float>(h, q, metrics, phi, out, form), h->N, s);
     else if (h->precision == ESDG_FP64_FF)
-        e = esdg::launch_surface_fp64ff(surface_args<double>(h, q, metrics, phi, out), h->N, s);
+        e = esdg::launch_surface_fp64ff(surface_args<double>(h, q, metrics, phi, out, form), h->N, s);
     else
-        e = esdg::launch_surface_fp64(surface_args<double>(h, q, metrics, phi, out), h->N, s);
+        e = esdg::launch_surface_fp64(surface_args<double>(h, q, metrics, phi, out, form), h->N, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "surface kernel launch");
     return ESDG_OK;
+}
+
+int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    return surface_form(h, q, metrics, phi, out, stream, h->form);
+}
+
+// Volume + surface.  The 2D volume form's diagonal f(q_i).Ja^r(i) at face
+// nodes and the strong surface form's -f(q_i).n_own are equal and opposite,
+// so the sum is the skew volume form plus F* alone: both kernels run in their
+// skew forms, which skips that pair of terms (same result up to rounding).
+int esdg_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream) {
+    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (int rc = volume_range(h, 0, (long)h->K, q, metrics, phi, out, stream, ESDG_FORM_SKEW)) return rc;
+    return surface_form(h, q, metrics, phi, out, stream, ESDG_FORM_SKEW);
 }
 
 int esdg_lsrk_coefficients(int* stages, double* A, double* B, double* C) {
@@ -521,8 +544,7 @@ int esdg_lsrk_step(esdg_handle h, void* q, void* dq, void* rhs, const void* metr
                    double dt, void* stream) {
     if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
     for (int k = 0; k < 5; ++k) {
-        if (int rc = esdg_volume_rhs(h, q, metrics, phi, rhs, stream)) return rc;
-        if (int rc = esdg_surface_rhs(h, q, metrics, phi, rhs, stream)) return rc;
+        if (int rc = esdg_rhs(h, q, metrics, phi, rhs, stream)) return rc;
         if (int rc = esdg_rk_stage(h, q, dq, rhs, J, lsrk_coef(kLsrkA[k]), lsrk_coef(kLsrkB[k]), dt, stream))
             return rc;
     }

@@ -221,9 +221,9 @@ int esdg_set_coriolis(esdg_handle h, double f);
 int esdg_rk_stage(esdg_handle h, void* q, void* dq, const void* rhs, const void* J, double a, double b,
                   double dt, void* stream);
 
-/* One full time step of size dt: five stages of esdg_volume_rhs,
- * esdg_surface_rhs (boundary kinds, dissipation and form of the handle) and
- * esdg_rk_stage, i.e. 25 launches on `stream`, no synchronisation, no
+/* One full time step of size dt: five stages of esdg_rhs (boundary kinds
+ * and dissipation of the handle) and esdg_rk_stage, i.e. 25 launches on
+ * `stream`, no synchronisation, no
  * allocation (so the call can be captured into a CUDA graph).  rhs is
  * scratch (5*n values).  Errors: as the three calls. */
 int esdg_lsrk_step(esdg_handle h, void* q, void* dq, void* rhs, const void* metrics, const void* phi,
@@ -278,6 +278,15 @@ const char* esdg_pipeline_last_error(esdg_pipeline p);
 
 /* Wait for outstanding work and free the slots.  Accepts NULL. */
 int esdg_pipeline_destroy(esdg_pipeline p);
+
+/* The full right-hand side: out = volume + surface (boundary kinds and
+ * dissipation of the handle), dq/dt = h - out/J.  For ESDG_FORM_2D the volume
+ * diagonal f(q_i).Ja^r(i) at face nodes and the surface term's -f(q_i).n_own
+ * cancel exactly, so both kernels run in their skew forms: the same result as
+ * esdg_volume_rhs followed by esdg_surface_rhs up to rounding, with less
+ * work.  Arguments as esdg_volume_rhs (out written).  Four launches on
+ * `stream`.  Errors: as esdg_volume_rhs. */
+int esdg_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream);
 
 /* Copy the status word to *flags and clear it.  Synchronises `stream`.
  * Errors: ESDG_ERR_ARG, ESDG_ERR_CUDA. */

@@ -161,3 +161,26 @@ def test_surface_argument_errors():
     phi = torch.zeros(n, dtype=torch.float64, device="cuda")
     with pytest.raises(fd.EsdgError):
         op.surface_rhs(q, Ja, phi, q)  # out aliases q
+
+
+@pytest.mark.parametrize("precision", ["fp64", "fp32", "fp64ff"])
+@pytest.mark.parametrize("bc", [(0, 0, 0), (0, 1, 1)])
+def test_rhs_entry_equals_volume_then_surface(precision, bc):
+    """esdg_rhs runs both kernels in their skew forms (the 2D form's volume
+    diagonal and the strong surface correction cancel); it must agree with
+    esdg_volume_rhs followed by esdg_surface_rhs to rounding."""
+    cfg = wl.small_config(4, K=(3, 2, 2), warp=True, state="noisy", precision=precision, bc=bc)
+    g = wl.generate(cfg)
+    op = fd.VolumeOperator(cfg.Kx, cfg.Ky, cfg.Kz, cfg.N, precision, "2d", bc=bc)
+    dg = hz.to_device(g)
+    Ja = op.set_geometry(dg["x"], dg["y"], dg["z"])
+    q = dg["q"].to(op.dtype).contiguous()
+    phi = dg["phi"].to(op.dtype).contiguous()
+    a = op.volume_rhs(q, Ja, phi)
+    op.surface_rhs(q, Ja, phi, a)
+    b = op.rhs(q, Ja, phi)
+    _, vs = hz.run_oracle(cfg, g)
+    _, ss = hz.run_oracle_surface(cfg, g)
+    e, _ = hz.errors(b.double().cpu().numpy(), a.double().cpu().numpy(), vs + ss)
+    eps = 2.0 ** -23 if precision == "fp32" else 2.0 ** -52
+    assert e.max() < 64 * eps, e
