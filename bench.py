@@ -647,7 +647,7 @@ def run_ours(args):
         if wname and "step" in results[wname]:
             rep = _step_report(results[wname]["cfg"], results[wname], ws, peaks.get("hbm_gbs"))
             (line if key == "main" else line[key])["step"] = rep
-            line["gpu_launches"] += 26 * args.steps
+            line["gpu_launches"] += 21 * args.steps
     if args.fp32_workload and "surface" in results[args.fp32_workload]:
         r32 = results[args.fp32_workload]
         line["fp32"]["surface"] = _surface_report(r32["cfg"], r32["surface"], ws, fp32_meas, "FP32 vector",
@@ -705,16 +705,17 @@ def _step_report(cfg, res, ws, hbm_peak_gbs):
     es = 4 if cfg.precision == "fp32" else 8
     stage_t = statistics.mean(st["stage_per"]) * 1e-3
     gbs = RK_STAGE_VALUES * es * cfg.n / stage_t / 1e9
-    vol = 5 * res["ms"]
     srf = 5 * res["surface"]["ms"]
-    rk = 5 * st["stage_ms"]
-    return {"what": "five-stage low-storage Runge-Kutta step (volume + surface + stage update per stage)",
-            "ms_per_step": st["ms"], "launches_per_step": 25,
+    return {"what": "five-stage low-storage Runge-Kutta step: per stage the surface term, then the volume "
+                    "kernel adding it and applying the stage update in its store (esdg_lsrk_step)",
+            "ms_per_step": st["ms"], "launches_per_step": 20,
             "GDOF/s": ws * cfg.n / (st["ms"] * 1e-3) / 1e9,
-            "shares": {"volume": vol / st["ms"], "surface": srf / st["ms"], "rk_stage": rk / st["ms"]},
-            "rk_stage": {"ms": st["stage_ms"], "bound": "hbm", "achieved_GB/s": gbs, "peak_GB/s": hbm_peak_gbs,
-                         "frac": gbs / hbm_peak_gbs if hbm_peak_gbs else None,
-                         "algorithmic_bytes_per_node": RK_STAGE_VALUES * es}}
+            "shares": {"surface": srf / st["ms"], "volume_with_fused_update": 1.0 - srf / st["ms"]},
+            "standalone_rk_stage": {"ms": st["stage_ms"], "bound": "hbm", "achieved_GB/s": gbs,
+                                    "peak_GB/s": hbm_peak_gbs, "frac": gbs / hbm_peak_gbs if hbm_peak_gbs else None,
+                                    "algorithmic_bytes_per_node": RK_STAGE_VALUES * es,
+                                    "note": "esdg_rk_stage on its own; the step fuses this update into the "
+                                            "volume kernel"}}
 
 
 def run_sweep(args):

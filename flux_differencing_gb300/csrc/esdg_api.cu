@@ -138,6 +138,7 @@ template <typename T>
 esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja, const void* phi, void* out,
                                 long long e0, long long e1, const esdg::OpTables<T>& ops, int form) {
     esdg::VolumeArgs<T> a;
+    std::memset(&a, 0, sizeof(a));  // rk_* null: the kernel writes out
     a.q = static_cast<const T*>(q);
     a.Ja = static_cast<const T*>(Ja);
     a.phi = static_cast<const T*>(phi);
@@ -540,14 +541,67 @@ int esdg_rk_stage(esdg_handle h, void* q, void* dq, const void* rhs, const void*
     return ESDG_OK;
 }
 
+// One fused stage: the surface term (skew form) accumulated into S at face
+// nodes, then the volume kernel (skew form) adds it and applies the stage
+// update to dq and q in its store, resetting S to zero where it read it.
+static int fused_stage(esdg_handle h, void* q, void* dq, void* S, const void* metrics, const void* phi,
+                       const void* J, double A, double B, double dt, void* stream) {
+    if (int rc = surface_form(h, q, metrics, phi, S, stream, ESDG_FORM_SKEW)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (h->precision == ESDG_FP32) {
+        auto a = volume_args<float>(h, q, metrics, phi, nullptr, 0, h->K, h->op32, ESDG_FORM_SKEW);
+        a.rk_q = static_cast<float*>(q);
+        a.rk_dq = static_cast<float*>(dq);
+        a.rk_S = static_cast<float*>(S);
+        a.rk_J = static_cast<const float*>(J);
+        a.rk_A = (float)A;
+        a.rk_B = (float)B;
+        a.rk_dt = (float)dt;
+        a.rk_f = (float)h->coriolis;
+        e = dispatch_fp32(h->N, a, s);
+    } else {
+        auto a = volume_args<double>(h, q, metrics, phi, nullptr, 0, h->K, h->op64, ESDG_FORM_SKEW);
+        a.rk_q = static_cast<double*>(q);
+        a.rk_dq = static_cast<double*>(dq);
+        a.rk_S = static_cast<double*>(S);
+        a.rk_J = static_cast<const double*>(J);
+        a.rk_A = A;
+        a.rk_B = B;
+        a.rk_dt = dt;
+        a.rk_f = h->coriolis;
+        e = h->precision == ESDG_FP64_FF ? dispatch_fp64ff(h->N, a, s) : dispatch_fp64(h->N, a, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "volume kernel launch (fused stage)");
+    return ESDG_OK;
+}
+
 int esdg_lsrk_step(esdg_handle h, void* q, void* dq, void* rhs, const void* metrics, const void* phi, const void* J,
                    double dt, void* stream) {
     if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
-    for (int k = 0; k < 5; ++k) {
-        if (int rc = esdg_rhs(h, q, metrics, phi, rhs, stream)) return rc;
-        if (int rc = esdg_rk_stage(h, q, dq, rhs, J, lsrk_coef(kLsrkA[k]), lsrk_coef(kLsrkB[k]), dt, stream))
+    if (!q || !dq || !rhs || !metrics || !phi || !J) return fail(h, ESDG_ERR_ARG, "null device pointer");
+    if (!aligned16(q) || !aligned16(dq) || !aligned16(rhs) || !aligned16(metrics) || !aligned16(phi) ||
+        !aligned16(J))
+        return fail(h, ESDG_ERR_ALIGN, "device pointers must be 16-byte aligned");
+    const size_t es = h->precision == ESDG_FP32 ? sizeof(float) : sizeof(double);
+    const size_t nb = es * (size_t)h->n;
+    const void* ins[4] = {q, dq, rhs, J};
+    const size_t sz[4] = {5 * nb, 5 * nb, 5 * nb, nb};
+    for (int x = 0; x < 4; ++x)
+        for (int y = x + 1; y < 4; ++y)
+            if (overlaps(ins[x], sz[x], ins[y], sz[y])) return fail(h, ESDG_ERR_ARG, "q, dq, rhs and J must not overlap");
+    if (overlaps(q, 5 * nb, metrics, 9 * nb) || overlaps(q, 5 * nb, phi, nb) || overlaps(rhs, 5 * nb, metrics, 9 * nb) ||
+        overlaps(rhs, 5 * nb, phi, nb) || overlaps(dq, 5 * nb, metrics, 9 * nb) || overlaps(dq, 5 * nb, phi, nb))
+        return fail(h, ESDG_ERR_ARG, "q, dq and rhs must not overlap metrics or phi");
+    if (int rc = check_device(h)) return rc;
+    // rhs serves as the face accumulator S: zero at the start, and every stage
+    // leaves it zero again
+    cudaError_t e = cudaMemsetAsync(rhs, 0, 5 * nb, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "clearing the surface accumulator");
+    for (int k = 0; k < 5; ++k)
+        if (int rc = fused_stage(h, q, dq, rhs, metrics, phi, J, lsrk_coef(kLsrkA[k]), lsrk_coef(kLsrkB[k]), dt,
+                                 stream))
             return rc;
-    }
     return ESDG_OK;
 }
 

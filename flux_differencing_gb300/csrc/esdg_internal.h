@@ -37,6 +37,15 @@ struct VolumeArgs {
     unsigned* status;  // device status word (atomicOr of ESDG_STATUS_* bits)
     const T* rho_ref;  // reference density (1 plane) or nullptr: q is then the full state
     const T* p_ref;    // reference pressure (1 plane), with rho_ref
+    // Fused Runge-Kutta stage (rk_q != nullptr): instead of writing out, each
+    // node takes rhs = volume + rk_S (rk_S: the surface term accumulated at
+    // face nodes, consumed and reset to zero there) and applies
+    // dq <- A dq + dt (h - rhs/J), q <- q + B dq to rk_dq and rk_q (== q).
+    T* rk_q;
+    T* rk_dq;
+    T* rk_S;
+    const T* rk_J;
+    T rk_A, rk_B, rk_dt, rk_f;
     OpTables<T> ops;
 };
 

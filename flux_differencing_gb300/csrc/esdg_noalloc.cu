@@ -80,6 +80,11 @@ cudaError_t launch_noalloc(long K, int N, int form, double gamma, const void* q,
     a.status = status;
     a.rho_ref = nullptr;  // full-state variables
     a.p_ref = nullptr;
+    a.rk_q = nullptr;  // writes out
+    a.rk_dq = nullptr;
+    a.rk_S = nullptr;
+    a.rk_J = nullptr;
+    a.rk_A = a.rk_B = a.rk_dt = a.rk_f = T(0);
     fill_ops(a.ops, N);
     if constexpr (sizeof(T) == sizeof(double)) {
         switch (N) {

@@ -379,6 +379,50 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
     t4 = -fE;
 }
 
+// The final write of one node's volume term t0..t4: to out, or, in a fused
+// Runge-Kutta stage, plus the surface term at face nodes, as a stage update of
+// dq and q (the node's own element only, so updating q in place is safe).
+template <typename T, int N>
+__device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, int na, int nb, int nc, T t0,
+                                           T t1, T t2, T t3, T t4) {
+    const long long n = a.n;
+    if (a.rk_q == nullptr) {
+        T* __restrict__ o = a.out;
+        o[0 * n + g] = t0;
+        o[1 * n + g] = t1;
+        o[2 * n + g] = t2;
+        o[3 * n + g] = t3;
+        o[4 * n + g] = t4;
+        return;
+    }
+    T tot[5] = {t0, t1, t2, t3, t4};
+    if (na == 0 || na == N || nb == 0 || nb == N || nc == 0 || nc == N) {
+#pragma unroll
+        for (int v = 0; v < 5; ++v) {
+            tot[v] += a.rk_S[v * n + g];
+            a.rk_S[v * n + g] = T(0);
+        }
+    }
+    const T sc = -a.rk_dt * Num<T>::rcp(a.rk_J[g]);
+    T qv[5], dL[5];
+#pragma unroll
+    for (int v = 0; v < 5; ++v) {
+        qv[v] = a.rk_q[v * n + g];
+        dL[v] = tot[v] * sc;
+    }
+    if (a.rk_f != T(0)) {
+        const T fdt = a.rk_f * a.rk_dt;
+        dL[1] = fma(fdt, qv[2], dL[1]);
+        dL[2] = fma(-fdt, qv[1], dL[2]);
+    }
+#pragma unroll
+    for (int v = 0; v < 5; ++v) {
+        const T d = (a.rk_A == T(0)) ? dL[v] : fma(a.rk_A, a.rk_dq[v * n + g], dL[v]);
+        a.rk_dq[v * n + g] = d;
+        a.rk_q[v * n + g] = fma(a.rk_B, d, qv[v]);
+    }
+}
+
 // One direction phase.  R = 0 (xi), 1 (eta), 2 (zeta).  FINAL = false: add
 // the scaled sum to the shared accumulators; true: add the shared
 // accumulators and store the node's result to global memory.  Offsets
@@ -462,13 +506,11 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         // linear node L*Nq + p is contiguous across lanes: coalesced stores
         static_assert(Layout<N>::ORD0 == 0, "xi lines must be dealt b-fastest");
         const long long g = node0 + (long long)L * NQ + p;
-        T* __restrict__ o = a.out;
-        const long long n = a.n;
-        o[0 * n + g] = Conv<T, C>::out(fma(acc0, iw, s_acc[0 * FS + i]));
-        o[1 * n + g] = Conv<T, C>::out(fma(acc1, iw, s_acc[1 * FS + i]));
-        o[2 * n + g] = Conv<T, C>::out(fma(acc2, iw, s_acc[2 * FS + i]));
-        o[3 * n + g] = Conv<T, C>::out(fma(acc3, iw, s_acc[3 * FS + i]));
-        o[4 * n + g] = Conv<T, C>::out(fma(acc4, iw, s_acc[4 * FS + i]));
+        store_node<T, N>(a, g, ia, ib, ic, Conv<T, C>::out(fma(acc0, iw, s_acc[0 * FS + i])),
+                         Conv<T, C>::out(fma(acc1, iw, s_acc[1 * FS + i])),
+                         Conv<T, C>::out(fma(acc2, iw, s_acc[2 * FS + i])),
+                         Conv<T, C>::out(fma(acc3, iw, s_acc[3 * FS + i])),
+                         Conv<T, C>::out(fma(acc4, iw, s_acc[4 * FS + i])));
     }
 }
 
@@ -705,10 +747,11 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         for (int t = threadIdx.x; t < e_count * NP3; t += LA::THREADS) {
             const int el = t / NP3;
             const int nd = t - el * NP3;
-            const int sl = SL::at(el, nd % NQ, (nd / NQ) % NQ, nd / (NQ * NQ));
+            const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
+            const int sl = SL::at(el, na, nb, nc);
             const long long g = node0 + t;
-#pragma unroll
-            for (int v = 0; v < 5; ++v) a.out[v * a.n + g] = CV::out(s_acc[v * FS + sl]);
+            store_node<T, N>(a, g, na, nb, nc, CV::out(s_acc[0 * FS + sl]), CV::out(s_acc[1 * FS + sl]),
+                             CV::out(s_acc[2 * FS + sl]), CV::out(s_acc[3 * FS + sl]), CV::out(s_acc[4 * FS + sl]));
         }
     } else {
         direction_phase<T, C, N, 1, false>(a, sm, e_count, node0, c8, iw, c_g);
