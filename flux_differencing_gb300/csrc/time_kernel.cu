@@ -26,17 +26,23 @@ template <typename T>
 __global__ void __launch_bounds__(256) rk_stage_kernel(const __grid_constant__ RkArgs<T> a) {
     const long long n = a.n;
     const T A = a.A, B = a.B, dt = a.dt, f = a.coriolis;
+    T* __restrict__ qp = a.q;
+    T* __restrict__ dqp = a.dq;
+    const T* __restrict__ rp = a.rhs;
+    const bool use_dq = A != T(0);
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
         // dt L = dt h + sc rhs with sc = -dt/J; the reciprocal by estimate +
         // Newton (FP64: within 2 ulp).  About 20 FP64 operations per node, which
         // keeps the FP64 stage near the memory roofline on GB300's FP64 pipe.
         const T sc = -dt * Num<T>::rcp(a.J[i]);
-        T qv[5], dL[5];
+        // all loads before any store (the pointers are restrict-qualified)
+        T qv[5], dL[5], dqv[5];
 #pragma unroll
         for (int v = 0; v < 5; ++v) {
-            qv[v] = a.q[v * n + i];
-            dL[v] = a.rhs[v * n + i] * sc;
+            qv[v] = qp[v * n + i];
+            dL[v] = rp[v * n + i] * sc;
+            dqv[v] = use_dq ? dqp[v * n + i] : T(0);
         }
         if (f != T(0)) {
             const T fdt = f * dt;
@@ -46,9 +52,9 @@ __global__ void __launch_bounds__(256) rk_stage_kernel(const __grid_constant__ R
         // a first stage (A == 0) neither reads dq nor lets its old contents through
 #pragma unroll
         for (int v = 0; v < 5; ++v) {
-            const T d = (A == T(0)) ? dL[v] : fma(A, a.dq[v * n + i], dL[v]);
-            a.dq[v * n + i] = d;
-            a.q[v * n + i] = fma(B, d, qv[v]);
+            const T d = use_dq ? fma(A, dqv[v], dL[v]) : dL[v];
+            dqp[v * n + i] = d;
+            qp[v * n + i] = fma(B, d, qv[v]);
         }
     }
 }

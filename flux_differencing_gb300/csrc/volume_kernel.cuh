@@ -395,21 +395,27 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
         o[4 * n + g] = t4;
         return;
     }
-    T tot[5] = {t0, t1, t2, t3, t4};
-    if (na == 0 || na == N || nb == 0 || nb == N || nc == 0 || nc == N) {
-#pragma unroll
-        for (int v = 0; v < 5; ++v) {
-            tot[v] += a.rk_S[v * n + g];
-            a.rk_S[v * n + g] = T(0);
-        }
-    }
-    const T sc = -a.rk_dt * Num<T>::rcp(a.rk_J[g]);
-    T qv[5], dL[5];
+    // every load first, through restrict-qualified pointers: loads interleaved
+    // with stores through possibly aliasing pointers would each wait for DRAM
+    // in turn (measured 1.0 ms against 0.22 ms for the plain FP32 kernel)
+    T* __restrict__ qp = a.rk_q;
+    T* __restrict__ dqp = a.rk_dq;
+    T* __restrict__ Sp = a.rk_S;
+    const bool face = na == 0 || na == N || nb == 0 || nb == N || nc == 0 || nc == N;
+    const bool use_dq = a.rk_A != T(0);
+    T qv[5], dqv[5], sv[5];
 #pragma unroll
     for (int v = 0; v < 5; ++v) {
-        qv[v] = a.rk_q[v * n + g];
-        dL[v] = tot[v] * sc;
+        qv[v] = qp[v * n + g];
+        dqv[v] = use_dq ? dqp[v * n + g] : T(0);
+        sv[v] = face ? Sp[v * n + g] : T(0);
     }
+    const T Jg = a.rk_J[g];
+    const T sc = -a.rk_dt * Num<T>::rcp(Jg);
+    const T tot[5] = {t0, t1, t2, t3, t4};
+    T dL[5];
+#pragma unroll
+    for (int v = 0; v < 5; ++v) dL[v] = (tot[v] + sv[v]) * sc;
     if (a.rk_f != T(0)) {
         const T fdt = a.rk_f * a.rk_dt;
         dL[1] = fma(fdt, qv[2], dL[1]);
@@ -417,9 +423,10 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
     }
 #pragma unroll
     for (int v = 0; v < 5; ++v) {
-        const T d = (a.rk_A == T(0)) ? dL[v] : fma(a.rk_A, a.rk_dq[v * n + g], dL[v]);
-        a.rk_dq[v * n + g] = d;
-        a.rk_q[v * n + g] = fma(a.rk_B, d, qv[v]);
+        const T d = use_dq ? fma(a.rk_A, dqv[v], dL[v]) : dL[v];
+        dqp[v * n + g] = d;
+        qp[v * n + g] = fma(a.rk_B, d, qv[v]);
+        if (face) Sp[v * n + g] = T(0);
     }
 }
 
