@@ -706,11 +706,15 @@ def _step_report(cfg, res, ws, hbm_peak_gbs):
     stage_t = statistics.mean(st["stage_per"]) * 1e-3
     gbs = RK_STAGE_VALUES * es * cfg.n / stage_t / 1e9
     srf = 5 * res["surface"]["ms"]
-    return {"what": "five-stage low-storage Runge-Kutta step: per stage the surface term, then the volume "
-                    "kernel adding it and applying the stage update in its store (esdg_lsrk_step)",
-            "ms_per_step": st["ms"], "launches_per_step": 20,
+    fused = cfg.precision != "fp64"
+    return {"what": "five-stage low-storage Runge-Kutta step (esdg_lsrk_step): per stage "
+                    + ("the surface term, then the volume kernel adding it and applying the stage update "
+                       "in its store" if fused else "volume + surface (esdg_rhs), then the stage kernel"),
+            "ms_per_step": st["ms"], "launches_per_step": 25 if cfg.precision == "fp64" else 20,
             "GDOF/s": ws * cfg.n / (st["ms"] * 1e-3) / 1e9,
-            "shares": {"surface": srf / st["ms"], "volume_with_fused_update": 1.0 - srf / st["ms"]},
+            "shares": ({"surface": srf / st["ms"], "volume_with_fused_update": 1.0 - srf / st["ms"]} if fused else
+                       {"volume": 5 * res["ms"] / st["ms"], "surface": srf / st["ms"],
+                        "rk_stage": 5 * st["stage_ms"] / st["ms"]}),
             "standalone_rk_stage": {"ms": st["stage_ms"], "bound": "hbm", "achieved_GB/s": gbs,
                                     "peak_GB/s": hbm_peak_gbs, "frac": gbs / hbm_peak_gbs if hbm_peak_gbs else None,
                                     "algorithmic_bytes_per_node": RK_STAGE_VALUES * es,

@@ -221,12 +221,14 @@ int esdg_set_coriolis(esdg_handle h, double f);
 int esdg_rk_stage(esdg_handle h, void* q, void* dq, const void* rhs, const void* J, double a, double b,
                   double dt, void* stream);
 
-/* One full time step of size dt: five stages, each the surface term
- * (boundary kinds and dissipation of the handle) followed by the volume
- * kernel in a fused mode that adds the surface term and applies the stage
- * update to dq and q in its store (the same arithmetic as esdg_rhs followed
- * by esdg_rk_stage, without writing and re-reading the right-hand side):
- * 20 launches and one memset on `stream`, no synchronisation, no allocation
+/* One full time step of size dt: five stages of esdg_rhs (boundary kinds
+ * and dissipation of the handle) and esdg_rk_stage.  For ESDG_FP32 and
+ * ESDG_FP64_FF each stage is the surface term followed by the volume kernel
+ * in a fused mode that adds the surface term and applies the stage update to
+ * dq and q in its store, without writing and re-reading the right-hand side
+ * (20 launches and one memset per step); native ESDG_FP64, bound by its FP64
+ * pipe, keeps the separate stage kernel (25 launches).  Everything is on
+ * `stream`, with no synchronisation and no allocation
  * (so the call can be captured into a CUDA graph).  rhs is scratch (5*n
  * values, used as the surface accumulator).  q, dq, rhs and J must not
  * overlap one another, metrics or phi.  Errors: as the component calls. */
