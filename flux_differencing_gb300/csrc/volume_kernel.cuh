@@ -60,6 +60,7 @@
 
 #include "esdg_internal.h"
 #include "floatfloat.cuh"
+#include "packed.cuh"
 
 namespace esdg {
 
@@ -174,6 +175,12 @@ struct Num<ff> {
         return (__float_as_uint(f.hi) & 0x7fffffffu) < 0x3C23D70Au;  // |f| < 0.01
     }
 };
+// two FP32 pair evaluations in packed registers: per-half estimate and test
+template <>
+struct Num<p2> {
+    static __device__ __forceinline__ p2 rcp(p2 x) { return p2(Num<float>::rcp(x.v.x), Num<float>::rcp(x.v.y)); }
+    static __device__ __forceinline__ m2 close(p2 d) { return m2{Num<float>::close(d.v.x), Num<float>::close(d.v.y)}; }
+};
 // x > 0 (false for NaN), for the non-physical-state check
 __device__ __forceinline__ bool positive(double x) { return x > 0.0; }
 __device__ __forceinline__ bool positive(float x) { return x > 0.0f; }
@@ -262,6 +269,36 @@ __device__ __forceinline__ NodeVals<T> load_node(const T* __restrict__ sm, int i
     return v;
 }
 
+// The values of two nodes in the two halves of packed operands.
+__device__ __forceinline__ NodeVals<p2> pack_vals(const NodeVals<float>& a, const NodeVals<float>& b) {
+    NodeVals<p2> v;
+    v.rho = p2(a.rho, b.rho);
+    v.u1 = p2(a.u1, b.u1);
+    v.u2 = p2(a.u2, b.u2);
+    v.u3 = p2(a.u3, b.u3);
+    v.b = p2(a.b, b.b);
+    v.ib = p2(a.ib, b.ib);
+    v.lr = p2(a.lr, b.lr);
+    v.lb = p2(a.lb, b.lb);
+    v.phi = p2(a.phi, b.phi);
+    v.h = p2(a.h, b.h);
+    v.A0 = p2(a.A0, b.A0);
+    v.A1 = p2(a.A1, b.A1);
+    v.A2 = p2(a.A2, b.A2);
+    return v;
+}
+
+// Whether the FP32 kernel evaluates its offsets two at a time in packed FP32
+// registers.  Chosen per order from the order sweep on GB300 (ms at about
+// 6.4e7 nodes, unpacked -> packed): N = 4 3.44 -> 2.92, N = 5 3.64 -> 3.54,
+// N = 6 4.32 -> 4.23, N = 8 5.00 -> 4.47 (with two line sets per warp at N = 4,
+// 5, 8 for the registers); N = 3 ties and N = 7 was slower (3.17 -> 3.32), so
+// those keep one evaluation per instruction.
+template <typename C, int N>
+struct PackPairs {
+    static constexpr bool value = std::is_same<C, float>::value && (N == 4 || N == 5 || N == 6 || N == 8);
+};
+
 // One pair (i, m) of a line, evaluated once for both nodes.  c8 = 2 Q_{pp'}/8
 // with p, p' the positions of i and m.  Adds node i's share 2Q_{pp'} (F +
 // G(i,m)) to o0..o4 and returns node m's share 2Q_{p'p} (F + G(m,i)) =
@@ -277,7 +314,7 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
 
     const T rsum = I.rho + M.rho;
     T rho_ln, inv_bsum, inv_bln, bsum;
-    if constexpr (std::is_same<T, float>::value) {
+    if constexpr (std::is_same<T, float>::value || std::is_same<T, p2>::value) {
         // FP32: per-lane selects in the original statement order (the vote
         // below was measured slower for this issue-bound kernel: 0.215 ->
         // 0.237 ms on the N = 7 channel, and a reordering alone cost 4 %)
@@ -494,6 +531,53 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
             if (pm >= NQ) pm -= NQ;
             offset(d, Conv<T, C>::in(T(0.125) * a.ops.Q2[p * NQ + pm]));
         }
+    } else if constexpr (PackPairs<C, N>::value) {
+        // offsets d and d + 1 in the two halves of packed FP32 operands: one
+        // issue slot for two evaluations' arithmetic
+        const NodeVals<p2> I2 = pack_vals(I, I);
+        const p2 cg2(c_g, c_g);
+        p2 o0(0.0), o1(0.0), o2(0.0), o3(0.0), o4(0.0);
+#pragma unroll
+        for (int d = 1; d + 1 <= NEAR; d += 2) {
+            int pm = p + d;
+            if (pm >= NQ) pm -= NQ;
+            int pn = pm + 1;
+            if (pn >= NQ) pn -= NQ;
+            int ma = ia, mb = ib, mc = ic, na = ia, nb = ib, nc = ic;
+            if (R == 0) { ma = pm; na = pn; }
+            else if (R == 1) { mb = pm; nb = pn; }
+            else { mc = pm; nc = pn; }
+            const NodeVals<p2> M = pack_vals(load_node<N>(sm, SL::at(el, ma, mb, mc), R),
+                                             load_node<N>(sm, SL::at(el, na, nb, nc), R));
+            p2 t0, t1, t2, t3, t4;
+            pair_flux<p2>(I2, M, p2(c8[d - 1], c8[d]), cg2, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
+            // partner shares: half x to the lane at p + d, half y to p + d + 1
+            // (none for the in-phase antipodal offset of even Nq)
+            int src = p - d;
+            if (src < 0) src += NQ;
+            src += slot * NQ;
+            acc0 += shfl(t0.v.x, src);
+            acc1 += shfl(t1.v.x, src);
+            acc2 += shfl(t2.v.x, src);
+            acc3 += shfl(t3.v.x, src);
+            acc4 += shfl(t4.v.x, src);
+            if (!(S::EVEN && d + 1 == S::H)) {
+                int src2 = p - d - 1;
+                if (src2 < 0) src2 += NQ;
+                src2 += slot * NQ;
+                acc0 += shfl(t0.v.y, src2);
+                acc1 += shfl(t1.v.y, src2);
+                acc2 += shfl(t2.v.y, src2);
+                acc3 += shfl(t3.v.y, src2);
+                acc4 += shfl(t4.v.y, src2);
+            }
+        }
+        if constexpr (NEAR % 2 == 1) offset(NEAR, c8[NEAR - 1]);
+        acc0 += o0.v.x + o0.v.y;
+        acc1 += o1.v.x + o1.v.y;
+        acc2 += o2.v.x + o2.v.y;
+        acc3 += o3.v.x + o3.v.y;
+        acc4 += o4.v.x + o4.v.y;
     } else {
 #pragma unroll
         for (int d = 1; d <= NEAR; ++d) offset(d, c8[d - 1]);
@@ -529,14 +613,15 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
 //  * float-float: always 2 (256-thread CTAs at N = 7);
 //  * FP64: 2 only at N = 7 (111.2 -> 109.4 ms); at N = 2, 4, 5, 6, 8 the
 //    halved CTA was 2-7 % slower;
-//  * FP32: 2 only at N = 8, where one element's 81 lines would otherwise need
-//    an 864-thread CTA (5.05 -> 5.00 ms).
+//  * FP32: 2 at N = 4, 5 and 8, where the packed pair evaluation (PackPairs)
+//    needs more than the 64 registers a 512-thread CTA pair leaves; at N = 8
+//    one element's 81 lines would otherwise also need an 864-thread CTA.
 template <int N, typename C>
 struct Launch {
     using S = Shape<N>;
     static constexpr int VWARPS = (S::LINES + S::LPW - 1) / S::LPW;  // warps' worth of lines
     static constexpr bool FP64 = sizeof(C) == 8;
-    static constexpr int REPS = IsFF<C>::value ? 2 : FP64 ? (N == 7 ? 2 : 1) : (N == 8 ? 2 : 1);
+    static constexpr int REPS = IsFF<C>::value ? 2 : FP64 ? (N == 7 ? 2 : 1) : ((N == 4 || N == 5 || N == 8) ? 2 : 1);
     static constexpr int WARPS = (VWARPS + REPS - 1) / REPS;
     static constexpr int THREADS = WARPS * 32;
     static constexpr size_t SMEM = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
