@@ -419,11 +419,11 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
 // The final write of one node's volume term t0..t4: to out, or, in a fused
 // Runge-Kutta stage, plus the surface term at face nodes, as a stage update of
 // dq and q (the node's own element only, so updating q in place is safe).
-template <typename T, int N>
+template <typename T, int N, bool RK>
 __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, int na, int nb, int nc, T t0,
                                            T t1, T t2, T t3, T t4) {
     const long long n = a.n;
-    if (a.rk_q == nullptr) {
+    if constexpr (!RK) {
         T* __restrict__ o = a.out;
         o[0 * n + g] = t0;
         o[1 * n + g] = t1;
@@ -467,12 +467,13 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
     }
 }
 
-// One direction phase.  R = 0 (xi), 1 (eta), 2 (zeta).  FINAL = false: add
-// the scaled sum to the shared accumulators; true: add the shared
-// accumulators and store the node's result to global memory.  Offsets
+// One direction phase.  R = 0 (xi), 1 (eta), 2 (zeta).  FINAL = 0: add the
+// scaled sum to the shared accumulators; 1: add the shared accumulators and
+// store the node's result to global memory; 2: the same, as a fused
+// Runge-Kutta stage update (store_node).  Offsets
 // d = 1..NEAR; the antipodal offset Nq/2 of even Nq is left to
 // antipodal_phase.
-template <typename T, typename C, int N, bool FINAL>
+template <typename T, typename C, int N, int FINAL>
 __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count,
                                                 long long node0, const C (&c8)[Shape<N>::H], C iw, C c_g,
                                                 int vwarp, int R) {
@@ -584,7 +585,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
     }
 
     C* s_acc = sm + F_ACC0 * FS;
-    if (!FINAL) {
+    if constexpr (FINAL == 0) {
         if (valid) {
             s_acc[0 * FS + i] = fma(acc0, iw, s_acc[0 * FS + i]);
             s_acc[1 * FS + i] = fma(acc1, iw, s_acc[1 * FS + i]);
@@ -597,7 +598,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         // linear node L*Nq + p is contiguous across lanes: coalesced stores
         static_assert(Layout<N>::ORD0 == 0, "xi lines must be dealt b-fastest");
         const long long g = node0 + (long long)L * NQ + p;
-        store_node<T, N>(a, g, ia, ib, ic, Conv<T, C>::out(fma(acc0, iw, s_acc[0 * FS + i])),
+        store_node<T, N, FINAL == 2>(a, g, ia, ib, ic, Conv<T, C>::out(fma(acc0, iw, s_acc[0 * FS + i])),
                          Conv<T, C>::out(fma(acc1, iw, s_acc[1 * FS + i])),
                          Conv<T, C>::out(fma(acc2, iw, s_acc[2 * FS + i])),
                          Conv<T, C>::out(fma(acc3, iw, s_acc[3 * FS + i])),
@@ -630,7 +631,7 @@ struct Launch {
         ((sizeof(C) == 4 && THREADS <= 512) || IsFF<C>::value || (FP64 && REPS == 2)) && TWO_FIT ? 2 : 1;
 };
 
-template <typename T, typename C, int N, int R, bool FINAL>
+template <typename T, typename C, int N, int R, int FINAL>
 __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count,
                                                 long long node0, const C (&c8)[Shape<N>::H], C iw, C c_g) {
     using LA = Launch<N, C>;
@@ -685,7 +686,9 @@ __device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, C* __res
     }
 }
 
-template <typename T, int N, typename C>
+// RK: fused Runge-Kutta stage (store_node); a separate instantiation so that
+// the plain kernel's code and registers are those of a store to out.
+template <typename T, int N, typename C, bool RK>
 __global__ void __launch_bounds__(Launch<N, C>::THREADS, Launch<N, C>::MIN_BLOCKS)
 volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     using S = Shape<N>;
@@ -825,7 +828,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             const int R = (k == 0) ? 1 : (k == 1) ? 2 : 0;
 #pragma unroll 1
             for (int rep = 0; rep < LA::REPS; ++rep)
-                direction_lines<T, C, N, false>(a, sm, e_count, node0, c8, iw, c_g, warp + rep * LA::WARPS, R);
+                direction_lines<T, C, N, 0>(a, sm, e_count, node0, c8, iw, c_g, warp + rep * LA::WARPS, R);
             __syncthreads();
         }
         if constexpr (S::EVEN && SplitAntipodal<C>::value) {
@@ -842,13 +845,13 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
             const int sl = SL::at(el, na, nb, nc);
             const long long g = node0 + t;
-            store_node<T, N>(a, g, na, nb, nc, CV::out(s_acc[0 * FS + sl]), CV::out(s_acc[1 * FS + sl]),
+            store_node<T, N, RK>(a, g, na, nb, nc, CV::out(s_acc[0 * FS + sl]), CV::out(s_acc[1 * FS + sl]),
                              CV::out(s_acc[2 * FS + sl]), CV::out(s_acc[3 * FS + sl]), CV::out(s_acc[4 * FS + sl]));
         }
     } else {
-        direction_phase<T, C, N, 1, false>(a, sm, e_count, node0, c8, iw, c_g);
+        direction_phase<T, C, N, 1, 0>(a, sm, e_count, node0, c8, iw, c_g);
         __syncthreads();
-        direction_phase<T, C, N, 2, false>(a, sm, e_count, node0, c8, iw, c_g);
+        direction_phase<T, C, N, 2, 0>(a, sm, e_count, node0, c8, iw, c_g);
         __syncthreads();
         if constexpr (S::EVEN && SplitAntipodal<C>::value) {
             antipodal_phase<T, C, N>(a, sm, e_count, c_g, 1);
@@ -858,26 +861,35 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             antipodal_phase<T, C, N>(a, sm, e_count, c_g, 0);
             __syncthreads();
         }
-        direction_phase<T, C, N, 0, true>(a, sm, e_count, node0, c8, iw, c_g);
+        direction_phase<T, C, N, 0, RK ? 2 : 1>(a, sm, e_count, node0, c8, iw, c_g);
     }
 }
 
-template <typename T, int N, typename C = T>
-cudaError_t launch_volume(const VolumeArgs<T>& a, cudaStream_t s) {
+template <typename T, int N, typename C, bool RK>
+cudaError_t launch_volume_mode(const VolumeArgs<T>& a, cudaStream_t s) {
     using S = Shape<N>;
     const long long K = a.e_end - a.e_begin;
     if (K <= 0) return cudaSuccess;
     const size_t smem = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
     static bool attr_done = false;  // per instantiation; set once per process
     if (!attr_done) {
-        cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N, C>,
+        cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N, C, RK>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         attr_done = true;
     }
     const long long blocks = (K + S::EPB - 1) / S::EPB;
-    volume_kernel<T, N, C><<<(unsigned)blocks, Launch<N, C>::THREADS, smem, s>>>(a);
+    volume_kernel<T, N, C, RK><<<(unsigned)blocks, Launch<N, C>::THREADS, smem, s>>>(a);
     return cudaGetLastError();
+}
+
+// The fused Runge-Kutta mode is built for FP32 and float-float only (native
+// FP64 keeps the separate stage kernel).
+template <typename T, int N, typename C = T>
+cudaError_t launch_volume(const VolumeArgs<T>& a, cudaStream_t s) {
+    if (a.rk_q == nullptr) return launch_volume_mode<T, N, C, false>(a, s);
+    if constexpr (std::is_same<C, double>::value) return cudaErrorNotSupported;
+    else return launch_volume_mode<T, N, C, true>(a, s);
 }
 
 }  // namespace esdg
