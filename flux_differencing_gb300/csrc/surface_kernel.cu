@@ -254,8 +254,17 @@ __device__ __forceinline__ void add_out(const SurfaceArgs<T>& a, long long g, co
 // (an interface with the next element, wrapped when periodic, or a wall).
 // Slots beyond: the -xi_DIR faces of the first layer of elements when the
 // direction has walls.
+// Float-float needs ~127 registers unbounded (two CTAs per SM) and is bound by
+// latency there; a bound of three CTAs per SM (80 registers, a 228-byte
+// spill) measured 0.44 -> 0.405 ms per call on the N = 7 channel, four CTAs
+// (64 registers) no better.
+template <typename C>
+struct SurfaceOccupancy {
+    static constexpr int value = std::is_same<C, ff>::value ? 3 : 1;
+};
+
 template <typename T, typename C, int N, int DIR>
-__global__ void __launch_bounds__(256) surface_kernel(const __grid_constant__ SurfaceArgs<T> a) {
+__global__ void __launch_bounds__(256, SurfaceOccupancy<C>::value) surface_kernel(const __grid_constant__ SurfaceArgs<T> a) {
     constexpr int NQ = N + 1;
     constexpr int NF = NQ * NQ;
     using CV = Conv<T, C>;
