@@ -257,7 +257,8 @@ __device__ __forceinline__ void add_out(const SurfaceArgs<T>& a, long long g, co
 // Float-float needs ~127 registers unbounded (two CTAs per SM) and is bound by
 // latency there; a bound of three CTAs per SM (80 registers, a 228-byte
 // spill) measured 0.44 -> 0.405 ms per call on the N = 7 channel, four CTAs
-// (64 registers) no better.
+// (64 registers) no better.  The FP32 kernel (59 registers) was slower when
+// bounded to six CTAs per SM (0.143 -> 0.156 ms), so it stays unbounded.
 template <typename C>
 struct SurfaceOccupancy {
     static constexpr int value = std::is_same<C, ff>::value ? 3 : 1;
