@@ -28,11 +28,12 @@
 //    by a warp shuffle, so no atomics and a fixed summation order (bitwise
 //    deterministic).
 //  * For even Nq the antipodal pairs (p, p + Nq/2) are where Eq. 6 loses
-//    balance and Fig. 1(b) evaluates each pair twice with weight 1/2.  Here
-//    they get a pass of their own per direction: within one direction every
-//    node is in exactly one antipodal pair, so one thread evaluates the pair
-//    once and adds both shares to shared memory without races, and the
-//    threads left over are whole idle warps, which cost no issue slots.
+//    balance and Fig. 1(b) evaluates each pair twice with weight 1/2.  In
+//    FP64 and float-float they get a pass of their own per direction: within
+//    one direction every node is in exactly one antipodal pair, so one thread
+//    evaluates the pair once and adds both shares to shared memory without
+//    races, and the threads left over are whole idle warps, which cost no
+//    issue slots.  FP32 keeps the in-phase evaluation (cheaper there).
 //  * Shared memory is laid out per order (padding or an XOR swizzle, and the
 //    order in which lines are dealt to warps) so that the partner loads of
 //    every direction phase are free of bank conflicts where possible.
@@ -41,8 +42,13 @@
 //    direction vector, never as a 3x5 flux matrix (Sec. 4.1).  Log means use
 //    the per-node logarithms, switching to a series in ((a+ - a-)/(a+ + a-))^2
 //    when the two logarithms are close, and 1/{{b}}_log is computed directly
-//    (Sec. 4.1).  The switch is a select on one reciprocal, so lanes never
-//    diverge on it, and the closeness test runs on the integer pipe.
+//    (Sec. 4.1).  The closeness test runs on the integer pipe; in FP64 and
+//    float-float a warp vote skips the branch no lane needs, a mixed warp
+//    (and FP32 always) evaluates both and selects per lane.
+//  * FP32 at N = 4, 5, 6, 8 evaluates two offsets per instruction in packed
+//    float2 registers (issue-bound kernel; PackPairs).
+//  * A second instantiation (RK) fuses a Runge-Kutta stage update into the
+//    final store, for the FP32 and float-float time step.
 //  * FP64 on GB300 has 1/64 of the FP32 rate, so the FP64 kernel is bound by
 //    its FP64 instruction count: reciprocals are a hardware estimate refined
 //    by one third-order Newton-Raphson step rather than a correctly rounded
