@@ -751,6 +751,62 @@ def _step_report(cfg, res, ws, hbm_peak_gbs):
                                             "volume kernel"}}
 
 
+def run_graph_sweep(args, device, stream):
+    """One five-stage time step of small meshes, launched eagerly (20-25
+    launches per step from the host) and replayed from a CUDA graph captured
+    once: where the kernels are short, the launch path is the cost."""
+    import torch
+
+    import workloads as wl
+
+    cases = [wl.get_config("tiny_box_N3")]
+    for N, k in ((3, 8), (7, 4), (7, 8)):
+        for prec in ("fp64", "fp32"):
+            cases.append(wl.small_config(N, K=(k, k, k), warp=True, precision=prec))
+    steps = max(args.steps, 50)
+    for cfg in cases:
+        op, q, Ja, phi, out = _setup(cfg, device)
+        dq = torch.zeros_like(q)
+        qs = q.clone()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                op.lsrk_step(qs, dq, out, Ja, phi, op.J, STEP_DT, stream=stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                op.lsrk_step(qs, dq, out, Ja, phi, op.J, STEP_DT, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        eager = e0.elapsed_time(e1) / steps
+        graph = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream(device)
+        gs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(graph, stream=gs):
+                op.lsrk_step(qs, dq, out, Ja, phi, op.J, STEP_DT, stream=gs)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(steps):
+            graph.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        replay = g0.elapsed_time(g1) / steps
+        assert op.status() == 0
+        print(json.dumps({"sweep": "graph", "config": cfg.name, "N": cfg.N, "K": cfg.K, "nodes": cfg.n,
+                          "precision": cfg.precision, "launches_per_step": 25 if cfg.precision == "fp64" else 20,
+                          "eager_ms_per_step": eager, "graph_ms_per_step": replay,
+                          "speedup": eager / replay}), flush=True)
+        op.close()
+        del q, Ja, phi, out, dq, qs
+        torch.cuda.empty_cache()
+
+
 def run_sweep(args):
     """Opt-in measurement sweeps, one JSON line per point on stdout.
 
@@ -768,6 +824,9 @@ def run_sweep(args):
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
     points = []
+    if args.sweep == "graph":
+        run_graph_sweep(args, device, stream)
+        return
     if args.sweep == "orders":
         for N in range(2, 9):
             for prec in ("fp64", "fp32", "fp64ff"):
@@ -813,7 +872,7 @@ def main():
     ap.add_argument("--no-peaks", action="store_true", help="skip the FMA-throughput peak measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=int, default=256)
-    ap.add_argument("--sweep", choices=["orders", "elements"], default=None,
+    ap.add_argument("--sweep", choices=["orders", "elements", "graph"], default=None,
                     help="opt-in measurement sweeps (one JSON line per point) instead of the bench line")
     args = ap.parse_args()
     if args.warmup < 3:
