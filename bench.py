@@ -441,9 +441,52 @@ def _cpu_baseline(cfg, budget_s: float = 12.0):
     oracle.volume(cfg.N, count, gc["q"], Ja, gc["phi"], nthreads=nthreads)
     dt = time.perf_counter() - t0
     nodes = count * cfg.Nq ** 3
+    single = _cpu_single_core(cfg, min(3.0, budget_s / 4))
     return {"value": nodes / dt / 1e9, "unit": "GDOF/s", "cores": nthreads, "kind": "oracle",
             "sample": f"first {count} of {cfg.K} elements of {cfg.name} ({nodes} nodes), FP64 oracle, "
-                      f"{dt:.1f} s, OpenMP over elements"}
+                      f"{dt:.1f} s, OpenMP over elements",
+            "single_core": single}
+
+
+def _cpu_single_core(cfg, budget_s: float = 2.0):
+    """The oracle on one host core (a bounded prefix of the workload's elements)."""
+    import oracle
+    import workloads as wl
+
+    pilot = np.arange(min(cfg.K, 4))
+    g = wl.generate_elements(cfg, pilot)
+    gc = {k: v.numpy() for k, v in g.items()}
+    Ja, _ = oracle.metrics(cfg.N, len(pilot), gc["x"], gc["y"], gc["z"])
+    t0 = time.perf_counter()
+    oracle.volume(cfg.N, len(pilot), gc["q"], Ja, gc["phi"], nthreads=1)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    count = int(min(cfg.K, max(len(pilot), len(pilot) * budget_s / dt)))
+    g = wl.generate_elements(cfg, np.arange(count))
+    gc = {k: v.numpy() for k, v in g.items()}
+    Ja, _ = oracle.metrics(cfg.N, count, gc["x"], gc["y"], gc["z"])
+    t0 = time.perf_counter()
+    oracle.volume(cfg.N, count, gc["q"], Ja, gc["phi"], nthreads=1)
+    dt = time.perf_counter() - t0
+    nodes = count * cfg.Nq ** 3
+    return {"value": nodes / dt / 1e9, "unit": "GDOF/s", "cores": 1,
+            "sample": f"first {count} of {cfg.K} elements of {cfg.name}, {dt:.1f} s"}
+
+
+def run_oracle_sweep(args):
+    """The oracle on the host: all cores and one core, on the three fixed configs
+    (tiny box N = 3, bubble N = 4, channel N = 7); one JSON line each."""
+    for name in ("tiny_box_N3", "bubble_N4", "channel_N7"):
+        cfg = _wl().get_config(name)
+        allc = _cpu_baseline(cfg, args.cpu_seconds)
+        print(json.dumps({"sweep": "oracle", "config": name, "N": cfg.N, "nodes": cfg.n,
+                          "all_cores_GDOF/s": allc["value"], "cores": allc["cores"],
+                          "single_core_GDOF/s": allc["single_core"]["value"],
+                          "samples": [allc["sample"], allc["single_core"]["sample"]]}), flush=True)
+
+
+def _wl():
+    import workloads as wl
+    return wl
 
 
 def run_reference(args):
@@ -872,7 +915,7 @@ def main():
     ap.add_argument("--no-peaks", action="store_true", help="skip the FMA-throughput peak measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=int, default=256)
-    ap.add_argument("--sweep", choices=["orders", "elements", "graph"], default=None,
+    ap.add_argument("--sweep", choices=["orders", "elements", "graph", "oracle"], default=None,
                     help="opt-in measurement sweeps (one JSON line per point) instead of the bench line")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -883,6 +926,8 @@ def main():
         args.ff_workload = None
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep == "oracle":
+        run_oracle_sweep(args)
     elif args.sweep:
         run_sweep(args)
     else:
