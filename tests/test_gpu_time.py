@@ -50,7 +50,7 @@ def _stable_dt(cfg, q, phi, cfl=0.3):
     return cfl * h / speed / (cfg.N + 1) ** 2
 
 
-@pytest.mark.parametrize("N", [1, 2, 3, 5, 7])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("precision", ["fp64", "fp32", "fp64ff"])
 def test_lsrk_step_parity(N, precision):
     cfg = wl.small_config(N, K=(2, 2, 2), warp=True, state="noisy", precision=precision, bc=(0, 1, 1))
@@ -158,7 +158,7 @@ def test_lsrk_step_in_a_cuda_graph():
     assert torch.equal(q_e, q_g)
 
 
-@pytest.mark.parametrize("precision", ["fp64", "fp32"])
+@pytest.mark.parametrize("precision", ["fp64", "fp32", "fp64ff"])
 def test_pipeline_from_host_buffers(precision):
     """esdg_pipeline_*: several submissions from pinned host buffers, overlapping,
     each giving the same bits as esdg_volume_rhs on device buffers."""
