@@ -533,6 +533,11 @@ def run_ours(args):
 
     import workloads as wl
 
+    # each workload argument feeds the report section of its own precision
+    for flag, wname, prec in (("--workload", args.workload, "fp64"), ("--fp32-workload", args.fp32_workload, "fp32"),
+                              ("--ff-workload", args.ff_workload, "fp64ff")):
+        if wname and wl.get_config(wname).precision != prec:
+            raise SystemExit(f"{flag} {wname}: expected a {prec} workload")
     ws, rank, local = _dist()
     if ws > 1:
         dist.init_process_group("nccl")
@@ -705,7 +710,8 @@ def run_ours(args):
         if wname and "step" in results[wname]:
             rep = _step_report(results[wname]["cfg"], results[wname], ws, peaks.get("hbm_gbs"))
             (line if key == "main" else line[key])["step"] = rep
-            line["gpu_launches"] += 21 * args.steps
+            # the step's launches plus the standalone stage timing (one per step)
+            line["gpu_launches"] += (rep["launches_per_step"] + 1) * args.steps
     if args.fp32_workload and "surface" in results[args.fp32_workload]:
         r32 = results[args.fp32_workload]
         line["fp32"]["surface"] = _surface_report(r32["cfg"], r32["surface"], ws, fp32_meas, "FP32 vector",
@@ -870,16 +876,17 @@ def run_sweep(args):
     if args.sweep == "graph":
         run_graph_sweep(args, device, stream)
         return
+    precs = [x for x in ("fp64", "fp32", "fp64ff") if x in args.precisions.split(",")]
     if args.sweep == "orders":
         for N in range(2, 9):
-            for prec in ("fp64", "fp32", "fp64ff"):
+            for prec in precs:
                 points.append(wl.get_config(f"sweep_N{N}" + {"fp64": "", "fp32": "_fp32", "fp64ff": "_ff"}[prec]))
     else:
         for N in (2, 4, 7, 8):
             for k in (2, 4, 8, 16, 32, 48, 64):
                 if k ** 3 * (N + 1) ** 3 > 1.1e8:
                     continue
-                for prec in ("fp64", "fp32", "fp64ff"):
+                for prec in precs:
                     points.append(wl.small_config(N, K=(k, k, k), warp=True, precision=prec))
     for cfg in points:
         op, q, Ja, phi, out = _setup(cfg, device)
@@ -917,6 +924,8 @@ def main():
     ap.add_argument("--ref-elements", type=int, default=256)
     ap.add_argument("--sweep", choices=["orders", "elements", "graph", "oracle"], default=None,
                     help="opt-in measurement sweeps (one JSON line per point) instead of the bench line")
+    ap.add_argument("--precisions", default="fp64,fp32,fp64ff",
+                    help="comma-separated precisions of the orders and elements sweeps")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -40,11 +40,15 @@
 //  * The mass flux is {{rho}}_log {{u}}.n, the energy flux the entropy-
 //    conserving completion; both are formed directly from the contravariant
 //    direction vector, never as a 3x5 flux matrix (Sec. 4.1).  Log means use
-//    the per-node logarithms, switching to a series in ((a+ - a-)/(a+ + a-))^2
-//    when the two logarithms are close, and 1/{{b}}_log is computed directly
+//    the per-node logarithms, switching to a series when the two logarithms
+//    are close -- in FP64 and float-float a series in the difference of the
+//    logarithms itself (no reciprocal), in FP32 one in
+//    ((a+ - a-)/(a+ + a-))^2 -- and 1/{{b}}_log is computed directly
 //    (Sec. 4.1).  The closeness test runs on the integer pipe; in FP64 and
 //    float-float a warp vote skips the branch no lane needs, a mixed warp
-//    (and FP32 always) evaluates both and selects per lane.
+//    (and FP32 always) evaluates both and selects per lane.  The per-node
+//    values are stored pre-scaled (u/2, 2b, phi/8) so that no factor of two
+//    is applied per pair.
 //  * FP32 at N = 4, 5, 6, 8 evaluates two offsets per instruction in packed
 //    float2 registers (issue-bound kernel; PackPairs).
 //  * A second instantiation (RK) fuses a Runge-Kutta stage update into the
@@ -305,27 +309,38 @@ struct PackPairs {
     static constexpr bool value = std::is_same<C, float>::value && (N == 4 || N == 5 || N == 6 || N == 8);
 };
 
-// One pair (i, m) of a line, evaluated once for both nodes.  c8 = 2 Q_{pp'}/8
+// One pair (i, m) of a line, evaluated once for both nodes.  cq = Q_{pp'}
 // with p, p' the positions of i and m.  Adds node i's share 2Q_{pp'} (F +
 // G(i,m)) to o0..o4 and returns node m's share 2Q_{p'p} (F + G(m,i)) =
-// -2Q_{pp'} (F + G(m,i)) in t0..t4, G(m,i) = -G(i,m) b_i/b_m (Sec. 4.1).
-// Both shares still need the 1/w scaling of their own node.
+// -2Q_{pp'} (F + G(m,i)) in t0..t4, G(m,i) = -G(i,m) b_i/b_m (Sec. 4.1);
+// t0 and t4 are returned with the opposite sign (the receiver subtracts
+// them), which saves two negations per pair.  Both shares still need the
+// 1/w scaling of their own node.
+//
+// Scaling of the per-node values (chosen so that no factor of 2 is applied
+// per pair): u holds u/2, so s = u_i + u_m is the mean velocity; b holds
+// b2 = 2b = rho/p (1/b and ln b2 as stored); phi holds phi/8; the metric
+// terms are unscaled, so A = Ja_i + Ja_m is twice the averaged metric and
+// Un = s.A twice the contravariant velocity U.  c_g2 = 1/(gamma - 1).
 template <typename T>
-__device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T>& M, T c8, T c_g, T& o0, T& o1,
+__device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T>& M, T cq, T c_g2, T& o0, T& o1,
                                           T& o2, T& o3, T& o4, T& t0, T& t1, T& t2, T& t3, T& t4) {
-    // 2 x averaged metric, 2 x averaged velocity, 4 x {{u}}.n
     const T A0 = I.A0 + M.A0, A1 = I.A1 + M.A1, A2 = I.A2 + M.A2;
     const T s1 = I.u1 + M.u1, s2 = I.u2 + M.u2, s3 = I.u3 + M.u3;
     const T Un = fma(s3, A2, fma(s2, A1, s1 * A0));
 
+    // rho_ln = {{rho}}_log, inv_bsum = 1/(b2+ + b2-) = 1/(4{{b}}) and
+    // inv_bln = 1/(2{{b}}_log)
     const T rsum = I.rho + M.rho;
-    T rho_ln, inv_bsum, inv_bln, bsum;
+    const T bsum = I.b + M.b;
+    const T dlr = M.lr - I.lr;
+    const T dlb = M.lb - I.lb;
+    T rho_ln, inv_bsum, inv_bln;
     if constexpr (std::is_same<T, float>::value || std::is_same<T, p2>::value) {
-        // FP32: per-lane selects in the original statement order (the vote
-        // below was measured slower for this issue-bound kernel: 0.215 ->
-        // 0.237 ms on the N = 7 channel, and a reordering alone cost 4 %)
+        // FP32: per-lane selects (the vote of the FP64 branch was measured
+        // slower for this issue-bound kernel: 0.215 -> 0.237 ms on the N = 7
+        // channel), series in f = (a+ - a-)/(a+ + a-) from one reciprocal
         const T drho = M.rho - I.rho;
-        const T dlr = M.lr - I.lr;
         const auto cr = Num<T>::close(dlr);
         const T rr = Num<T>::rcp(sel(cr, rsum, dlr));
         const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
@@ -334,92 +349,83 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
         const T polr = fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
         rho_ln = sel(cr, rsum * polr, tr);
 
-        // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
-        bsum = I.b + M.b;
+        // 1/(b2+ + b2-) and the inverse log mean from one reciprocal
         const T db = M.b - I.b;
-        const T dlb = M.lb - I.lb;
         const auto cb = Num<T>::close(dlb);
         const T rb = Num<T>::rcp(sel(cb, bsum, db * bsum));
         inv_bsum = sel(cb, rb, db * rb);
         const T fb = db * inv_bsum;
         const T ub = fb * fb;
-        // (2/bsum) atanh(f)/f = (2/bsum)(1 + u/3 + u^2/5 + u^3/7)
+        // 1/(2{{b}}_log) = (1/bsum2)(2 + 2u/3 + 2u^2/5 + 2u^3/7), f = db/bsum
         const T polb = fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
         inv_bln = sel(cb, inv_bsum * polb, dlb * (bsum * rb));
     } else {
-        // {{rho}}_log: (rho+ - rho-)/(ln rho+ - ln rho-), or the series when close.
-        // A warp vote skips the branch no lane of the warp needs (lines of one
-        // direction in one warp are usually all close or all far); a mixed warp
-        // evaluates both and selects.  Each lane computes the same formula either
-        // way, so the result does not depend on the vote.
-        const T drho = M.rho - I.rho;
-        const T dlr = M.lr - I.lr;
+        // Log means from the per-node logarithms: far, (a+ - a-)/(ln a+ - ln a-);
+        // close (|d| < 0.02, d = ln a+ - ln a-), with x = d/2,
+        //     {{a}}_log = {{a}} tanh(x)/x,  1/{{a}}_log = (x/tanh(x))/{{a}},
+        // as series in v = d^2 -- no reciprocal for rho, and d's absolute
+        // error only enters multiplied by d.  A warp vote skips the branch no
+        // lane of the warp needs; a mixed warp evaluates both and selects.
+        // Each lane computes the same formula either way.
         const auto cr = Num<T>::close(dlr);
-        bsum = I.b + M.b;
-        const T db = M.b - I.b;
-        const T dlb = M.lb - I.lb;
         const auto cb = Num<T>::close(dlb);
         const unsigned mask = __activemask();
-        // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945), f = drho/rsum
-        auto series_r = [&](T ur) {
-            return fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
+        // tanh(x)/x / 2 = 1/2 - v/24 + v^2/240 - 17 v^3/40320
+        auto series_r = [&](T v) {
+            return fma(v, fma(v, fma(v, T(-17.0 / 40320.0), T(1.0 / 240.0)), T(-1.0 / 24.0)), T(0.5));
         };
-        // (2/bsum) atanh(f)/f = (2/bsum)(1 + u/3 + u^2/5 + u^3/7), f = db/bsum
-        auto series_b = [&](T ub) {
-            return fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
+        // 2 x/tanh(x) = 2 + v/6 - v^2/360 + v^3/15120
+        auto series_b = [&](T v) {
+            return fma(v, fma(v, fma(v, T(1.0 / 15120.0), T(-1.0 / 360.0)), T(1.0 / 6.0)), T(2.0));
         };
         if (!__any_sync(mask, cr)) {
-            rho_ln = drho * Num<T>::rcp(dlr);
+            rho_ln = (M.rho - I.rho) * Num<T>::rcp(dlr);
         } else if (__all_sync(mask, cr)) {
-            const T tr = drho * Num<T>::rcp(rsum);
-            rho_ln = rsum * series_r(tr * tr);
+            rho_ln = rsum * series_r(dlr * dlr);
         } else {
-            const T rr = Num<T>::rcp(sel(cr, rsum, dlr));
-            const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
-            rho_ln = sel(cr, rsum * series_r(tr * tr), tr);
+            rho_ln = sel(cr, rsum * series_r(dlr * dlr), (M.rho - I.rho) * Num<T>::rcp(dlr));
         }
 
-        // 1/{{b}}_log and 1/(b+ + b-) from one reciprocal
+        // 1/(b2+ + b2-) and, far, 1/(2{{b}}_log) = dlb/db2 from one reciprocal
         if (!__any_sync(mask, cb)) {
+            const T db = M.b - I.b;
             const T rb = Num<T>::rcp(db * bsum);
             inv_bsum = db * rb;
             inv_bln = dlb * (bsum * rb);
         } else if (__all_sync(mask, cb)) {
-            const T rb = Num<T>::rcp(bsum);
-            inv_bsum = rb;
-            const T fb = db * rb;
-            inv_bln = rb * series_b(fb * fb);
+            inv_bsum = Num<T>::rcp(bsum);
+            inv_bln = inv_bsum * series_b(dlb * dlb);
         } else {
+            const T db = M.b - I.b;
             const T rb = Num<T>::rcp(sel(cb, bsum, db * bsum));
             inv_bsum = sel(cb, rb, db * rb);
-            const T fb = db * inv_bsum;
-            inv_bln = sel(cb, inv_bsum * series_b(fb * fb), dlb * (bsum * rb));
+            inv_bln = sel(cb, inv_bsum * series_b(dlb * dlb), dlb * (bsum * rb));
         }
     }
 
-    // flux scalars, already multiplied by 2Q_{pp'}
-    const T cr8 = c8 * rho_ln;
-    const T frh = cr8 * Un;                            // 2Q F_rho / 2
-    const T fr = frh + frh;                            // 2Q F_rho
-    const T gq = cr8 * (bsum * (M.phi - I.phi));       // 2Q rho_ln {{b}} [[phi]] / 2: gravity
-    const T cp = c8 * (rsum * inv_bsum);               // 2Q {{rho}}/(2{{b}}) / 4
-    const T phq = cp + cp;                             // 2Q p_hat / 2
-    const T ss = fma(s3, s3, fma(s2, s2, s1 * s1));
-    const T Kf = fma(c_g, inv_bln, fma(T(0.25), ss, I.h + M.h));
-    const T fE = fma(fr, Kf, cp * Un);                 // 2Q F_E
+    // flux scalars, already multiplied by 2Q_{pp'} (momentum parts by Q, as
+    // they multiply A = 2 x averaged metric)
+    const T cr = cq * rho_ln;
+    const T fr = cr * Un;                               // 2Q F_rho
+    const T gq = cr * (bsum * (M.phi - I.phi));         // Q rho_ln {{b}} [[phi]] / 2: gravity
+    const T phq = cq * (rsum * inv_bsum);               // Q p_hat, p_hat = {{rho}}/(2{{b}})
+    // 1/(2 (gamma-1) {{b}}_log) - {{|u|^2}}/2 + {{phi}} + |{{u}}|^2
+    const T hs = I.h + M.h;
+    const T Kf = fma(c_g2, inv_bln, fma(s3, s3, fma(s2, s2, fma(s1, s1, hs))));
+    const T fE = fma(fr, Kf, phq * Un);                 // 2Q F_E
     const T Pi = fma(gq, I.ib, phq);  // own: pressure mean + gravity scaled at b_i
     const T Pm = fma(gq, M.ib, -phq); // partner: -pressure mean + gravity scaled at b_m
 
     o0 += fr;
-    o1 = fma(A0, Pi, fma(frh, s1, o1));
-    o2 = fma(A1, Pi, fma(frh, s2, o2));
-    o3 = fma(A2, Pi, fma(frh, s3, o3));
+    o1 = fma(A0, Pi, fma(fr, s1, o1));
+    o2 = fma(A1, Pi, fma(fr, s2, o2));
+    o3 = fma(A2, Pi, fma(fr, s3, o3));
     o4 += fE;
-    t0 = -fr;
-    t1 = fma(A0, Pm, -(frh * s1));
-    t2 = fma(A1, Pm, -(frh * s2));
-    t3 = fma(A2, Pm, -(frh * s3));
-    t4 = -fE;
+    t0 = fr;  // subtracted by the receiver
+    t1 = fma(A0, Pm, -(fr * s1));
+    t2 = fma(A1, Pm, -(fr * s2));
+    t3 = fma(A2, Pm, -(fr * s3));
+    t4 = fE;  // subtracted by the receiver
 }
 
 // The final write of one node's volume term t0..t4: to out, or, in a fused
@@ -481,7 +487,7 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
 // antipodal_phase.
 template <typename T, typename C, int N, int FINAL>
 __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count,
-                                                long long node0, const C (&c8)[Shape<N>::H], C iw, C c_g,
+                                                long long node0, const C (&cq)[Shape<N>::H], C iw, C c_g,
                                                 int vwarp, int R) {
     using S = Shape<N>;
     using SL = Slots<N>;
@@ -504,7 +510,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
 
     C acc0 = C(0.0), acc1 = C(0.0), acc2 = C(0.0), acc3 = C(0.0), acc4 = C(0.0);
 
-    auto offset = [&](int d, C c8d) {
+    auto offset = [&](int d, C cqd) {
         int pm = p + d;
         if (pm >= NQ) pm -= NQ;
         int ma = ia, mb = ib, mc = ic;
@@ -513,7 +519,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         else mc = pm;
         const NodeVals<C> M = load_node<N>(sm, SL::at(el, ma, mb, mc), R);
         C t0, t1, t2, t3, t4;
-        pair_flux<C>(I, M, c8d, c_g, acc0, acc1, acc2, acc3, acc4, t0, t1, t2, t3, t4);
+        pair_flux<C>(I, M, cqd, c_g, acc0, acc1, acc2, acc3, acc4, t0, t1, t2, t3, t4);
         // In-phase antipodal offset (when not split off): both nodes evaluate
         // the pair and keep their own share -- Fig. 1(b)'s two weight-1/2
         // evaluations summed per node.
@@ -523,11 +529,11 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         int src = p - d;
         if (src < 0) src += NQ;
         src += slot * NQ;
-        acc0 += shfl(t0, src);
+        acc0 -= shfl(t0, src);
         acc1 += shfl(t1, src);
         acc2 += shfl(t2, src);
         acc3 += shfl(t3, src);
-        acc4 += shfl(t4, src);
+        acc4 -= shfl(t4, src);
     };
     if constexpr (IsFF<C>::value) {
         // one copy of the (long) float-float pair evaluation: no unrolling,
@@ -536,7 +542,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         for (int d = 1; d <= NEAR; ++d) {
             int pm = p + d;
             if (pm >= NQ) pm -= NQ;
-            offset(d, Conv<T, C>::in(T(0.125) * a.ops.Q2[p * NQ + pm]));
+            offset(d, Conv<T, C>::in(T(0.5) * a.ops.Q2[p * NQ + pm]));
         }
     } else if constexpr (PackPairs<C, N>::value) {
         // offsets d and d + 1 in the two halves of packed FP32 operands: one
@@ -557,29 +563,29 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
             const NodeVals<p2> M = pack_vals(load_node<N>(sm, SL::at(el, ma, mb, mc), R),
                                              load_node<N>(sm, SL::at(el, na, nb, nc), R));
             p2 t0, t1, t2, t3, t4;
-            pair_flux<p2>(I2, M, p2(c8[d - 1], c8[d]), cg2, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
+            pair_flux<p2>(I2, M, p2(cq[d - 1], cq[d]), cg2, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
             // partner shares: half x to the lane at p + d, half y to p + d + 1
             // (none for the in-phase antipodal offset of even Nq)
             int src = p - d;
             if (src < 0) src += NQ;
             src += slot * NQ;
-            acc0 += shfl(t0.v.x, src);
+            acc0 -= shfl(t0.v.x, src);
             acc1 += shfl(t1.v.x, src);
             acc2 += shfl(t2.v.x, src);
             acc3 += shfl(t3.v.x, src);
-            acc4 += shfl(t4.v.x, src);
+            acc4 -= shfl(t4.v.x, src);
             if (!(S::EVEN && d + 1 == S::H)) {
                 int src2 = p - d - 1;
                 if (src2 < 0) src2 += NQ;
                 src2 += slot * NQ;
-                acc0 += shfl(t0.v.y, src2);
+                acc0 -= shfl(t0.v.y, src2);
                 acc1 += shfl(t1.v.y, src2);
                 acc2 += shfl(t2.v.y, src2);
                 acc3 += shfl(t3.v.y, src2);
-                acc4 += shfl(t4.v.y, src2);
+                acc4 -= shfl(t4.v.y, src2);
             }
         }
-        if constexpr (NEAR % 2 == 1) offset(NEAR, c8[NEAR - 1]);
+        if constexpr (NEAR % 2 == 1) offset(NEAR, cq[NEAR - 1]);
         acc0 += o0.v.x + o0.v.y;
         acc1 += o1.v.x + o1.v.y;
         acc2 += o2.v.x + o2.v.y;
@@ -587,7 +593,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         acc4 += o4.v.x + o4.v.y;
     } else {
 #pragma unroll
-        for (int d = 1; d <= NEAR; ++d) offset(d, c8[d - 1]);
+        for (int d = 1; d <= NEAR; ++d) offset(d, cq[d - 1]);
     }
 
     C* s_acc = sm + F_ACC0 * FS;
@@ -639,12 +645,12 @@ struct Launch {
 
 template <typename T, typename C, int N, int R, int FINAL>
 __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count,
-                                                long long node0, const C (&c8)[Shape<N>::H], C iw, C c_g) {
+                                                long long node0, const C (&cq)[Shape<N>::H], C iw, C c_g) {
     using LA = Launch<N, C>;
     const int warp = threadIdx.x >> 5;
 #pragma unroll 1
     for (int rep = 0; rep < LA::REPS; ++rep)
-        direction_lines<T, C, N, FINAL>(a, sm, e_count, node0, c8, iw, c_g, warp + rep * LA::WARPS, R);
+        direction_lines<T, C, N, FINAL>(a, sm, e_count, node0, cq, iw, c_g, warp + rep * LA::WARPS, R);
 }
 
 // Antipodal pairs (p, p + Nq/2) of every line of direction R, for even Nq.
@@ -676,19 +682,19 @@ __device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, C* __res
         const NodeVals<C> I = load_node<N>(sm, i, R);
         const NodeVals<C> M = load_node<N>(sm, j, R);
         C o0 = C(0.0), o1 = C(0.0), o2 = C(0.0), o3 = C(0.0), o4 = C(0.0), t0, t1, t2, t3, t4;
-        const C c8 = Conv<T, C>::in(T(0.125) * a.ops.Q2[p * NQ + p + H]);
-        pair_flux<C>(I, M, c8, c_g, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
+        const C cq = Conv<T, C>::in(T(0.5) * a.ops.Q2[p * NQ + p + H]);
+        pair_flux<C>(I, M, cq, c_g, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
         const C iwi = Conv<T, C>::in(a.ops.invw[p]), iwj = Conv<T, C>::in(a.ops.invw[p + H]);
         s_acc[0 * FS + i] = fma(o0, iwi, s_acc[0 * FS + i]);
         s_acc[1 * FS + i] = fma(o1, iwi, s_acc[1 * FS + i]);
         s_acc[2 * FS + i] = fma(o2, iwi, s_acc[2 * FS + i]);
         s_acc[3 * FS + i] = fma(o3, iwi, s_acc[3 * FS + i]);
         s_acc[4 * FS + i] = fma(o4, iwi, s_acc[4 * FS + i]);
-        s_acc[0 * FS + j] = fma(t0, iwj, s_acc[0 * FS + j]);
+        s_acc[0 * FS + j] = fma(-t0, iwj, s_acc[0 * FS + j]);
         s_acc[1 * FS + j] = fma(t1, iwj, s_acc[1 * FS + j]);
         s_acc[2 * FS + j] = fma(t2, iwj, s_acc[2 * FS + j]);
         s_acc[3 * FS + j] = fma(t3, iwj, s_acc[3 * FS + j]);
-        s_acc[4 * FS + j] = fma(t4, iwj, s_acc[4 * FS + j]);
+        s_acc[4 * FS + j] = fma(-t4, iwj, s_acc[4 * FS + j]);
     }
 }
 
@@ -765,19 +771,20 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
                          : gm1 * (E - rho * fma(P(0.5), uu, phi));
         if (!real) pr = P(0.5) * gm1;  // padding node: finite values, never stored
         bad |= !positive(rho) || !positive(pr);
-        const P ipr = Num<P>::rcp(pr);
-        const P b = P(0.5) * rho * ipr;
+        // stored with the scalings pair_flux expects: u/2, b2 = 2b = rho/p,
+        // ln b2, phi/8 (1/b and h = phi/2 - |u|^2/4 unscaled)
+        const P b2 = rho * Num<P>::rcp(pr);
         const P ib = P(2.0) * pr * irho;
         const P h = fma(P(-0.25), uu, P(0.5) * phi);
         sm[F_RHO * FS + sl] = rho;
-        sm[F_U1 * FS + sl] = u1;
-        sm[F_U2 * FS + sl] = u2;
-        sm[F_U3 * FS + sl] = u3;
-        sm[F_B * FS + sl] = b;
+        sm[F_U1 * FS + sl] = P(0.5) * u1;
+        sm[F_U2 * FS + sl] = P(0.5) * u2;
+        sm[F_U3 * FS + sl] = P(0.5) * u3;
+        sm[F_B * FS + sl] = b2;
         sm[F_INVB * FS + sl] = ib;
         sm[F_LNRHO * FS + sl] = Num<P>::log_(rho);
-        sm[F_LNB * FS + sl] = Num<P>::log_(b);
-        sm[F_PHI * FS + sl] = phi;
+        sm[F_LNB * FS + sl] = Num<P>::log_(b2);
+        sm[F_PHI * FS + sl] = P(0.125) * phi;
         sm[F_H * FS + sl] = h;
 #pragma unroll
         for (int k = 0; k < 9; ++k) sm[(F_JA0 + k) * FS + sl] = ja[k];
@@ -793,11 +800,10 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             const P V1 = fma(dC, ja[7], fma(dB, ja[4], dA * ja[1]));
             const P V2 = fma(dC, ja[8], fma(dB, ja[5], dA * ja[2]));
             const P rU = rho * fma(u3, V2, fma(u2, V1, u1 * V0));
-            const P pp = P(0.5) * rho * ib;
             f0 = rU;
-            f1 = fma(rU, u1, pp * V0);
-            f2 = fma(rU, u2, pp * V1);
-            f3 = fma(rU, u3, pp * V2);
+            f1 = fma(rU, u1, pr * V0);
+            f2 = fma(rU, u2, pr * V1);
+            f3 = fma(rU, u3, pr * V2);
             f4 = rU * fma(PV::in(a.c_h), ib, P(2.0) * (phi - h));  // (E + p) U
         }
         sm[(F_ACC0 + 0) * FS + sl] = f0;
@@ -808,18 +814,18 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(a.status, 1u);
 
-    // lane constants: 2Q_{p,p+d}/8 for every offset and 1/w_p
+    // lane constants: Q_{p,p+d} for every offset, 1/w_p and 1/(gamma - 1)
     const int lane = threadIdx.x & 31;
     const int p = lane - (lane / NQ) * NQ;
-    C c8[S::H];
+    C cq[S::H];
 #pragma unroll
     for (int d = 1; d <= S::H; ++d) {
         int pm = p + d;
         if (pm >= NQ) pm -= NQ;
-        c8[d - 1] = CV::in(T(0.125) * a.ops.Q2[p * NQ + pm]);
+        cq[d - 1] = CV::in(T(0.5) * a.ops.Q2[p * NQ + pm]);
     }
     const C iw = CV::in(a.ops.invw[p]);
-    const C c_g = CV::in(a.c_g);
+    const C c_g = CV::in(T(2) * a.c_g);  // 1/(gamma - 1)
     __syncthreads();
 
     if constexpr (IsFF<C>::value) {
@@ -834,7 +840,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             const int R = (k == 0) ? 1 : (k == 1) ? 2 : 0;
 #pragma unroll 1
             for (int rep = 0; rep < LA::REPS; ++rep)
-                direction_lines<T, C, N, 0>(a, sm, e_count, node0, c8, iw, c_g, warp + rep * LA::WARPS, R);
+                direction_lines<T, C, N, 0>(a, sm, e_count, node0, cq, iw, c_g, warp + rep * LA::WARPS, R);
             __syncthreads();
         }
         if constexpr (S::EVEN && SplitAntipodal<C>::value) {
@@ -855,9 +861,9 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
                              CV::out(s_acc[2 * FS + sl]), CV::out(s_acc[3 * FS + sl]), CV::out(s_acc[4 * FS + sl]));
         }
     } else {
-        direction_phase<T, C, N, 1, 0>(a, sm, e_count, node0, c8, iw, c_g);
+        direction_phase<T, C, N, 1, 0>(a, sm, e_count, node0, cq, iw, c_g);
         __syncthreads();
-        direction_phase<T, C, N, 2, 0>(a, sm, e_count, node0, c8, iw, c_g);
+        direction_phase<T, C, N, 2, 0>(a, sm, e_count, node0, cq, iw, c_g);
         __syncthreads();
         if constexpr (S::EVEN && SplitAntipodal<C>::value) {
             antipodal_phase<T, C, N>(a, sm, e_count, c_g, 1);
@@ -867,7 +873,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             antipodal_phase<T, C, N>(a, sm, e_count, c_g, 0);
             __syncthreads();
         }
-        direction_phase<T, C, N, 0, RK ? 2 : 1>(a, sm, e_count, node0, c8, iw, c_g);
+        direction_phase<T, C, N, 0, RK ? 2 : 1>(a, sm, e_count, node0, cq, iw, c_g);
     }
 }
 
