@@ -72,6 +72,7 @@ _SIGS = {
     "esdg_bench_fma": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int, _P, _P]),
     "esdg_selftest_rcp": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, _P, _P, _P]),
     "esdg_selftest_ff": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, _P, _P, _P, _P]),
+    "esdg_selftest_log": (ctypes.c_int, [ctypes.c_long, _P, _P, _P]),
 }
 
 

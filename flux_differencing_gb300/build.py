@@ -51,7 +51,7 @@ def _sources():
     out = []
     for d in (CSRC, INCLUDE):
         for f in os.listdir(d):
-            if f.endswith((".cu", ".cuh", ".h")):
+            if f.endswith((".cu", ".cuh", ".h", ".inc")):
                 out.append(os.path.join(d, f))
     out.append(os.path.abspath(__file__))
     return out

@@ -82,3 +82,17 @@ extern "C" int esdg_selftest_ff(int op, long n, const double* x, const double* y
     ff_selftest<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(op, x, y, out, n);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
+
+namespace {
+__global__ void log_selftest(const double* __restrict__ x, double* __restrict__ y, long n) {
+    const long k = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < n) y[k] = esdg::Num<double>::log_(x[k]);
+}
+}  // namespace
+
+extern "C" int esdg_selftest_log(long n, const double* x, double* y, void* stream) {
+    if (n < 1 || !x || !y) return 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    log_selftest<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(x, y, n);
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}

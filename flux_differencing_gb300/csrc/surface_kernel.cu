@@ -45,6 +45,12 @@ namespace esdg {
 __device__ __forceinline__ double sqrt_(double x) { return sqrt(x); }
 __device__ __forceinline__ float sqrt_(float x) { return sqrtf(x); }
 __device__ __forceinline__ ff sqrt_(ff x) { return ff_sqrt(x); }
+// logarithms of the (rare) far-pair path: CUDA's log in FP64, whose compact
+// code keeps this kernel's registers (the volume kernel's inlined table log,
+// four copies here, raised them from 122 to 138 and halved the occupancy)
+__device__ __forceinline__ double far_log(double x) { return log(x); }
+__device__ __forceinline__ float far_log(float x) { return Num<float>::log_(x); }
+__device__ __forceinline__ ff far_log(ff x) { return Num<ff>::log_(x); }
 
 namespace {
 
@@ -134,8 +140,8 @@ __device__ __forceinline__ void interface_flux(const FaceNode<C>& I, const FaceN
     C dlb = fb * polb;
     if (!__all_sync(__activemask(), cr && cb)) {
         // a far pair in this warp: logarithms for all its lanes, selected per lane
-        const C lr = Num<C>::log_(J.rho) - Num<C>::log_(I.rho);
-        const C lb = Num<C>::log_(J.b) - Num<C>::log_(I.b);
+        const C lr = far_log(J.rho) - far_log(I.rho);
+        const C lb = far_log(J.b) - far_log(I.b);
         rho_ln = sel(cr, rho_ln, drho * Num<C>::rcp(sel(cr, C(1.0), lr)));
         inv_bln = sel(cb, inv_bln, lb * Num<C>::rcp(sel(cb, C(1.0), db)));
         dlr = sel(cr, dlr, lr);

@@ -70,6 +70,7 @@
 
 #include "esdg_internal.h"
 #include "floatfloat.cuh"
+#include "log_fp64.cuh"
 #include "packed.cuh"
 
 namespace esdg {
@@ -149,7 +150,8 @@ struct Num<double> {
     static __device__ __forceinline__ bool close(double d) {
         return (static_cast<unsigned>(__double2hiint(d)) & 0x7fffffffu) < 0x3F947AE1u;
     }
-    static __device__ __forceinline__ double log_(double x) { return log(x); }
+    // table-driven, 14 FP64 operations (log_fp64.cuh); within 2 ulp
+    static __device__ __forceinline__ double log_(double x) { return log_fp64(x); }
     // |f| < 0.01 (high word of 0.01 = 0x3F847AE1): for f = (a+ - a-)/(a+ + a-)
     // this is |ln a+ - ln a-| < 2 atanh(0.01), the same closeness as close()
     static __device__ __forceinline__ bool close_ratio(double f) {

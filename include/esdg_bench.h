@@ -41,6 +41,15 @@ int esdg_selftest_rcp(int fp64, long n, const void* x, void* y, void* stream);
  * launch error). */
 int esdg_selftest_ff(int op, long n, const double* x, const double* y, double* out, void* stream);
 
+/* Self-test of the FP64 volume kernel's per-node logarithm (the table-driven
+ * reduction of Tang, ACM TOMS 16(4), 1990, used for ln rho and ln 2b):
+ * y[k] = ln x[k] computed exactly as the kernel computes it, so the test
+ * suite can measure its error in ulps against the host's log.  Meaningful
+ * for positive normal x; other x give an unspecified value without a fault.
+ * x, y: device arrays of n doubles.  Asynchronous on `stream`.  Returns 0,
+ * 1 (bad argument) or 4 (CUDA launch error). */
+int esdg_selftest_log(long n, const double* x, double* y, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
