@@ -104,12 +104,11 @@ NOMINAL_FP64_TFLOPS = 1.25  # GB300 FP64 vector, nominal
 
 
 _CSRC = os.path.join(ROOT, "flux_differencing_gb300", "csrc")
+_NUMERIC = ("numeric.cuh", "floatfloat.cuh", "log_fp64.cuh", "log_table.inc", "esdg_internal.h")
 KERNEL_SOURCES = {
-    "volume": [os.path.join(_CSRC, f) for f in ("volume_kernel.cuh", "floatfloat.cuh", "log_fp64.cuh",
-                                                 "log_table.inc", "packed.cuh", "esdg_internal.h",
-                                                 "volume_inst.cu")],
+    "volume": [os.path.join(_CSRC, f) for f in ("volume_kernel.cuh", "packed.cuh", "volume_inst.cu") + _NUMERIC],
+    "surface": [os.path.join(_CSRC, f) for f in ("surface_kernel.cu",) + _NUMERIC],
 }
-KERNEL_SOURCES["surface"] = KERNEL_SOURCES["volume"] + [os.path.join(_CSRC, "surface_kernel.cu")]
 
 
 def kernel_source_sha(kind: str = "volume") -> str:
@@ -891,7 +890,7 @@ def run_sweep(args):
         return
     precs = [x for x in ("fp64", "fp32", "fp64ff") if x in args.precisions.split(",")]
     if args.sweep == "orders":
-        for N in range(2, 9):
+        for N in [int(v) for v in args.orders.split(",")]:
             for prec in precs:
                 points.append(wl.get_config(f"sweep_N{N}" + {"fp64": "", "fp32": "_fp32", "fp64ff": "_ff"}[prec]))
     else:
@@ -939,6 +938,7 @@ def main():
                     help="opt-in measurement sweeps (one JSON line per point) instead of the bench line")
     ap.add_argument("--precisions", default="fp64,fp32,fp64ff",
                     help="comma-separated precisions of the orders and elements sweeps")
+    ap.add_argument("--orders", default="2,3,4,5,6,7,8", help="comma-separated orders N of the orders sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

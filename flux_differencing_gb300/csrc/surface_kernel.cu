@@ -38,7 +38,7 @@
 #include <cuda_runtime.h>
 
 #include "esdg_internal.h"
-#include "volume_kernel.cuh"
+#include "numeric.cuh"
 
 namespace esdg {
 

@@ -17,7 +17,7 @@
 #include <cuda_runtime.h>
 
 #include "esdg_internal.h"
-#include "volume_kernel.cuh"
+#include "numeric.cuh"
 
 namespace esdg {
 namespace {

@@ -49,7 +49,7 @@
 //    (and FP32 always) evaluates both and selects per lane.  The per-node
 //    values are stored pre-scaled (u/2, 2b, phi/8) so that no factor of two
 //    is applied per pair.
-//  * FP32 at N = 4, 5, 6, 8 evaluates two offsets per instruction in packed
+//  * FP32 at N = 4..8 evaluates two offsets per instruction in packed
 //    float2 registers (issue-bound kernel; PackPairs).
 //  * A second instantiation (RK) fuses a Runge-Kutta stage update into the
 //    final store, for the FP32 and float-float time step.
@@ -70,7 +70,7 @@
 
 #include "esdg_internal.h"
 #include "floatfloat.cuh"
-#include "log_fp64.cuh"
+#include "numeric.cuh"
 #include "packed.cuh"
 
 namespace esdg {
@@ -132,101 +132,11 @@ enum SmemField {
     F_COUNT = F_ACC0 + 5
 };
 
-template <typename T>
-struct Num;
-template <>
-struct Num<double> {
-    // 1/x: hardware estimate (rcp.approx.ftz.f64) and one Newton-Raphson step
-    // of third order, r' = r (1 + e + e^2) with e = 1 - x r, which cubes the
-    // estimate's relative error.  Zeros and infinities never reach a result
-    // that is used (the selects pick the other branch).
-    static __device__ __forceinline__ double rcp(double x) {
-        double r;
-        asm("rcp.approx.ftz.f64 %0, %1;" : "=d"(r) : "d"(x));
-        const double e = fma(-x, r, 1.0);
-        return fma(r, fma(e, e, e), r);
-    }
-    // |d| < 0.02 (high word of 0.02 = 0x3F947AE1), tested on the integer pipe
-    static __device__ __forceinline__ bool close(double d) {
-        return (static_cast<unsigned>(__double2hiint(d)) & 0x7fffffffu) < 0x3F947AE1u;
-    }
-    // table-driven, 14 FP64 operations (log_fp64.cuh); within 2 ulp
-    static __device__ __forceinline__ double log_(double x) { return log_fp64(x); }
-    // |f| < 0.01 (high word of 0.01 = 0x3F847AE1): for f = (a+ - a-)/(a+ + a-)
-    // this is |ln a+ - ln a-| < 2 atanh(0.01), the same closeness as close()
-    static __device__ __forceinline__ bool close_ratio(double f) {
-        return (static_cast<unsigned>(__double2hiint(f)) & 0x7fffffffu) < 0x3F847AE1u;
-    }
-};
-template <>
-struct Num<float> {
-    static __device__ __forceinline__ float rcp(float x) {
-        float r;
-        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-        return r;
-    }
-    // |d| < 0.2 (0x3E4CCCCD)
-    static __device__ __forceinline__ bool close(float d) {
-        return (__float_as_uint(d) & 0x7fffffffu) < 0x3E4CCCCDu;
-    }
-    static __device__ __forceinline__ float log_(float x) { return logf(x); }
-    // |f| < 0.1 (0x3DCCCCCD), i.e. |ln a+ - ln a-| < 2 atanh(0.1) ~ 0.2
-    static __device__ __forceinline__ bool close_ratio(float f) {
-        return (__float_as_uint(f) & 0x7fffffffu) < 0x3DCCCCCDu;
-    }
-};
-// float-float pair arithmetic (ESDG_FP64_FF): thresholds as in FP64, tested on hi
-template <>
-struct Num<ff> {
-    static __device__ __forceinline__ ff rcp(ff x) { return ff_rcp(x); }
-    static __device__ __forceinline__ bool close(ff d) {
-        return (__float_as_uint(d.hi) & 0x7fffffffu) < 0x3CA3D70Au;  // |d| < 0.02
-    }
-    static __device__ __forceinline__ ff log_(ff x) { return ff_log(x); }
-    static __device__ __forceinline__ bool close_ratio(ff f) {
-        return (__float_as_uint(f.hi) & 0x7fffffffu) < 0x3C23D70Au;  // |f| < 0.01
-    }
-};
 // two FP32 pair evaluations in packed registers: per-half estimate and test
 template <>
 struct Num<p2> {
     static __device__ __forceinline__ p2 rcp(p2 x) { return p2(Num<float>::rcp(x.v.x), Num<float>::rcp(x.v.y)); }
     static __device__ __forceinline__ m2 close(p2 d) { return m2{Num<float>::close(d.v.x), Num<float>::close(d.v.y)}; }
-};
-// x > 0 (false for NaN), for the non-physical-state check
-__device__ __forceinline__ bool positive(double x) { return x > 0.0; }
-__device__ __forceinline__ bool positive(float x) { return x > 0.0f; }
-__device__ __forceinline__ bool positive(ff x) { return x.hi > 0.0f; }
-
-template <typename C>
-struct IsFF {
-    static constexpr bool value = false;
-};
-template <>
-struct IsFF<ff> {
-    static constexpr bool value = true;
-};
-
-template <typename T>
-__device__ __forceinline__ T shfl(T v, int src) {
-    return __shfl_sync(0xffffffffu, v, src);
-}
-template <>
-__device__ __forceinline__ ff shfl<ff>(ff v, int src) {
-    return shfl_ff(v, src);
-}
-
-// Conversion between the I/O type T of the kernel's arguments and the type C
-// its pair arithmetic runs in (the same type, or float-float for FP64 I/O).
-template <typename T, typename C>
-struct Conv {
-    static __device__ __forceinline__ C in(T x) { return x; }
-    static __device__ __forceinline__ T out(C x) { return x; }
-};
-template <>
-struct Conv<double, ff> {
-    static __device__ __forceinline__ ff in(double x) { return ff_split(x); }
-    static __device__ __forceinline__ double out(ff x) { return ff_join(x); }
 };
 
 // Node (a, b, c) of line `ell` of direction R at line position p.  R may be
@@ -304,11 +214,13 @@ __device__ __forceinline__ NodeVals<p2> pack_vals(const NodeVals<float>& a, cons
 // registers.  Chosen per order from the order sweep on GB300 (ms at about
 // 6.4e7 nodes, unpacked -> packed): N = 4 3.44 -> 2.92, N = 5 3.64 -> 3.54,
 // N = 6 4.32 -> 4.23, N = 8 5.00 -> 4.47 (with two line sets per warp at N = 4,
-// 5, 8 for the registers); N = 3 ties and N = 7 was slower (3.17 -> 3.32), so
-// those keep one evaluation per instruction.
+// 5, 8 for the registers); N = 7 3.210 -> 3.188 with the pre-scaled node
+// values (the channel: 0.2183 -> 0.2167 ms; with two line sets per warp it
+// was slower, 3.281); N = 3 ties and keeps one evaluation per instruction.
 template <typename C, int N>
 struct PackPairs {
-    static constexpr bool value = std::is_same<C, float>::value && (N == 4 || N == 5 || N == 6 || N == 8);
+    static constexpr bool value =
+        std::is_same<C, float>::value && (N == 4 || N == 5 || N == 6 || N == 7 || N == 8);
 };
 
 // One pair (i, m) of a line, evaluated once for both nodes.  cq = Q_{pp'}
