@@ -104,7 +104,7 @@ NOMINAL_FP64_TFLOPS = 1.25  # GB300 FP64 vector, nominal
 
 
 _CSRC = os.path.join(ROOT, "flux_differencing_gb300", "csrc")
-_NUMERIC = ("numeric.cuh", "floatfloat.cuh", "log_fp64.cuh", "log_table.inc", "esdg_internal.h")
+_NUMERIC = ("numeric.cuh", "floatfloat.cuh", "log_fp64.cuh", "log_table.inc", "esdg_internal.h", "surface_flux.cuh")
 KERNEL_SOURCES = {
     "volume": [os.path.join(_CSRC, f) for f in ("volume_kernel.cuh", "packed.cuh", "volume_inst.cu") + _NUMERIC],
     "surface": [os.path.join(_CSRC, f) for f in ("surface_kernel.cu",) + _NUMERIC],
@@ -277,7 +277,7 @@ def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier, what="volu
 
     what: "volume" (one launch), "surface" (three launches, accumulating into
     out), "rhs" (volume then surface: four launches), "step" (one five-stage
-    Runge-Kutta step: 25 launches, on a copy of q) or "stage" (one
+    Runge-Kutta step: 5 to 25 launches, on a copy of q) or "stage" (one
     Runge-Kutta stage update)."""
     import torch
 
@@ -789,6 +789,20 @@ def _surface_report(cfg, sres, ws, alu_peak_tflops, alu_peak_name, hbm_peak_gbs)
     }
 
 
+def step_launches(precision: str) -> int:
+    """Kernel launches of one esdg_lsrk_step (five stages)."""
+    return {"fp64": 25, "fp64ff": 20, "fp32": 5}[precision]
+
+
+_STEP_WHAT = {
+    "fp64": "volume + surface (esdg_rhs), then the stage kernel",
+    "fp64ff": "the surface term, then the volume kernel adding it and applying the stage update in its store",
+    "fp32": "one launch: the volume kernel also evaluates its elements' faces (reading the neighbours' face "
+            "traces) and applies the stage update in its store, q and rhs alternating as state buffers; "
+            "one device copy of the state back to q per step",
+}
+
+
 def _step_report(cfg, res, ws, hbm_peak_gbs):
     """One five-stage Runge-Kutta step: time, throughput and per-kernel shares."""
     st = res["step"]
@@ -796,15 +810,19 @@ def _step_report(cfg, res, ws, hbm_peak_gbs):
     stage_t = statistics.mean(st["stage_per"]) * 1e-3
     gbs = RK_STAGE_VALUES * es * cfg.n / stage_t / 1e9
     srf = 5 * res["surface"]["ms"]
-    fused = cfg.precision != "fp64"
-    return {"what": "five-stage low-storage Runge-Kutta step (esdg_lsrk_step): per stage "
-                    + ("the surface term, then the volume kernel adding it and applying the stage update "
-                       "in its store" if fused else "volume + surface (esdg_rhs), then the stage kernel"),
-            "ms_per_step": st["ms"], "launches_per_step": 25 if cfg.precision == "fp64" else 20,
+    if cfg.precision == "fp64":
+        shares = {"volume": 5 * res["ms"] / st["ms"], "surface": srf / st["ms"],
+                  "rk_stage": 5 * st["stage_ms"] / st["ms"]}
+    elif cfg.precision == "fp64ff":
+        shares = {"surface": srf / st["ms"], "volume_with_fused_update": 1.0 - srf / st["ms"]}
+    else:
+        # one fused launch per stage: its time over the plain volume kernel's
+        shares = {"fused_stage_ms": st["ms"] / 5, "volume_only_ms": res["ms"],
+                  "fused_over_volume_only": st["ms"] / 5 / res["ms"]}
+    return {"what": "five-stage low-storage Runge-Kutta step (esdg_lsrk_step): per stage " + _STEP_WHAT[cfg.precision],
+            "ms_per_step": st["ms"], "launches_per_step": step_launches(cfg.precision),
             "GDOF/s": ws * cfg.n / (st["ms"] * 1e-3) / 1e9,
-            "shares": ({"surface": srf / st["ms"], "volume_with_fused_update": 1.0 - srf / st["ms"]} if fused else
-                       {"volume": 5 * res["ms"] / st["ms"], "surface": srf / st["ms"],
-                        "rk_stage": 5 * st["stage_ms"] / st["ms"]}),
+            "shares": shares,
             "standalone_rk_stage": {"ms": st["stage_ms"], "bound": "hbm", "achieved_GB/s": gbs,
                                     "peak_GB/s": hbm_peak_gbs, "frac": gbs / hbm_peak_gbs if hbm_peak_gbs else None,
                                     "algorithmic_bytes_per_node": RK_STAGE_VALUES * es,
@@ -813,7 +831,7 @@ def _step_report(cfg, res, ws, hbm_peak_gbs):
 
 
 def run_graph_sweep(args, device, stream):
-    """One five-stage time step of small meshes, launched eagerly (20-25
+    """One five-stage time step of small meshes, launched eagerly (5-25
     launches per step from the host) and replayed from a CUDA graph captured
     once: where the kernels are short, the launch path is the cost."""
     import torch
@@ -860,7 +878,7 @@ def run_graph_sweep(args, device, stream):
         replay = g0.elapsed_time(g1) / steps
         assert op.status() == 0
         print(json.dumps({"sweep": "graph", "config": cfg.name, "N": cfg.N, "K": cfg.K, "nodes": cfg.n,
-                          "precision": cfg.precision, "launches_per_step": 25 if cfg.precision == "fp64" else 20,
+                          "precision": cfg.precision, "launches_per_step": step_launches(cfg.precision),
                           "eager_ms_per_step": eager, "graph_ms_per_step": replay,
                           "speedup": eager / replay}), flush=True)
         op.close()

@@ -158,6 +158,19 @@ esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja
 }
 
 template <typename T>
+esdg::SurfaceConsts<T> surface_consts(const esdg_ctx* h) {
+    const long double g = h->gamma;
+    esdg::SurfaceConsts<T> k;
+    k.gm1 = (T)(g - 1);
+    k.igm1 = (T)(1 / (g - 1));
+    k.c_g = (T)(1 / (2 * (g - 1)));
+    k.gamma = (T)g;
+    k.c_ac = (T)(1 / (2 * g));
+    k.c_en = (T)((g - 1) / g);
+    return k;
+}
+
+template <typename T>
 esdg::SurfaceArgs<T> surface_args(const esdg_ctx* h, const void* q, const void* Ja, const void* phi, void* out,
                                   int form) {
     esdg::SurfaceArgs<T> a;
@@ -174,13 +187,7 @@ esdg::SurfaceArgs<T> surface_args(const esdg_ctx* h, const void* q, const void* 
     a.form = form;
     a.dissipation = h->dissipation;
     a.inv_w0 = (T)(1.0L / (long double)h->weights[0]);
-    const long double g = h->gamma;
-    a.k.gm1 = (T)(g - 1);
-    a.k.igm1 = (T)(1 / (g - 1));
-    a.k.c_g = (T)(1 / (2 * (g - 1)));
-    a.k.gamma = (T)g;
-    a.k.c_ac = (T)(1 / (2 * g));
-    a.k.c_en = (T)((g - 1) / g);
+    a.k = surface_consts<T>(h);
     a.status = h->d_status;
     a.rho_ref = static_cast<const T*>(h->ref_rho);
     a.p_ref = static_cast<const T*>(h->ref_p);
@@ -544,25 +551,36 @@ int esdg_rk_stage(esdg_handle h, void* q, void* dq, const void* rhs, const void*
 // One fused stage: the surface term (skew form) accumulated into S at face
 // nodes, then the volume kernel (skew form) adds it and applies the stage
 // update to dq and q in its store, resetting S to zero where it read it.
-static int fused_stage(esdg_handle h, void* q, void* dq, void* S, const void* metrics, const void* phi,
-                       const void* J, double A, double B, double dt, void* stream) {
-    if (int rc = surface_form(h, q, metrics, phi, S, stream, ESDG_FORM_SKEW)) return rc;
+// One fused stage.  FP32: volume and surface in one launch, reading q and
+// writing the new state to q_out (!= q).  Float-float: the surface term into
+// S, then the volume kernel consuming S and updating q in place (q_out == q).
+static int fused_stage(esdg_handle h, void* q, void* q_out, void* dq, void* S, const void* metrics,
+                       const void* phi, const void* J, double A, double B, double dt, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (h->precision == ESDG_FP32) {
         auto a = volume_args<float>(h, q, metrics, phi, nullptr, 0, h->K, h->op32, ESDG_FORM_SKEW);
         a.rk_q = static_cast<float*>(q);
+        a.rk_qout = static_cast<float*>(q_out);
         a.rk_dq = static_cast<float*>(dq);
-        a.rk_S = static_cast<float*>(S);
         a.rk_J = static_cast<const float*>(J);
         a.rk_A = (float)A;
         a.rk_B = (float)B;
         a.rk_dt = (float)dt;
         a.rk_f = (float)h->coriolis;
+        a.Kx = h->Kx;
+        a.Ky = h->Ky;
+        a.Kz = h->Kz;
+        for (int r = 0; r < 3; ++r) a.bc[r] = h->bc[r];
+        a.dissipation = h->dissipation;
+        a.inv_w0 = (float)(1.0L / (long double)h->weights[0]);
+        a.sk = surface_consts<float>(h);
         e = dispatch_fp32(h->N, a, s);
     } else {
+        if (int rc = surface_form(h, q, metrics, phi, S, stream, ESDG_FORM_SKEW)) return rc;
         auto a = volume_args<double>(h, q, metrics, phi, nullptr, 0, h->K, h->op64, ESDG_FORM_SKEW);
         a.rk_q = static_cast<double*>(q);
+        a.rk_qout = static_cast<double*>(q);
         a.rk_dq = static_cast<double*>(dq);
         a.rk_S = static_cast<double*>(S);
         a.rk_J = static_cast<const double*>(J);
@@ -605,13 +623,25 @@ int esdg_lsrk_step(esdg_handle h, void* q, void* dq, void* rhs, const void* metr
         }
         return ESDG_OK;
     }
-    // rhs serves as the face accumulator S: zero at the start, and every stage
-    // leaves it zero again
+    if (h->precision == ESDG_FP32) {
+        // state buffers alternate q -> rhs -> q ...; five stages end in rhs
+        void* buf[2] = {q, rhs};
+        for (int k = 0; k < 5; ++k)
+            if (int rc = fused_stage(h, buf[k & 1], buf[(k + 1) & 1], dq, nullptr, metrics, phi, J,
+                                     lsrk_coef(kLsrkA[k]), lsrk_coef(kLsrkB[k]), dt, stream))
+                return rc;
+        const cudaError_t e =
+            cudaMemcpyAsync(q, rhs, 5 * nb, cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(h, e, "copying the new state back to q");
+        return ESDG_OK;
+    }
+    // float-float: rhs serves as the face accumulator S: zero at the start,
+    // and every stage leaves it zero again
     cudaError_t e = cudaMemsetAsync(rhs, 0, 5 * nb, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "clearing the surface accumulator");
     for (int k = 0; k < 5; ++k)
-        if (int rc = fused_stage(h, q, dq, rhs, metrics, phi, J, lsrk_coef(kLsrkA[k]), lsrk_coef(kLsrkB[k]), dt,
-                                 stream))
+        if (int rc = fused_stage(h, q, q, dq, rhs, metrics, phi, J, lsrk_coef(kLsrkA[k]), lsrk_coef(kLsrkB[k]),
+                                 dt, stream))
             return rc;
     return ESDG_OK;
 }

@@ -21,6 +21,17 @@ struct OpTables {
     T invw[kMaxNq];
 };
 
+// Surface term: constants derived from gamma.
+template <typename T>
+struct SurfaceConsts {
+    T gm1;     // gamma - 1
+    T igm1;    // 1/(gamma - 1)
+    T c_g;     // 1/(2 (gamma - 1))
+    T gamma;
+    T c_ac;    // 1/(2 gamma): acoustic-wave entry of the eigenvector scaling
+    T c_en;    // (gamma - 1)/gamma: entropy-wave entry of the eigenvector scaling
+};
+
 template <typename T>
 struct VolumeArgs {
     const T* q;        // 5 planes
@@ -38,14 +49,27 @@ struct VolumeArgs {
     const T* rho_ref;  // reference density (1 plane) or nullptr: q is then the full state
     const T* p_ref;    // reference pressure (1 plane), with rho_ref
     // Fused Runge-Kutta stage (rk_q != nullptr): instead of writing out, each
-    // node takes rhs = volume + rk_S (rk_S: the surface term accumulated at
-    // face nodes, consumed and reset to zero there) and applies
-    // dq <- A dq + dt (h - rhs/J), q <- q + B dq to rk_dq and rk_q (== q).
+    // node takes rhs = volume + surface and applies
+    // dq <- A dq + dt (h - rhs/J), q <- q + B dq to rk_dq and q.
+    //  * float-float: the surface term comes accumulated in rk_S at face
+    //    nodes (consumed and reset to zero there); q is updated in place
+    //    (rk_q == q, rk_qout == rk_q).
+    //  * FP32: the kernel evaluates each element's faces itself (one-sided,
+    //    with the surface fields below) and writes the new state to rk_qout,
+    //    a second buffer: neighbouring elements read their face traces from q
+    //    during the launch.  rk_S is unused.
     T* rk_q;
+    T* rk_qout;
     T* rk_dq;
     T* rk_S;
     const T* rk_J;
     T rk_A, rk_B, rk_dt, rk_f;
+    // surface fields of the FP32 fused stage
+    long long Kx, Ky, Kz;  // element e = ex + Kx (ey + Ky ez)
+    int bc[3];             // per direction: 0 periodic, 1 slip wall
+    int dissipation;       // 0: entropy-conserving interface flux only
+    T inv_w0;              // 1 / (LGL end weight)
+    SurfaceConsts<T> sk;
     OpTables<T> ops;
 };
 
@@ -64,17 +88,6 @@ ESDG_DECLARE_LAUNCH(6)
 ESDG_DECLARE_LAUNCH(7)
 ESDG_DECLARE_LAUNCH(8)
 #undef ESDG_DECLARE_LAUNCH
-
-// Surface term: constants derived from gamma.
-template <typename T>
-struct SurfaceConsts {
-    T gm1;     // gamma - 1
-    T igm1;    // 1/(gamma - 1)
-    T c_g;     // 1/(2 (gamma - 1))
-    T gamma;
-    T c_ac;    // 1/(2 gamma): acoustic-wave entry of the eigenvector scaling
-    T c_en;    // (gamma - 1)/gamma: entropy-wave entry of the eigenvector scaling
-};
 
 template <typename T>
 struct SurfaceArgs {

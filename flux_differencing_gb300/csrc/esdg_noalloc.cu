@@ -65,7 +65,7 @@ void fill_ops(esdg::OpTables<T>& t, int N) {
 template <typename T>
 cudaError_t launch_noalloc(long K, int N, int form, double gamma, const void* q, const void* Ja, const void* phi,
                            void* out, unsigned* status, cudaStream_t s) {
-    esdg::VolumeArgs<T> a;
+    esdg::VolumeArgs<T> a{};  // value-initialised: the fused-stage fields stay null
     a.q = static_cast<const T*>(q);
     a.Ja = static_cast<const T*>(Ja);
     a.phi = static_cast<const T*>(phi);

@@ -72,6 +72,7 @@
 #include "floatfloat.cuh"
 #include "numeric.cuh"
 #include "packed.cuh"
+#include "surface_flux.cuh"
 
 namespace esdg {
 
@@ -223,6 +224,72 @@ struct PackPairs {
         std::is_same<C, float>::value && (N == 4 || N == 5 || N == 6 || N == 7 || N == 8);
 };
 
+// The FP32 fused Runge-Kutta stage evaluates the surface term inside this
+// kernel: every element takes each of its face nodes from its own side (the
+// interface flux of surface_flux.cuh), reading the neighbour's trace while it
+// loads its own element, so the planes are read once per stage instead of
+// once more per direction by the face-centric surface kernel (whose xi and
+// eta passes touch every DRAM line).  Each interface is evaluated twice, once
+// per side; FP32 has the issue slots for that.  Float-float keeps the
+// separate surface kernel and the face accumulator.
+template <typename C>
+struct FusedSurface {
+    static constexpr bool value = std::is_same<C, float>::value;
+};
+
+// Face slots of a CTA: slot = el PER_EL + (2 dir + side) NF + i1 + NQ i2, with
+// side 0 the face at index 0 along direction dir, side 1 the face at index
+// N, and (i1, i2) the node's other two indices in (a, b, c) order.  The face
+// buffer holds FIELDS values per slot (neighbour q, its metric row of the
+// face direction, phi, rho_ref, p_ref), replaced by the slot's surface
+// contribution (5 values) in the face phase.
+template <int N>
+struct FaceSlots {
+    static constexpr int NQ = N + 1;
+    static constexpr int NF = NQ * NQ;
+    static constexpr int PER_EL = 6 * NF;
+    static constexpr int COUNT = PER_EL * Shape<N>::EPB;
+    static constexpr int FIELDS = 11;
+    static __device__ __forceinline__ int slot(int el, int dir, int side, int i1, int i2) {
+        return el * PER_EL + (2 * dir + side) * NF + i1 + NQ * i2;
+    }
+    static __device__ __forceinline__ void decode(int s, int& el, int& dir, int& side, int& i1, int& i2) {
+        el = s / PER_EL;
+        const int r = s - el * PER_EL;
+        const int f = r / NF;
+        const int w = r - f * NF;
+        dir = f >> 1;
+        side = f & 1;
+        i1 = w % NQ;
+        i2 = w / NQ;
+    }
+    // (a, b, c) of the node at index A along dir with other indices (i1, i2)
+    static __device__ __forceinline__ void node(int dir, int A, int i1, int i2, int& na, int& nb, int& nc) {
+        na = dir == 0 ? A : i1;
+        nb = dir == 1 ? A : (dir == 0 ? i1 : i2);
+        nc = dir == 2 ? A : i2;
+    }
+};
+
+// The element across face (dir, side) of element e and the node there that
+// faces node (i1, i2); false at a slip wall (no neighbour).
+template <int N, typename T>
+__device__ __forceinline__ bool face_neighbour(const VolumeArgs<T>& a, long long e, int dir, int side, int i1, int i2,
+                                               long long& g) {
+    constexpr int NQ = N + 1;
+    const long long Kd = dir == 0 ? a.Kx : dir == 1 ? a.Ky : a.Kz;
+    const long long stride = dir == 0 ? 1 : dir == 1 ? a.Kx : a.Kx * a.Ky;
+    const long long r = (e / stride) % Kd;  // element index along dir
+    long long en;
+    if (side) en = r + 1 < Kd ? e + stride : (a.bc[dir] ? -1 : e - (Kd - 1) * stride);
+    else en = r > 0 ? e - stride : (a.bc[dir] ? -1 : e + (Kd - 1) * stride);
+    if (en < 0) return false;
+    int na, nb, nc;
+    FaceSlots<N>::node(dir, side ? 0 : N, i1, i2, na, nb, nc);
+    g = en * (long long)(NQ * NQ * NQ) + na + NQ * (nb + NQ * nc);
+    return true;
+}
+
 // One pair (i, m) of a line, evaluated once for both nodes.  cq = Q_{pp'}
 // with p, p' the positions of i and m.  Adds node i's share 2Q_{pp'} (F +
 // G(i,m)) to o0..o4 and returns node m's share 2Q_{p'p} (F + G(m,i)) =
@@ -346,8 +413,8 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
 // Runge-Kutta stage, plus the surface term at face nodes, as a stage update of
 // dq and q (the node's own element only, so updating q in place is safe).
 template <typename T, int N, bool RK>
-__device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, int na, int nb, int nc, T t0,
-                                           T t1, T t2, T t3, T t4) {
+__device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, int na, int nb, int nc, int el,
+                                           const T* __restrict__ fb, T t0, T t1, T t2, T t3, T t4) {
     const long long n = a.n;
     if constexpr (!RK) {
         T* __restrict__ o = a.out;
@@ -361,7 +428,9 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
     // every load first, through restrict-qualified pointers: loads interleaved
     // with stores through possibly aliasing pointers would each wait for DRAM
     // in turn (measured 1.0 ms against 0.22 ms for the plain FP32 kernel)
-    T* __restrict__ qp = a.rk_q;
+    constexpr bool FUSED = FusedSurface<T>::value;
+    const T* __restrict__ qp = a.rk_q;
+    T* __restrict__ qo = FUSED ? a.rk_qout : a.rk_q;
     T* __restrict__ dqp = a.rk_dq;
     T* __restrict__ Sp = a.rk_S;
     const bool face = na == 0 || na == N || nb == 0 || nb == N || nc == 0 || nc == N;
@@ -371,7 +440,22 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
     for (int v = 0; v < 5; ++v) {
         qv[v] = qp[v * n + g];
         dqv[v] = use_dq ? dqp[v * n + g] : T(0);
-        sv[v] = face ? Sp[v * n + g] : T(0);
+        sv[v] = (!FUSED && face) ? Sp[v * n + g] : T(0);
+    }
+    if constexpr (FUSED) {
+        // this node's face contributions from the face phase, in the fixed
+        // order xi, eta, zeta
+        using FSL = FaceSlots<N>;
+        auto add_slot = [&](int sl) {
+#pragma unroll
+            for (int v = 0; v < 5; ++v) sv[v] += fb[v * FSL::COUNT + sl];
+        };
+        if (na == 0) add_slot(FSL::slot(el, 0, 0, nb, nc));
+        else if (na == N) add_slot(FSL::slot(el, 0, 1, nb, nc));
+        if (nb == 0) add_slot(FSL::slot(el, 1, 0, na, nc));
+        else if (nb == N) add_slot(FSL::slot(el, 1, 1, na, nc));
+        if (nc == 0) add_slot(FSL::slot(el, 2, 0, na, nb));
+        else if (nc == N) add_slot(FSL::slot(el, 2, 1, na, nb));
     }
     const T Jg = a.rk_J[g];
     const T sc = -a.rk_dt * Num<T>::rcp(Jg);
@@ -388,8 +472,8 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
     for (int v = 0; v < 5; ++v) {
         const T d = use_dq ? fma(a.rk_A, dqv[v], dL[v]) : dL[v];
         dqp[v * n + g] = d;
-        qp[v * n + g] = fma(a.rk_B, d, qv[v]);
-        if (face) Sp[v * n + g] = T(0);
+        qo[v * n + g] = fma(a.rk_B, d, qv[v]);
+        if (!FUSED && face) Sp[v * n + g] = T(0);
     }
 }
 
@@ -524,7 +608,8 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         // linear node L*Nq + p is contiguous across lanes: coalesced stores
         static_assert(Layout<N>::ORD0 == 0, "xi lines must be dealt b-fastest");
         const long long g = node0 + (long long)L * NQ + p;
-        store_node<T, N, FINAL == 2>(a, g, ia, ib, ic, Conv<T, C>::out(fma(acc0, iw, s_acc[0 * FS + i])),
+        store_node<T, N, FINAL == 2>(a, g, ia, ib, ic, el, reinterpret_cast<const T*>(sm + F_COUNT * FS),
+                                     Conv<T, C>::out(fma(acc0, iw, s_acc[0 * FS + i])),
                          Conv<T, C>::out(fma(acc1, iw, s_acc[1 * FS + i])),
                          Conv<T, C>::out(fma(acc2, iw, s_acc[2 * FS + i])),
                          Conv<T, C>::out(fma(acc3, iw, s_acc[3 * FS + i])),
@@ -609,6 +694,75 @@ __device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, C* __res
         s_acc[2 * FS + j] = fma(t2, iwj, s_acc[2 * FS + j]);
         s_acc[3 * FS + j] = fma(t3, iwj, s_acc[3 * FS + j]);
         s_acc[4 * FS + j] = fma(-t4, iwj, s_acc[4 * FS + j]);
+    }
+}
+
+// Face phase of the FP32 fused stage: one thread per face slot evaluates the
+// interface flux of its face node from the element's own side (the node
+// owning the outward normal), with the neighbour's trace loaded into the face
+// buffer during the load phase, or a mirror ghost at a slip wall, and leaves
+// 1/w_0 times the contribution in the slot (read back by the node's final
+// store).  The own state comes from the shared-memory fields (pre-scaled by
+// powers of two, so it is the node state exactly).
+template <typename T, typename C, int N>
+__device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count, long long e0) {
+    using SL = Slots<N>;
+    using FSL = FaceSlots<N>;
+    constexpr int FS = SL::SIZE;
+    constexpr int CNT = FSL::COUNT;
+    C* fb = sm + F_COUNT * FS;
+    Consts<C> k;
+    k.gm1 = a.sk.gm1;
+    k.igm1 = a.sk.igm1;
+    k.c_g = a.sk.c_g;
+    k.gamma = a.sk.gamma;
+    k.c_ac = a.sk.c_ac;
+    k.c_en = a.sk.c_en;
+    const bool perturbed = a.rho_ref != nullptr;
+    for (int s = threadIdx.x; s < e_count * FSL::PER_EL; s += Launch<N, C>::THREADS) {
+        int el, dir, side, i1, i2, na, nb, nc;
+        FSL::decode(s, el, dir, side, i1, i2);
+        FSL::node(dir, side ? N : 0, i1, i2, na, nb, nc);
+        const int sl = SL::at(el, na, nb, nc);
+        FaceNode<C> I;
+        I.rho = sm[F_RHO * FS + sl];
+        I.u1 = C(2) * sm[F_U1 * FS + sl];
+        I.u2 = C(2) * sm[F_U2 * FS + sl];
+        I.u3 = C(2) * sm[F_U3 * FS + sl];
+        I.uu = fma(I.u3, I.u3, fma(I.u2, I.u2, I.u1 * I.u1));
+        I.b = C(0.5) * sm[F_B * FS + sl];
+        I.ib = sm[F_INVB * FS + sl];
+        I.phi = C(8) * sm[F_PHI * FS + sl];
+        I.p = C(0);  // p and E are not used by the interface flux
+        I.E = C(0);
+        const C j0 = sm[(F_JA0 + 3 * dir + 0) * FS + sl];
+        const C j1 = sm[(F_JA0 + 3 * dir + 1) * FS + sl];
+        const C j2 = sm[(F_JA0 + 3 * dir + 2) * FS + sl];
+        const C sg = side ? C(1) : C(-1);  // outward
+        long long g;
+        C fi[5], fo[5];
+        if (face_neighbour<N>(a, e0 + el, dir, side, i1, i2, g)) {
+            const FaceNode<C> J = node_state<C>(fb[0 * CNT + s], fb[1 * CNT + s], fb[2 * CNT + s], fb[3 * CNT + s],
+                                                fb[4 * CNT + s], fb[8 * CNT + s], k.gm1, perturbed,
+                                                fb[9 * CNT + s], fb[10 * CNT + s]);
+            const C n0 = sg * C(0.5) * (j0 + fb[5 * CNT + s]);
+            const C n1 = sg * C(0.5) * (j1 + fb[6 * CNT + s]);
+            const C n2 = sg * C(0.5) * (j2 + fb[7 * CNT + s]);
+            interface_flux(I, J, n0, n1, n2, k, a.dissipation != 0, fi, fo);
+        } else {
+            // slip wall: mirror ghost (rho, m - 2 (m.n^) n^, E), same phi
+            const C n0 = sg * j0, n1 = sg * j1, n2 = sg * j2;
+            const C inn = Num<C>::rcp(sqrt_(fma(n2, n2, fma(n1, n1, n0 * n0))));
+            const C h0 = n0 * inn, h1 = n1 * inn, h2 = n2 * inn;
+            const C un2 = C(2.0) * fma(I.u3, h2, fma(I.u2, h1, I.u1 * h0));
+            FaceNode<C> G = I;
+            G.u1 = fma(-un2, h0, I.u1);
+            G.u2 = fma(-un2, h1, I.u2);
+            G.u3 = fma(-un2, h2, I.u3);
+            interface_flux(I, G, n0, n1, n2, k, a.dissipation != 0, fi, fo);
+        }
+#pragma unroll
+        for (int v = 0; v < 5; ++v) fb[v * CNT + s] = a.inv_w0 * fi[v];
     }
 }
 
@@ -726,6 +880,28 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         sm[(F_ACC0 + 3) * FS + sl] = f3;
         sm[(F_ACC0 + 4) * FS + sl] = f4;
     }
+    if constexpr (RK && FusedSurface<C>::value) {
+        // neighbour traces of this CTA's face slots (walls: none)
+        using FSL = FaceSlots<N>;
+        constexpr int CNT = FSL::COUNT;
+        C* fb = sm + F_COUNT * FS;
+        const long long n = a.n;
+        for (int s = threadIdx.x; s < e_count * FSL::PER_EL; s += Launch<N, C>::THREADS) {
+            int el, dir, side, i1, i2;
+            FSL::decode(s, el, dir, side, i1, i2);
+            long long g;
+            if (!face_neighbour<N>(a, e0 + el, dir, side, i1, i2, g)) continue;
+#pragma unroll
+            for (int v = 0; v < 5; ++v) fb[v * CNT + s] = __ldg(a.q + v * n + g);
+#pragma unroll
+            for (int c = 0; c < 3; ++c) fb[(5 + c) * CNT + s] = __ldg(a.Ja + (3 * dir + c) * n + g);
+            fb[8 * CNT + s] = __ldg(a.phi + g);
+            if (a.rho_ref) {
+                fb[9 * CNT + s] = __ldg(a.rho_ref + g);
+                fb[10 * CNT + s] = __ldg(a.p_ref + g);
+            }
+        }
+    }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(a.status, 1u);
 
     // lane constants: Q_{p,p+d} for every offset, 1/w_p and 1/(gamma - 1)
@@ -771,10 +947,12 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
             const int sl = SL::at(el, na, nb, nc);
             const long long g = node0 + t;
-            store_node<T, N, RK>(a, g, na, nb, nc, CV::out(s_acc[0 * FS + sl]), CV::out(s_acc[1 * FS + sl]),
+            store_node<T, N, RK>(a, g, na, nb, nc, el, nullptr, CV::out(s_acc[0 * FS + sl]),
+                                 CV::out(s_acc[1 * FS + sl]),
                              CV::out(s_acc[2 * FS + sl]), CV::out(s_acc[3 * FS + sl]), CV::out(s_acc[4 * FS + sl]));
         }
     } else {
+        if constexpr (RK && FusedSurface<C>::value) face_phase<T, C, N>(a, sm, e_count, e0);
         direction_phase<T, C, N, 1, 0>(a, sm, e_count, node0, cq, iw, c_g);
         __syncthreads();
         direction_phase<T, C, N, 2, 0>(a, sm, e_count, node0, cq, iw, c_g);
@@ -796,7 +974,9 @@ cudaError_t launch_volume_mode(const VolumeArgs<T>& a, cudaStream_t s) {
     using S = Shape<N>;
     const long long K = a.e_end - a.e_begin;
     if (K <= 0) return cudaSuccess;
-    const size_t smem = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
+    const size_t smem = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE +
+                        ((RK && FusedSurface<C>::value) ? sizeof(C) * (size_t)FaceSlots<N>::FIELDS * FaceSlots<N>::COUNT
+                                                         : 0);
     static bool attr_done = false;  // per instantiation; set once per process
     if (!attr_done) {
         cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N, C, RK>,

@@ -222,16 +222,24 @@ int esdg_rk_stage(esdg_handle h, void* q, void* dq, const void* rhs, const void*
                   double dt, void* stream);
 
 /* One full time step of size dt: five stages of esdg_rhs (boundary kinds
- * and dissipation of the handle) and esdg_rk_stage.  For ESDG_FP32 and
- * ESDG_FP64_FF each stage is the surface term followed by the volume kernel
- * in a fused mode that adds the surface term and applies the stage update to
- * dq and q in its store, without writing and re-reading the right-hand side
- * (20 launches and one memset per step); native ESDG_FP64, bound by its FP64
- * pipe, keeps the separate stage kernel (25 launches).  Everything is on
- * `stream`, with no synchronisation and no allocation
- * (so the call can be captured into a CUDA graph).  rhs is scratch (5*n
- * values, used as the surface accumulator).  q, dq, rhs and J must not
- * overlap one another, metrics or phi.  Errors: as the component calls. */
+ * and dissipation of the handle) and esdg_rk_stage, the same arithmetic
+ * organised per precision:
+ *  - ESDG_FP32: one launch per stage.  The volume kernel also evaluates each
+ *    element's faces (from the element's own side, reading the neighbours'
+ *    face traces) and applies the stage update in its store; since the
+ *    neighbours read q during the launch, stages alternate between q and
+ *    rhs as state buffers and a final device copy returns the state to q
+ *    (5 launches and one copy per step).
+ *  - ESDG_FP64_FF: per stage the surface term into an accumulator, then the
+ *    volume kernel adding it and applying the update in place (20 launches
+ *    and one memset per step).
+ *  - ESDG_FP64, bound by its FP64 pipe: esdg_rhs and the separate stage
+ *    kernel (25 launches).
+ * Everything is on `stream`, with no synchronisation and no allocation (so
+ * the call can be captured into a CUDA graph).  rhs is scratch (5*n values:
+ * the second state buffer, the surface accumulator or the right-hand side).
+ * q, dq, rhs and J must not overlap one another, metrics or phi.  Errors: as
+ * the component calls. */
 int esdg_lsrk_step(esdg_handle h, void* q, void* dq, void* rhs, const void* metrics, const void* phi,
                    const void* J, double dt, void* stream);
 
