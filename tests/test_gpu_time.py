@@ -73,6 +73,76 @@ def test_lsrk_step_parity(N, precision):
     assert err.max() < hz.TOL[precision], err
 
 
+@pytest.mark.parametrize("N,K,bc,dissipation", [
+    (1, (5, 3, 2), (0, 1, 0), True),   # 30 elements: two 16-element CTAs, neighbours inside one CTA
+    (3, (3, 1, 2), (0, 0, 1), True),   # one element along eta, periodic: the face's neighbour is itself
+    (4, (2, 3, 2), (1, 1, 1), True),   # walls on every side
+    (7, (2, 2, 3), (0, 0, 0), True),   # fully periodic
+    (5, (3, 2, 2), (0, 1, 1), False),  # entropy-conserving interface flux (no dissipation)
+])
+def test_lsrk_fp32_fused_stage_two_steps(N, K, bc, dissipation):
+    """The FP32 step (one launch per stage, faces evaluated inside the volume
+    kernel, q and rhs alternating as state buffers) against two oracle steps,
+    on meshes that exercise the face-slot and neighbour indexing: several
+    elements per CTA, a single element along a periodic direction, walls on
+    every side, full periodicity, and the flux without dissipation."""
+    cfg = wl.small_config(N, K=K, warp=True, state="noisy", precision="fp32", bc=bc)
+    g, op, Ja, J, q, phi = _setup(cfg, dissipation=dissipation)
+    qn, phin = g["q"].numpy(), g["phi"].numpy()
+    dt = _stable_dt(cfg, qn, phin)
+    dq = torch.zeros_like(q)
+    rhs = torch.empty_like(q)
+    for _ in range(2):
+        op.lsrk_step(q, dq, rhs, Ja, phi, J, dt)
+    torch.cuda.synchronize()
+    assert op.status() == 0
+    got = q.double().cpu().numpy()
+    Jao, Jo = oracle.metrics(N, cfg.K, g["x"].numpy(), g["y"].numpy(), g["z"].numpy())
+    K3 = (cfg.Kx, cfg.Ky, cfg.Kz)
+    ref, dqo = lsrk.lsrk_step(N, K3, qn, np.zeros_like(qn), Jao, phin, Jo, dt, bc=cfg.bc, dissipation=dissipation)
+    ref, _ = lsrk.lsrk_step(N, K3, ref, dqo, Jao, phin, Jo, dt, bc=cfg.bc, dissipation=dissipation)
+    _, vs = oracle.volume(N, cfg.K, qn, Jao, phin, with_scale=True)
+    _, ss = oracle.surface(N, K3, qn, Jao, phin, cfg.bc, dissipation=dissipation, with_scale=True)
+    scale = 2 * dt * np.max((vs + ss) / Jo, axis=1) + 16 * EPS["fp32"] * np.max(np.abs(qn), axis=1)
+    err = np.max(np.abs(got - ref), axis=1) / scale
+    assert err.max() < hz.TOL["fp32"], err
+
+
+def test_lsrk_fp32_fused_stage_perturbation_variables():
+    """The fused FP32 step on perturbation variables (neighbour traces include
+    rho_ref and p_ref) against the oracle step on the full FP64 state."""
+    cfg = wl.small_config(4, K=(3, 2, 2), warp=True, state="noisy", precision="fp32", bc=(0, 1, 1))
+    g, op, Ja, J, q, phi = _setup(cfg)
+    ref_state = wl.reference_state(cfg)
+    rr, pr = ref_state["rho_ref"], ref_state["p_ref"]
+    op.set_reference(rr.to("cuda", torch.float32).contiguous(), pr.to("cuda", torch.float32).contiguous())
+    qn, phin = g["q"].numpy(), g["phi"].numpy()
+    qp = g["q"].clone()
+    qp[0] -= rr
+    qp[4] -= pr / 0.4 + rr * g["phi"]
+    q = qp.to("cuda", torch.float32).contiguous()
+    dt = _stable_dt(cfg, qn, phin)
+    dq = torch.zeros_like(q)
+    rhs = torch.empty_like(q)
+    op.lsrk_step(q, dq, rhs, Ja, phi, J, dt)
+    torch.cuda.synchronize()
+    assert op.status() == 0
+    got = q.double().cpu()
+    got[0] += rr
+    got[4] += pr / 0.4 + rr * g["phi"]
+    got = got.numpy()
+    Jao, Jo = oracle.metrics(4, cfg.K, g["x"].numpy(), g["y"].numpy(), g["z"].numpy())
+    K3 = (cfg.Kx, cfg.Ky, cfg.Kz)
+    ref, _ = lsrk.lsrk_step(4, K3, qn, np.zeros_like(qn), Jao, phin, Jo, dt, bc=cfg.bc)
+    _, vs = oracle.volume(4, cfg.K, qn, Jao, phin, with_scale=True)
+    _, ss = oracle.surface(4, K3, qn, Jao, phin, cfg.bc, with_scale=True)
+    # the change q(t+dt) - q(t) in FP32 perturbation storage: rounding of the
+    # small stored values instead of the full state
+    scale = dt * np.max((vs + ss) / Jo, axis=1) + 8 * EPS["fp32"] * np.max(np.abs(qp.numpy()), axis=1)
+    err = np.max(np.abs(got - ref), axis=1) / scale
+    assert err.max() < hz.TOL["fp32"], err
+
+
 @pytest.mark.parametrize("precision", ["fp64", "fp32"])
 def test_diagnostics_parity(precision):
     cfg = wl.small_config(4, K=(3, 2, 2), warp=True, state="noisy", precision=precision)
@@ -110,6 +180,27 @@ def test_gpu_conservation_and_entropy_over_steps(bc):
         assert s < prev
         prev = s
     assert op.status() == 0
+
+
+@pytest.mark.parametrize("bc", [(0, 0, 0), (1, 1, 1)])
+def test_fp32_global_conservation_over_steps(bc):
+    """FP32 steps (the fused stage, each interface evaluated once from each
+    side): integrated mass and total energy stay within the FP32 level the
+    paper reports for its 32-bit runs (relative variations ~1e-6, Sec. 5.2)
+    over 20 steps; the one-sided face evaluations cancel to rounding."""
+    cfg = wl.small_config(3, K=(3, 3, 2), warp=True, state="noisy", precision="fp32", bc=bc)
+    g, op, Ja, J, q, phi = _setup(cfg)
+    dt = _stable_dt(cfg, g["q"].numpy(), g["phi"].numpy())
+    dq = torch.zeros_like(q)
+    rhs = torch.empty_like(q)
+    m0, e0, _ = op.diagnostics(q, J, phi).cpu().numpy()
+    worst = [0.0, 0.0]
+    for _ in range(20):
+        op.lsrk_step(q, dq, rhs, Ja, phi, J, dt)
+        m, e, _ = op.diagnostics(q, J, phi).cpu().numpy()
+        worst = [max(worst[0], abs(m - m0) / abs(m0)), max(worst[1], abs(e - e0) / abs(e0))]
+    assert op.status() == 0
+    assert worst[0] < 1e-6 and worst[1] < 1e-6, worst
 
 
 def test_gpu_coriolis_rotation():
