@@ -271,23 +271,48 @@ struct FaceSlots {
     }
 };
 
-// The element across face (dir, side) of element e and the node there that
-// faces node (i1, i2); false at a slip wall (no neighbour).
-template <int N, typename T>
-__device__ __forceinline__ bool face_neighbour(const VolumeArgs<T>& a, long long e, int dir, int side, int i1, int i2,
-                                               long long& g) {
-    constexpr int NQ = N + 1;
+// The element across face (dir, side) of element e, or -1 at a slip wall
+// (64-bit divisions: evaluated once per element and face, into the CTA's
+// neighbour table).
+template <typename T>
+__device__ __forceinline__ long long neighbour_element(const VolumeArgs<T>& a, long long e, int dir, int side) {
     const long long Kd = dir == 0 ? a.Kx : dir == 1 ? a.Ky : a.Kz;
     const long long stride = dir == 0 ? 1 : dir == 1 ? a.Kx : a.Kx * a.Ky;
     const long long r = (e / stride) % Kd;  // element index along dir
-    long long en;
-    if (side) en = r + 1 < Kd ? e + stride : (a.bc[dir] ? -1 : e - (Kd - 1) * stride);
-    else en = r > 0 ? e - stride : (a.bc[dir] ? -1 : e + (Kd - 1) * stride);
+    if (side) return r + 1 < Kd ? e + stride : (a.bc[dir] ? -1 : e - (Kd - 1) * stride);
+    return r > 0 ? e - stride : (a.bc[dir] ? -1 : e + (Kd - 1) * stride);
+}
+
+// Global index of the node across face (dir, side) from node (i1, i2) of
+// local element el, with the neighbour table nbr[6 el + 2 dir + side]; false
+// at a slip wall.
+template <int N>
+__device__ __forceinline__ bool face_neighbour(const long long* nbr, int el, int dir, int side, int i1, int i2,
+                                               long long& g) {
+    constexpr int NQ = N + 1;
+    const long long en = nbr[6 * el + 2 * dir + side];
     if (en < 0) return false;
     int na, nb, nc;
     FaceSlots<N>::node(dir, side ? 0 : N, i1, i2, na, nb, nc);
     g = en * (long long)(NQ * NQ * NQ) + na + NQ * (nb + NQ * nc);
     return true;
+}
+
+// Dynamic shared memory of the volume kernel in bytes: the fields, and for
+// the FP32 fused stage the face buffer and the neighbour table behind them.
+template <typename C, int N, bool RK>
+constexpr size_t volume_smem_fields() {
+    return sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE +
+           ((RK && FusedSurface<C>::value) ? sizeof(C) * (size_t)FaceSlots<N>::FIELDS * FaceSlots<N>::COUNT : 0);
+}
+template <typename C, int N, bool RK>
+constexpr size_t volume_smem_nbr_offset() {
+    return (volume_smem_fields<C, N, RK>() + 7) & ~(size_t)7;
+}
+template <typename C, int N, bool RK>
+constexpr size_t volume_smem_bytes() {
+    return (RK && FusedSurface<C>::value) ? volume_smem_nbr_offset<C, N, RK>() + 6 * sizeof(long long) * Shape<N>::EPB
+                                          : volume_smem_fields<C, N, RK>();
 }
 
 // One pair (i, m) of a line, evaluated once for both nodes.  cq = Q_{pp'}
@@ -705,7 +730,8 @@ __device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, C* __res
 // store).  The own state comes from the shared-memory fields (pre-scaled by
 // powers of two, so it is the node state exactly).
 template <typename T, typename C, int N>
-__device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count, long long e0) {
+__device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict__ sm, const long long* nbr,
+                                           int e_count) {
     using SL = Slots<N>;
     using FSL = FaceSlots<N>;
     constexpr int FS = SL::SIZE;
@@ -741,7 +767,7 @@ __device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict
         const C sg = side ? C(1) : C(-1);  // outward
         long long g;
         C fi[5], fo[5];
-        if (face_neighbour<N>(a, e0 + el, dir, side, i1, i2, g)) {
+        if (face_neighbour<N>(nbr, el, dir, side, i1, i2, g)) {
             const FaceNode<C> J = node_state<C>(fb[0 * CNT + s], fb[1 * CNT + s], fb[2 * CNT + s], fb[3 * CNT + s],
                                                 fb[4 * CNT + s], fb[8 * CNT + s], k.gm1, perturbed,
                                                 fb[9 * CNT + s], fb[10 * CNT + s]);
@@ -784,6 +810,17 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     const long long rem = a.e_end - e0;
     const int e_count = rem < S::EPB ? (int)rem : S::EPB;
     const long long node0 = e0 * NP3;
+
+    // FP32 fused stage: the element across each face of the CTA's elements
+    // (-1 at a slip wall), one entry per thread
+    long long* nbr = nullptr;
+    if constexpr (RK && FusedSurface<C>::value) {
+        nbr = reinterpret_cast<long long*>(smem_raw + volume_smem_nbr_offset<C, N, RK>());
+        static_assert(6 * S::EPB <= Launch<N, C>::THREADS, "one neighbour entry per thread");
+        const int t = threadIdx.x;
+        if (t < 6 * e_count) nbr[t] = neighbour_element(a, e0 + t / 6, (t % 6) >> 1, t & 1);
+        __syncthreads();
+    }
 
     // ---- load phase: one node per thread, coalesced plane reads -> derived values.
     // The per-node arithmetic runs in P: the I/O type for FP64 and FP32, and
@@ -890,7 +927,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             int el, dir, side, i1, i2;
             FSL::decode(s, el, dir, side, i1, i2);
             long long g;
-            if (!face_neighbour<N>(a, e0 + el, dir, side, i1, i2, g)) continue;
+            if (!face_neighbour<N>(nbr, el, dir, side, i1, i2, g)) continue;
 #pragma unroll
             for (int v = 0; v < 5; ++v) fb[v * CNT + s] = __ldg(a.q + v * n + g);
 #pragma unroll
@@ -952,7 +989,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
                              CV::out(s_acc[2 * FS + sl]), CV::out(s_acc[3 * FS + sl]), CV::out(s_acc[4 * FS + sl]));
         }
     } else {
-        if constexpr (RK && FusedSurface<C>::value) face_phase<T, C, N>(a, sm, e_count, e0);
+        if constexpr (RK && FusedSurface<C>::value) face_phase<T, C, N>(a, sm, nbr, e_count);
         direction_phase<T, C, N, 1, 0>(a, sm, e_count, node0, cq, iw, c_g);
         __syncthreads();
         direction_phase<T, C, N, 2, 0>(a, sm, e_count, node0, cq, iw, c_g);
@@ -974,9 +1011,7 @@ cudaError_t launch_volume_mode(const VolumeArgs<T>& a, cudaStream_t s) {
     using S = Shape<N>;
     const long long K = a.e_end - a.e_begin;
     if (K <= 0) return cudaSuccess;
-    const size_t smem = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE +
-                        ((RK && FusedSurface<C>::value) ? sizeof(C) * (size_t)FaceSlots<N>::FIELDS * FaceSlots<N>::COUNT
-                                                         : 0);
+    const size_t smem = volume_smem_bytes<C, N, RK>();
     static bool attr_done = false;  // per instantiation; set once per process
     if (!attr_done) {
         cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N, C, RK>,
