@@ -829,6 +829,34 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     using P = typename std::conditional<IsFF<C>::value, ff, T>::type;
     using PV = Conv<T, P>;
     bool bad = false;
+    // FP32 fused stage: the neighbour trace of this thread's first face slot
+    // is requested before the element's own planes, so that the latencies of
+    // the two sets of loads overlap; it is written to the face buffer after
+    // the node loop
+    constexpr bool FUSED = RK && FusedSurface<C>::value;
+    constexpr int TR = 11;  // trace values: q (5), metric row (3), phi, rho_ref, p_ref
+    C trace[FUSED ? TR : 1];
+    bool trace_ok = false;
+    if constexpr (FUSED) {
+        using FSL = FaceSlots<N>;
+        const int s = threadIdx.x;
+        if (s < e_count * FSL::PER_EL) {
+            int el, dir, side, i1, i2;
+            FSL::decode(s, el, dir, side, i1, i2);
+            long long g;
+            if (face_neighbour<N>(nbr, el, dir, side, i1, i2, g)) {
+                trace_ok = true;
+                const long long n = a.n;
+#pragma unroll
+                for (int v = 0; v < 5; ++v) trace[v] = __ldg(a.q + v * n + g);
+#pragma unroll
+                for (int c = 0; c < 3; ++c) trace[5 + c] = __ldg(a.Ja + (3 * dir + c) * n + g);
+                trace[8] = __ldg(a.phi + g);
+                trace[9] = a.rho_ref ? __ldg(a.rho_ref + g) : C(0);
+                trace[10] = a.rho_ref ? __ldg(a.p_ref + g) : C(0);
+            }
+        }
+    }
     for (int t = threadIdx.x; t < S::NODES; t += Launch<N, C>::THREADS) {
         const int el = t / NP3;
         const int nd = t - el * NP3;
@@ -918,12 +946,17 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         sm[(F_ACC0 + 4) * FS + sl] = f4;
     }
     if constexpr (RK && FusedSurface<C>::value) {
-        // neighbour traces of this CTA's face slots (walls: none)
+        // neighbour traces of this CTA's face slots (walls: none): the
+        // prefetched first slot, then any further slots of this thread
         using FSL = FaceSlots<N>;
         constexpr int CNT = FSL::COUNT;
         C* fb = sm + F_COUNT * FS;
         const long long n = a.n;
-        for (int s = threadIdx.x; s < e_count * FSL::PER_EL; s += Launch<N, C>::THREADS) {
+        if (trace_ok) {
+#pragma unroll
+            for (int v = 0; v < TR; ++v) fb[v * CNT + threadIdx.x] = trace[v];
+        }
+        for (int s = threadIdx.x + Launch<N, C>::THREADS; s < e_count * FSL::PER_EL; s += Launch<N, C>::THREADS) {
             int el, dir, side, i1, i2;
             FSL::decode(s, el, dir, side, i1, i2);
             long long g;
