@@ -650,15 +650,18 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
 //  * float-float: always 2 (256-thread CTAs at N = 7);
 //  * FP64: 2 only at N = 7 (111.2 -> 109.4 ms); at N = 2, 4, 5, 6, 8 the
 //    halved CTA was 2-7 % slower;
-//  * FP32: 2 at N = 4, 5 and 8, where the packed pair evaluation (PackPairs)
-//    needs more than the 64 registers a 512-thread CTA pair leaves; at N = 8
-//    one element's 81 lines would otherwise also need an 864-thread CTA.
+//  * FP32: 2 at N = 4, 5, 6 and 8, where the packed pair evaluation
+//    (PackPairs) needs more than the 64 registers a 512-thread CTA pair
+//    leaves (N = 6: 4.34 -> 3.98 ms on the order sweep); at N = 8 one
+//    element's 81 lines would otherwise also need an 864-thread CTA.  At
+//    N = 7 one set is faster (3.19 against 3.28 ms).
 template <int N, typename C>
 struct Launch {
     using S = Shape<N>;
     static constexpr int VWARPS = (S::LINES + S::LPW - 1) / S::LPW;  // warps' worth of lines
     static constexpr bool FP64 = sizeof(C) == 8;
-    static constexpr int REPS = IsFF<C>::value ? 2 : FP64 ? (N == 7 ? 2 : 1) : ((N == 4 || N == 5 || N == 8) ? 2 : 1);
+    static constexpr int REPS =
+        IsFF<C>::value ? 2 : FP64 ? (N == 7 ? 2 : 1) : ((N == 4 || N == 5 || N == 6 || N == 8) ? 2 : 1);
     static constexpr int WARPS = (VWARPS + REPS - 1) / REPS;
     static constexpr int THREADS = WARPS * 32;
     static constexpr size_t SMEM = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
