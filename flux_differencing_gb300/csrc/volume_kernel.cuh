@@ -49,7 +49,7 @@
 //    (and FP32 always) evaluates both and selects per lane.  The per-node
 //    values are stored pre-scaled (u/2, 2b, phi/8) so that no factor of two
 //    is applied per pair.
-//  * FP32 at N = 4..8 evaluates two offsets per instruction in packed
+//  * FP32 at N = 3..8 evaluates two offsets per instruction in packed
 //    float2 registers (issue-bound kernel; PackPairs).
 //  * A second instantiation (RK) fuses a Runge-Kutta stage update into the
 //    final store, for the FP32 and float-float time step.
@@ -217,11 +217,11 @@ __device__ __forceinline__ NodeVals<p2> pack_vals(const NodeVals<float>& a, cons
 // N = 6 4.32 -> 4.23, N = 8 5.00 -> 4.47 (with two line sets per warp at N = 4,
 // 5, 8 for the registers); N = 7 3.210 -> 3.188 with the pre-scaled node
 // values (the channel: 0.2183 -> 0.2167 ms; with two line sets per warp it
-// was slower, 3.281); N = 3 ties and keeps one evaluation per instruction.
+// was slower, 3.281); N = 3 1.908 -> 1.817, and 1.727 with two line sets.
 template <typename C, int N>
 struct PackPairs {
     static constexpr bool value =
-        std::is_same<C, float>::value && (N == 4 || N == 5 || N == 6 || N == 7 || N == 8);
+        std::is_same<C, float>::value && N >= 3;
 };
 
 // The FP32 fused Runge-Kutta stage evaluates the surface term inside this
@@ -650,18 +650,20 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
 //  * float-float: always 2 (256-thread CTAs at N = 7);
 //  * FP64: 2 only at N = 7 (111.2 -> 109.4 ms); at N = 2, 4, 5, 6, 8 the
 //    halved CTA was 2-7 % slower;
-//  * FP32: 2 at N = 4, 5, 6 and 8, where the packed pair evaluation
+//  * FP32: 2 at N = 3, 4, 5, 6 and 8, where the packed pair evaluation
 //    (PackPairs) needs more than the 64 registers a 512-thread CTA pair
-//    leaves (N = 6: 4.34 -> 3.98 ms on the order sweep); at N = 8 one
-//    element's 81 lines would otherwise also need an 864-thread CTA.  At
-//    N = 7 one set is faster (3.19 against 3.28 ms).
+//    leaves (N = 6: 4.34 -> 3.98 ms on the order sweep, N = 3: 1.82 ->
+//    1.73); at N = 8 one element's 81 lines would otherwise also need an
+//    864-thread CTA.  At N = 7 one set is faster (3.19 against 3.28 ms).
+//  * FP64 rechecked with the current kernel: two sets at N = 4, 5, 6 gave
+//    61.8 -> 62.7, 75.5 -> 75.4 and 91.7 -> 94.4 ms, so only N = 7 uses them.
 template <int N, typename C>
 struct Launch {
     using S = Shape<N>;
     static constexpr int VWARPS = (S::LINES + S::LPW - 1) / S::LPW;  // warps' worth of lines
     static constexpr bool FP64 = sizeof(C) == 8;
     static constexpr int REPS =
-        IsFF<C>::value ? 2 : FP64 ? (N == 7 ? 2 : 1) : ((N == 4 || N == 5 || N == 6 || N == 8) ? 2 : 1);
+        IsFF<C>::value ? 2 : FP64 ? (N == 7 ? 2 : 1) : ((N >= 3 && N != 7) ? 2 : 1);
     static constexpr int WARPS = (VWARPS + REPS - 1) / REPS;
     static constexpr int THREADS = WARPS * 32;
     static constexpr size_t SMEM = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
