@@ -276,7 +276,7 @@ def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier, what="volu
     """Per-call times with CUDA events on the launching stream.
 
     what: "volume" (one launch), "surface" (three launches, accumulating into
-    out), "rhs" (volume then surface: four launches), "step" (one five-stage
+    out), "rhs" (esdg_rhs: four launches, one for FP32), "step" (one five-stage
     Runge-Kutta step: 5 to 25 launches, on a copy of q) or "stage" (one
     Runge-Kutta stage update)."""
     import torch
@@ -695,7 +695,7 @@ def run_ours(args):
                 "what": "perturbation variables about the hydrostatic background (esdg_set_reference)",
                 "volume_ms": pt["volume_ms"], "volume_GDOF/s": ws * c32.n / (pt["volume_ms"] * 1e-3) / 1e9,
                 "rhs_ms": pt["rhs_ms"], "overhead_vs_full_state": pt["volume_ms"] / r32["ms"] - 1.0}
-            line["gpu_launches"] += 5 * args.steps
+            line["gpu_launches"] += (1 + rhs_launches("fp32")) * args.steps  # volume and rhs timings
         line["gpu_launches"] += args.steps + ((E2E_WINDOWS + 1) * max(3, min(args.steps, 20)) if "e2e" in r32 else 0)
     if args.ff_workload:
         rf = results[args.ff_workload]
@@ -717,7 +717,7 @@ def run_ours(args):
         line["gpu_launches"] += args.steps + ((E2E_WINDOWS + 1) * max(3, min(args.steps, 20)) if "e2e" in rf else 0)
     if "surface" in main:
         line["surface"] = _surface_report(cfg, main["surface"], ws, peak64, "FP64 vector", peaks.get("hbm_gbs"))
-        line["gpu_launches"] += 7 * args.steps
+        line["gpu_launches"] += (3 + rhs_launches(cfg.precision)) * args.steps  # surface and rhs timings
     for key, wname in (("main", args.workload), ("fp32", args.fp32_workload), ("fp64ff", args.ff_workload)):
         if wname and "step" in results[wname]:
             rep = _step_report(results[wname]["cfg"], results[wname], ws, peaks.get("hbm_gbs"))
@@ -728,12 +728,12 @@ def run_ours(args):
         r32 = results[args.fp32_workload]
         line["fp32"]["surface"] = _surface_report(r32["cfg"], r32["surface"], ws, fp32_meas, "FP32 vector",
                                                   peaks.get("hbm_gbs"))
-        line["gpu_launches"] += 7 * args.steps
+        line["gpu_launches"] += (3 + rhs_launches("fp32")) * args.steps
     if args.ff_workload and "surface" in results[args.ff_workload]:
         rf = results[args.ff_workload]
         line["fp64ff"]["surface"] = _surface_report(rf["cfg"], rf["surface"], ws, peak64, "FP64 vector",
                                                     peaks.get("hbm_gbs"))
-        line["gpu_launches"] += 7 * args.steps
+        line["gpu_launches"] += (3 + rhs_launches("fp64ff")) * args.steps
     line["peaks_measured"] = {"fp64_tflops": fp64_meas, "fp32_tflops": fp32_meas}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(cfg, args.cpu_seconds)
@@ -784,9 +784,16 @@ def _surface_report(cfg, sres, ws, alu_peak_tflops, alu_peak_name, hbm_peak_gbs)
                                  "algorithmic_bytes_per_call": nbytes, "algorithmic_flops_per_call": flops,
                                  "traffic": traffic,
                                  "traffic_unit": "bytes per call (ncu dram read + write, three launches)"}},
-        "rhs": {"what": "volume + surface", "ms_per_step": sres["rhs_ms"], "launches_per_step": 4,
+        "rhs": {"what": "volume + surface (esdg_rhs)" + (": one launch, the volume kernel evaluating each "
+                                                         "element's faces" if cfg.precision == "fp32" else ""),
+                "ms_per_step": sres["rhs_ms"], "launches_per_step": rhs_launches(cfg.precision),
                 "GDOF/s": ws * cfg.n / (sres["rhs_ms"] * 1e-3) / 1e9},
     }
+
+
+def rhs_launches(precision: str) -> int:
+    """Kernel launches of one esdg_rhs."""
+    return 1 if precision == "fp32" else 4
 
 
 def step_launches(precision: str) -> int:

@@ -170,6 +170,18 @@ esdg::SurfaceConsts<T> surface_consts(const esdg_ctx* h) {
     return k;
 }
 
+// The surface fields of the FP32 volume kernel's face modes (the fused stage
+// and volume + surface to out).
+static void set_face_fields(const esdg_ctx* h, esdg::VolumeArgs<float>& a) {
+    a.Kx = h->Kx;
+    a.Ky = h->Ky;
+    a.Kz = h->Kz;
+    for (int r = 0; r < 3; ++r) a.bc[r] = h->bc[r];
+    a.dissipation = h->dissipation;
+    a.inv_w0 = (float)(1.0L / (long double)h->weights[0]);
+    a.sk = surface_consts<float>(h);
+}
+
 template <typename T>
 esdg::SurfaceArgs<T> surface_args(const esdg_ctx* h, const void* q, const void* Ja, const void* phi, void* out,
                                   int form) {
@@ -487,6 +499,24 @@ int esdg_surface_rhs(esdg_handle h, const void* q, const void* metrics, const vo
 // skew forms, which skips that pair of terms (same result up to rounding).
 int esdg_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream) {
     if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
+    if (h->precision == ESDG_FP32) {
+        // one launch: the volume kernel evaluates each element's faces itself
+        // (one-sided, as in the fused stage) and writes volume + surface
+        if (!q || !metrics || !phi || !out) return fail(h, ESDG_ERR_ARG, "null device pointer");
+        if (!aligned16(q) || !aligned16(metrics) || !aligned16(phi) || !aligned16(out))
+            return fail(h, ESDG_ERR_ALIGN, "device pointers must be 16-byte aligned");
+        const size_t nb = sizeof(float) * (size_t)h->n;
+        if (overlaps(out, 5 * nb, q, 5 * nb) || overlaps(out, 5 * nb, metrics, 9 * nb) ||
+            overlaps(out, 5 * nb, phi, nb))
+            return fail(h, ESDG_ERR_ARG, "out overlaps an input");
+        if (int rc = check_device(h)) return rc;
+        auto a = volume_args<float>(h, q, metrics, phi, out, 0, h->K, h->op32, ESDG_FORM_SKEW);
+        a.with_faces = 1;
+        set_face_fields(h, a);
+        const cudaError_t e = dispatch_fp32(h->N, a, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(h, e, "volume kernel launch (volume + faces)");
+        return ESDG_OK;
+    }
     if (int rc = volume_range(h, 0, (long)h->K, q, metrics, phi, out, stream, ESDG_FORM_SKEW)) return rc;
     return surface_form(h, q, metrics, phi, out, stream, ESDG_FORM_SKEW);
 }
@@ -568,13 +598,7 @@ static int fused_stage(esdg_handle h, void* q, void* q_out, void* dq, void* S, c
         a.rk_B = (float)B;
         a.rk_dt = (float)dt;
         a.rk_f = (float)h->coriolis;
-        a.Kx = h->Kx;
-        a.Ky = h->Ky;
-        a.Kz = h->Kz;
-        for (int r = 0; r < 3; ++r) a.bc[r] = h->bc[r];
-        a.dissipation = h->dissipation;
-        a.inv_w0 = (float)(1.0L / (long double)h->weights[0]);
-        a.sk = surface_consts<float>(h);
+        set_face_fields(h, a);
         e = dispatch_fp32(h->N, a, s);
     } else {
         if (int rc = surface_form(h, q, metrics, phi, S, stream, ESDG_FORM_SKEW)) return rc;

@@ -64,7 +64,10 @@ struct VolumeArgs {
     T* rk_S;
     const T* rk_J;
     T rk_A, rk_B, rk_dt, rk_f;
-    // surface fields of the FP32 fused stage
+    // FP32, rk_q == nullptr: also evaluate the surface term (skew form, with
+    // the surface fields below) in the kernel and write volume + surface to out
+    int with_faces;
+    // surface fields of the FP32 fused stage and of with_faces
     long long Kx, Ky, Kz;  // element e = ex + Kx (ey + Ky ez)
     int bc[3];             // per direction: 0 periodic, 1 slip wall
     int dissipation;       // 0: entropy-conserving interface flux only

@@ -300,19 +300,29 @@ __device__ __forceinline__ bool face_neighbour(const long long* nbr, int el, int
 
 // Dynamic shared memory of the volume kernel in bytes: the fields, and for
 // the FP32 fused stage the face buffer and the neighbour table behind them.
-template <typename C, int N, bool RK>
+// Kernel modes: 0 writes the volume term to out; 1 is the fused Runge-Kutta
+// stage (FP32 and float-float); 2 writes volume + surface to out, the faces
+// evaluated in the kernel (FP32).  Modes 1 and 2 in FP32 carry the face
+// machinery (FaceMode).
+template <typename C, int MODE>
+struct FaceMode {
+    static constexpr bool value = MODE != 0 && FusedSurface<C>::value;
+};
+
+template <typename C, int N, int MODE>
 constexpr size_t volume_smem_fields() {
     return sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE +
-           ((RK && FusedSurface<C>::value) ? sizeof(C) * (size_t)FaceSlots<N>::FIELDS * FaceSlots<N>::COUNT : 0);
+           (FaceMode<C, MODE>::value ? sizeof(C) * (size_t)FaceSlots<N>::FIELDS * FaceSlots<N>::COUNT : 0);
 }
-template <typename C, int N, bool RK>
+template <typename C, int N, int MODE>
 constexpr size_t volume_smem_nbr_offset() {
-    return (volume_smem_fields<C, N, RK>() + 7) & ~(size_t)7;
+    return (volume_smem_fields<C, N, MODE>() + 7) & ~(size_t)7;
 }
-template <typename C, int N, bool RK>
+template <typename C, int N, int MODE>
 constexpr size_t volume_smem_bytes() {
-    return (RK && FusedSurface<C>::value) ? volume_smem_nbr_offset<C, N, RK>() + 6 * sizeof(long long) * Shape<N>::EPB
-                                          : volume_smem_fields<C, N, RK>();
+    return FaceMode<C, MODE>::value
+               ? volume_smem_nbr_offset<C, N, MODE>() + 6 * sizeof(long long) * Shape<N>::EPB
+               : volume_smem_fields<C, N, MODE>();
 }
 
 // One pair (i, m) of a line, evaluated once for both nodes.  cq = Q_{pp'}
@@ -434,15 +444,44 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
     t4 = fE;  // subtracted by the receiver
 }
 
-// The final write of one node's volume term t0..t4: to out, or, in a fused
-// Runge-Kutta stage, plus the surface term at face nodes, as a stage update of
-// dq and q (the node's own element only, so updating q in place is safe).
-template <typename T, int N, bool RK>
+// The face contributions of node (na, nb, nc) of local element el from the
+// face phase, added to sv in the fixed order xi, eta, zeta.
+template <typename T, int N>
+__device__ __forceinline__ void face_sum(const T* __restrict__ fb, int el, int na, int nb, int nc, T (&sv)[5]) {
+    using FSL = FaceSlots<N>;
+    auto add_slot = [&](int sl) {
+#pragma unroll
+        for (int v = 0; v < 5; ++v) sv[v] += fb[v * FSL::COUNT + sl];
+    };
+    if (na == 0) add_slot(FSL::slot(el, 0, 0, nb, nc));
+    else if (na == N) add_slot(FSL::slot(el, 0, 1, nb, nc));
+    if (nb == 0) add_slot(FSL::slot(el, 1, 0, na, nc));
+    else if (nb == N) add_slot(FSL::slot(el, 1, 1, na, nc));
+    if (nc == 0) add_slot(FSL::slot(el, 2, 0, na, nb));
+    else if (nc == N) add_slot(FSL::slot(el, 2, 1, na, nb));
+}
+
+// The final write of one node's volume term t0..t4.  MODE 0: to out.  MODE
+// 2 (FP32): volume + the node's face contributions to out.  MODE 1: a fused
+// Runge-Kutta stage, plus the surface term at face nodes, as a stage update
+// of dq and q (the node's own element only, so updating q in place is safe
+// where the surface term comes precomputed).
+template <typename T, int N, int MODE>
 __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, int na, int nb, int nc, int el,
                                            const T* __restrict__ fb, T t0, T t1, T t2, T t3, T t4) {
     const long long n = a.n;
-    if constexpr (!RK) {
+    constexpr bool FUSED = FaceMode<T, MODE>::value;
+    if constexpr (MODE != 1) {
         T* __restrict__ o = a.out;
+        if constexpr (FUSED) {
+            T sv[5] = {T(0), T(0), T(0), T(0), T(0)};
+            face_sum<T, N>(fb, el, na, nb, nc, sv);
+            t0 += sv[0];
+            t1 += sv[1];
+            t2 += sv[2];
+            t3 += sv[3];
+            t4 += sv[4];
+        }
         o[0 * n + g] = t0;
         o[1 * n + g] = t1;
         o[2 * n + g] = t2;
@@ -453,7 +492,6 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
     // every load first, through restrict-qualified pointers: loads interleaved
     // with stores through possibly aliasing pointers would each wait for DRAM
     // in turn (measured 1.0 ms against 0.22 ms for the plain FP32 kernel)
-    constexpr bool FUSED = FusedSurface<T>::value;
     const T* __restrict__ qp = a.rk_q;
     T* __restrict__ qo = FUSED ? a.rk_qout : a.rk_q;
     T* __restrict__ dqp = a.rk_dq;
@@ -467,21 +505,7 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
         dqv[v] = use_dq ? dqp[v * n + g] : T(0);
         sv[v] = (!FUSED && face) ? Sp[v * n + g] : T(0);
     }
-    if constexpr (FUSED) {
-        // this node's face contributions from the face phase, in the fixed
-        // order xi, eta, zeta
-        using FSL = FaceSlots<N>;
-        auto add_slot = [&](int sl) {
-#pragma unroll
-            for (int v = 0; v < 5; ++v) sv[v] += fb[v * FSL::COUNT + sl];
-        };
-        if (na == 0) add_slot(FSL::slot(el, 0, 0, nb, nc));
-        else if (na == N) add_slot(FSL::slot(el, 0, 1, nb, nc));
-        if (nb == 0) add_slot(FSL::slot(el, 1, 0, na, nc));
-        else if (nb == N) add_slot(FSL::slot(el, 1, 1, na, nc));
-        if (nc == 0) add_slot(FSL::slot(el, 2, 0, na, nb));
-        else if (nc == N) add_slot(FSL::slot(el, 2, 1, na, nb));
-    }
+    if constexpr (FUSED) face_sum<T, N>(fb, el, na, nb, nc, sv);
     const T Jg = a.rk_J[g];
     const T sc = -a.rk_dt * Num<T>::rcp(Jg);
     const T tot[5] = {t0, t1, t2, t3, t4};
@@ -633,7 +657,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         // linear node L*Nq + p is contiguous across lanes: coalesced stores
         static_assert(Layout<N>::ORD0 == 0, "xi lines must be dealt b-fastest");
         const long long g = node0 + (long long)L * NQ + p;
-        store_node<T, N, FINAL == 2>(a, g, ia, ib, ic, el, reinterpret_cast<const T*>(sm + F_COUNT * FS),
+        store_node<T, N, FINAL - 1>(a, g, ia, ib, ic, el, reinterpret_cast<const T*>(sm + F_COUNT * FS),
                                      Conv<T, C>::out(fma(acc0, iw, s_acc[0 * FS + i])),
                          Conv<T, C>::out(fma(acc1, iw, s_acc[1 * FS + i])),
                          Conv<T, C>::out(fma(acc2, iw, s_acc[2 * FS + i])),
@@ -799,7 +823,7 @@ __device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict
 
 // RK: fused Runge-Kutta stage (store_node); a separate instantiation so that
 // the plain kernel's code and registers are those of a store to out.
-template <typename T, int N, typename C, bool RK>
+template <typename T, int N, typename C, int MODE>
 __global__ void __launch_bounds__(Launch<N, C>::THREADS, Launch<N, C>::MIN_BLOCKS)
 volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     using S = Shape<N>;
@@ -819,8 +843,8 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     // FP32 fused stage: the element across each face of the CTA's elements
     // (-1 at a slip wall), one entry per thread
     long long* nbr = nullptr;
-    if constexpr (RK && FusedSurface<C>::value) {
-        nbr = reinterpret_cast<long long*>(smem_raw + volume_smem_nbr_offset<C, N, RK>());
+    if constexpr (FaceMode<C, MODE>::value) {
+        nbr = reinterpret_cast<long long*>(smem_raw + volume_smem_nbr_offset<C, N, MODE>());
         static_assert(6 * S::EPB <= Launch<N, C>::THREADS, "one neighbour entry per thread");
         const int t = threadIdx.x;
         if (t < 6 * e_count) nbr[t] = neighbour_element(a, e0 + t / 6, (t % 6) >> 1, t & 1);
@@ -838,7 +862,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     // is requested before the element's own planes, so that the latencies of
     // the two sets of loads overlap; it is written to the face buffer after
     // the node loop
-    constexpr bool FUSED = RK && FusedSurface<C>::value;
+    constexpr bool FUSED = FaceMode<C, MODE>::value;
     constexpr int TR = 11;  // trace values: q (5), metric row (3), phi, rho_ref, p_ref
     C trace[FUSED ? TR : 1];
     bool trace_ok = false;
@@ -950,7 +974,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         sm[(F_ACC0 + 3) * FS + sl] = f3;
         sm[(F_ACC0 + 4) * FS + sl] = f4;
     }
-    if constexpr (RK && FusedSurface<C>::value) {
+    if constexpr (FaceMode<C, MODE>::value) {
         // neighbour traces of this CTA's face slots (walls: none): the
         // prefetched first slot, then any further slots of this thread
         using FSL = FaceSlots<N>;
@@ -1022,12 +1046,12 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
             const int sl = SL::at(el, na, nb, nc);
             const long long g = node0 + t;
-            store_node<T, N, RK>(a, g, na, nb, nc, el, nullptr, CV::out(s_acc[0 * FS + sl]),
+            store_node<T, N, MODE>(a, g, na, nb, nc, el, nullptr, CV::out(s_acc[0 * FS + sl]),
                                  CV::out(s_acc[1 * FS + sl]),
                              CV::out(s_acc[2 * FS + sl]), CV::out(s_acc[3 * FS + sl]), CV::out(s_acc[4 * FS + sl]));
         }
     } else {
-        if constexpr (RK && FusedSurface<C>::value) face_phase<T, C, N>(a, sm, nbr, e_count);
+        if constexpr (FaceMode<C, MODE>::value) face_phase<T, C, N>(a, sm, nbr, e_count);
         direction_phase<T, C, N, 1, 0>(a, sm, e_count, node0, cq, iw, c_g);
         __syncthreads();
         direction_phase<T, C, N, 2, 0>(a, sm, e_count, node0, cq, iw, c_g);
@@ -1040,35 +1064,41 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             antipodal_phase<T, C, N>(a, sm, e_count, c_g, 0);
             __syncthreads();
         }
-        direction_phase<T, C, N, 0, RK ? 2 : 1>(a, sm, e_count, node0, cq, iw, c_g);
+        direction_phase<T, C, N, 0, MODE + 1>(a, sm, e_count, node0, cq, iw, c_g);
     }
 }
 
-template <typename T, int N, typename C, bool RK>
+template <typename T, int N, typename C, int MODE>
 cudaError_t launch_volume_mode(const VolumeArgs<T>& a, cudaStream_t s) {
     using S = Shape<N>;
     const long long K = a.e_end - a.e_begin;
     if (K <= 0) return cudaSuccess;
-    const size_t smem = volume_smem_bytes<C, N, RK>();
+    const size_t smem = volume_smem_bytes<C, N, MODE>();
     static bool attr_done = false;  // per instantiation; set once per process
     if (!attr_done) {
-        cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N, C, RK>,
+        cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N, C, MODE>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         attr_done = true;
     }
     const long long blocks = (K + S::EPB - 1) / S::EPB;
-    volume_kernel<T, N, C, RK><<<(unsigned)blocks, Launch<N, C>::THREADS, smem, s>>>(a);
+    volume_kernel<T, N, C, MODE><<<(unsigned)blocks, Launch<N, C>::THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 
 // The fused Runge-Kutta mode is built for FP32 and float-float only (native
-// FP64 keeps the separate stage kernel).
+// FP64 keeps the separate stage kernel); volume + faces to out for FP32 only.
 template <typename T, int N, typename C = T>
 cudaError_t launch_volume(const VolumeArgs<T>& a, cudaStream_t s) {
-    if (a.rk_q == nullptr) return launch_volume_mode<T, N, C, false>(a, s);
-    if constexpr (std::is_same<C, double>::value) return cudaErrorNotSupported;
-    else return launch_volume_mode<T, N, C, true>(a, s);
+    if (a.rk_q != nullptr) {
+        if constexpr (std::is_same<C, double>::value) return cudaErrorNotSupported;
+        else return launch_volume_mode<T, N, C, 1>(a, s);
+    }
+    if (a.with_faces) {
+        if constexpr (FusedSurface<C>::value) return launch_volume_mode<T, N, C, 2>(a, s);
+        else return cudaErrorNotSupported;
+    }
+    return launch_volume_mode<T, N, C, 0>(a, s);
 }
 
 }  // namespace esdg

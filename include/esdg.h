@@ -298,7 +298,10 @@ int esdg_pipeline_destroy(esdg_pipeline p);
  * diagonal f(q_i).Ja^r(i) at face nodes and the surface term's -f(q_i).n_own
  * cancel exactly, so both kernels run in their skew forms: the same result as
  * esdg_volume_rhs followed by esdg_surface_rhs up to rounding, with less
- * work.  Arguments as esdg_volume_rhs (out written).  Four launches on
+ * work.  Arguments as esdg_volume_rhs (out written).  ESDG_FP32: one launch,
+ * the volume kernel evaluating each element's faces from its own side (each
+ * interface once per side); ESDG_FP64 and ESDG_FP64_FF: the volume kernel and
+ * the three face-centric surface launches (four launches).  Everything on
  * `stream`.  Errors: as esdg_volume_rhs. */
 int esdg_rhs(esdg_handle h, const void* q, const void* metrics, const void* phi, void* out, void* stream);
 
