@@ -680,7 +680,10 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
 //    1.73); at N = 8 one element's 81 lines would otherwise also need an
 //    864-thread CTA.  At N = 7 one set is faster (3.19 against 3.28 ms).
 //  * FP64 rechecked with the current kernel: two sets at N = 4, 5, 6 gave
-//    61.8 -> 62.7, 75.5 -> 75.4 and 91.7 -> 94.4 ms, so only N = 7 uses them.
+//    61.8 -> 62.7, 75.5 -> 75.4 and 91.7 -> 94.4 ms, so only N = 7 uses them;
+//    but two CTAs of one set per SM (MIN_BLOCKS = 2: 72, 64 and 72 registers
+//    with 24-128 byte spills) are faster there: 61.8 -> 60.0, 75.5 -> 74.0,
+//    91.7 -> 90.2 ms.
 template <int N, typename C>
 struct Launch {
     using S = Shape<N>;
@@ -693,7 +696,10 @@ struct Launch {
     static constexpr size_t SMEM = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
     static constexpr bool TWO_FIT = 2 * SMEM <= 227 * 1024;
     static constexpr int MIN_BLOCKS =
-        ((sizeof(C) == 4 && THREADS <= 512) || IsFF<C>::value || (FP64 && REPS == 2)) && TWO_FIT ? 2 : 1;
+        ((sizeof(C) == 4 && THREADS <= 512) || IsFF<C>::value || (FP64 && (REPS == 2 || (N >= 4 && N <= 6)))) &&
+                TWO_FIT
+            ? 2
+            : 1;
 };
 
 template <typename T, typename C, int N, int R, int FINAL>
