@@ -683,7 +683,8 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
 //    61.8 -> 62.7, 75.5 -> 75.4 and 91.7 -> 94.4 ms, so only N = 7 uses them;
 //    but two CTAs of one set per SM (MIN_BLOCKS = 2: 72, 64 and 72 registers
 //    with 24-128 byte spills) are faster there: 61.8 -> 60.0, 75.5 -> 74.0,
-//    91.7 -> 90.2 ms.
+//    91.7 -> 90.2 ms.  Four CTAs per SM at N = 2, 3 (56 and 64 registers)
+//    were no faster (34.8 -> 35.3, 44.3 -> 44.3 ms).
 template <int N, typename C>
 struct Launch {
     using S = Shape<N>;
