@@ -51,8 +51,12 @@
 //    is applied per pair.
 //  * FP32 at N = 3..8 evaluates two offsets per instruction in packed
 //    float2 registers (issue-bound kernel; PackPairs).
-//  * A second instantiation (RK) fuses a Runge-Kutta stage update into the
-//    final store, for the FP32 and float-float time step.
+//  * Further instantiations (MODE) change the final store: a Runge-Kutta
+//    stage update fused into it (FP32 and float-float time steps), and in
+//    FP32 the element's own faces evaluated in the kernel (neighbour traces
+//    gathered while the element loads), so that a whole stage, or the full
+//    right-hand side, is one launch.
+//  * FP64 per-node logarithms by a table-driven reduction (log_fp64.cuh).
 //  * FP64 on GB300 has 1/64 of the FP32 rate, so the FP64 kernel is bound by
 //    its FP64 instruction count: reciprocals are a hardware estimate refined
 //    by one third-order Newton-Raphson step rather than a correctly rounded
@@ -527,9 +531,9 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
 }
 
 // One direction phase.  R = 0 (xi), 1 (eta), 2 (zeta).  FINAL = 0: add the
-// scaled sum to the shared accumulators; 1: add the shared accumulators and
-// store the node's result to global memory; 2: the same, as a fused
-// Runge-Kutta stage update (store_node).  Offsets
+// scaled sum to the shared accumulators; 1, 2, 3: add the shared
+// accumulators and store the node's result with store_node in MODE FINAL - 1
+// (to out; as a fused Runge-Kutta stage update; with the faces, to out).  Offsets
 // d = 1..NEAR; the antipodal offset Nq/2 of even Nq is left to
 // antipodal_phase.
 template <typename T, typename C, int N, int FINAL>
@@ -828,8 +832,9 @@ __device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict
     }
 }
 
-// RK: fused Runge-Kutta stage (store_node); a separate instantiation so that
-// the plain kernel's code and registers are those of a store to out.
+// MODE (store_node): 0 volume to out, 1 fused Runge-Kutta stage, 2 (FP32)
+// volume + faces to out; separate instantiations, so that the plain kernel's
+// code and registers are those of a store to out.
 template <typename T, int N, typename C, int MODE>
 __global__ void __launch_bounds__(Launch<N, C>::THREADS, Launch<N, C>::MIN_BLOCKS)
 volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
