@@ -106,6 +106,32 @@ def test_rhs_is_volume_plus_surface(precision):
     assert e.max() < hz.TOL[precision], e
 
 
+@pytest.mark.parametrize("N", list(range(1, 9)))
+@pytest.mark.parametrize("bc", [(0, 1, 1), (1, 0, 1)])
+@pytest.mark.parametrize("dissipation", [True, False])
+def test_fp32_rhs_one_launch_parity(N, bc, dissipation):
+    """esdg_rhs in FP32 is one launch of the volume kernel with the faces
+    evaluated inside it (one-sided, as in the fused stage); against the
+    oracle's volume + surface at every order, with walls and periodic
+    directions and with the entropy-conserving interface flux alone.  K
+    gives several elements per CTA at low N and one element along a
+    periodic direction."""
+    cfg = wl.small_config(N, K=(3, 1, 2), warp=True, precision="fp32", bc=bc, state="noisy")
+    g = wl.generate(cfg)
+    op = fd.VolumeOperator(cfg.Kx, cfg.Ky, cfg.Kz, N, "fp32", "2d", bc=bc, dissipation=dissipation)
+    dg = hz.to_device(g)
+    Ja = op.set_geometry(dg["x"], dg["y"], dg["z"])
+    q = dg["q"].to(op.dtype).contiguous()
+    phi = dg["phi"].to(op.dtype).contiguous()
+    got = op.rhs(q, Ja, phi).double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert op.status() == 0
+    vref, vscale = hz.run_oracle(cfg, g)
+    sref, sscale = hz.run_oracle_surface(cfg, g, dissipation=dissipation)
+    e, _ = hz.errors(got, vref + sref, vscale + sscale)
+    assert e.max() < hz.TOL["fp32"], e
+
+
 def test_surface_is_deterministic():
     cfg = wl.small_config(7, K=(3, 3, 2), warp=True, bc=(0, 1, 1), state="noisy")
     g = wl.generate(cfg)
