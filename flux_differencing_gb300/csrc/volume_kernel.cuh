@@ -158,6 +158,54 @@ __device__ __forceinline__ void line_node(int R, int ell, int p, int& a, int& b,
     c = (R == 2) ? p : o2;
 }
 
+// Load-phase order of an element's nodes.  FP64 (FaceFirst) takes the face
+// nodes first -- the slabs c = 0 and c = N, then for each inner slab the
+// rows b = 0 and b = N and the ends a = 0, N of its other rows -- and the
+// (N-1)^3 interior nodes after them, so that whole warps of interior nodes
+// skip the 2D form's diagonal term (nonzero only at line ends), which a
+// warp otherwise evaluates as soon as one of its lanes holds a face node
+// (every warp does, in the natural order).  The same lines are read; only
+// the order of the nodes within the element changes.  Other precisions keep
+// the natural order (fully coalesced loads matter more there).
+template <typename C>
+struct FaceFirst {
+    static constexpr bool value = std::is_same<C, double>::value;
+};
+
+template <int N>
+__device__ __forceinline__ int face_first_node(int k) {
+    constexpr int NQ = N + 1;
+    constexpr int SLAB = NQ * NQ;
+    constexpr int NI = N - 1;                    // interior nodes per line
+    constexpr int RING = 4 * N;                  // face nodes of an inner slab
+    constexpr int FACE = 2 * SLAB + NI * RING;   // = NQ^3 - NI^3
+    int a, b, c;
+    if (k < 2 * SLAB) {
+        c = k < SLAB ? 0 : N;
+        const int r = k < SLAB ? k : k - SLAB;
+        a = r % NQ;
+        b = r / NQ;
+    } else if (k < FACE) {
+        const int u = k - 2 * SLAB;
+        c = 1 + u / RING;
+        const int r = u % RING;
+        if (r < 2 * NQ) {
+            a = r % NQ;
+            b = r < NQ ? 0 : N;
+        } else {
+            const int w = r - 2 * NQ;
+            a = (w & 1) ? N : 0;
+            b = 1 + (w >> 1);
+        }
+    } else {
+        const int i = k - FACE;
+        a = 1 + i % NI;
+        b = 1 + (i / NI) % NI;
+        c = 1 + i / (NI * NI);
+    }
+    return a + NQ * (b + NQ * c);
+}
+
 // Whether the antipodal pairs of even Nq get their own pass (evaluated once,
 // both shares written to shared memory) or stay in the direction phases
 // (evaluated by both nodes, own share kept).  The pass halves those
@@ -900,7 +948,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     }
     for (int t = threadIdx.x; t < S::NODES; t += Launch<N, C>::THREADS) {
         const int el = t / NP3;
-        const int nd = t - el * NP3;
+        const int nd = FaceFirst<C>::value ? face_first_node<N>(t - el * NP3) : t - el * NP3;
         const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
         const int sl = SL::at(el, na, nb, nc);
         T rho_t = T(1), m1_t = T(0), m2_t = T(0), m3_t = T(0), E_t = T(1), phi_t = T(0);
@@ -911,7 +959,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         const bool perturbed = a.rho_ref != nullptr;
         T rr_t = T(0), pr_t = T(0);
         if (real) {
-            const long long g = node0 + t;
+            const long long g = FaceFirst<C>::value ? node0 + (long long)el * NP3 + nd : node0 + t;
             const long long n = a.n;
             rho_t = __ldg(a.q + g);
             m1_t = __ldg(a.q + n + g);
@@ -966,7 +1014,11 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         // diagonal pairs of the 2D form: sum_r 2 D_{a_r a_r} Ja^r(i) . f(q_i), nonzero
         // only where a_r is 0 or N; f is the physical flux of Eq. 1
         P f0 = P(0.0), f1 = P(0.0), f2 = P(0.0), f3 = P(0.0), f4 = P(0.0);
-        if (a.form == 0) {
+        bool with_diag = a.form == 0;
+        if constexpr (FaceFirst<C>::value)  // whole warps of interior nodes skip it
+            with_diag = with_diag && __any_sync(__activemask(), na == 0 || na == N || nb == 0 || nb == N ||
+                                                                    nc == 0 || nc == N);
+        if (with_diag) {
             const P dA = PV::in((na == 0 || na == N) ? a.ops.Q2[na * NQ + na] * a.ops.invw[na] : T(0));
             const P dB = PV::in((nb == 0 || nb == N) ? a.ops.Q2[nb * NQ + nb] * a.ops.invw[nb] : T(0));
             const P dC = PV::in((nc == 0 || nc == N) ? a.ops.Q2[nc * NQ + nc] * a.ops.invw[nc] : T(0));
