@@ -197,11 +197,13 @@ __device__ __forceinline__ int face_first_node(int k) {
             a = (w & 1) ? N : 0;
             b = 1 + (w >> 1);
         }
-    } else {
+    } else if constexpr (NI > 0) {
         const int i = k - FACE;
         a = 1 + i % NI;
         b = 1 + (i / NI) % NI;
         c = 1 + i / (NI * NI);
+    } else {
+        a = b = c = 0;  // N = 1 has no interior node: not reached
     }
     return a + NQ * (b + NQ * c);
 }
