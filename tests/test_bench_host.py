@@ -1,0 +1,67 @@
+"""Host-side logic of bench.py (no GPU): face-node counts of the surface
+roofline, the guard that drops a committed ncu traffic record once the kernel
+source changes, and the operation-count formula."""
+import itertools
+from types import SimpleNamespace
+
+import pytest
+
+import bench
+
+
+def _brute_surface_counts(N, Kx, Ky, Kz, bc):
+    """Interior interface nodes (each interface once) and wall face nodes, by
+    walking all six faces of every element: a face on a wall boundary is a
+    wall face, every other face is one of the two sides of an interface (a
+    single element along a periodic direction meets itself)."""
+    Nq2 = (N + 1) ** 2
+    Kd = (Kx, Ky, Kz)
+    walls = sides = 0
+    for idx in itertools.product(range(Kx), range(Ky), range(Kz)):
+        for r in range(3):
+            for step in (-1, 1):
+                if bc[r] and not 0 <= idx[r] + step < Kd[r]:
+                    walls += 1
+                else:
+                    sides += 1
+    assert sides % 2 == 0
+    return sides // 2 * Nq2, walls * Nq2
+
+
+@pytest.mark.parametrize("N", [1, 3, 7])
+@pytest.mark.parametrize("K", [(3, 2, 2), (1, 4, 2), (2, 1, 1), (4, 3, 5)])
+@pytest.mark.parametrize("bc", [(0, 0, 0), (1, 1, 1), (0, 1, 1), (1, 0, 1)])
+def test_surface_counts_match_brute_force(N, K, bc):
+    cfg = SimpleNamespace(N=N, Kx=K[0], Ky=K[1], Kz=K[2], K=K[0] * K[1] * K[2], bc=bc)
+    assert bench.surface_counts(cfg) == _brute_surface_counts(N, *K, bc)
+
+
+def test_channel_face_counts():
+    # the N = 7 channel: periodic in x, walls in y and z
+    cfg = SimpleNamespace(N=7, Kx=64, Ky=16, Kz=8, K=8192, bc=(0, 1, 1))
+    assert bench.surface_counts(cfg) == (1474560, 196608)
+
+
+def test_traffic_record_only_for_the_committed_source(monkeypatch):
+    rec = bench.recorded_traffic("volume_kernel<double, 7>", "channel_N7")
+    assert isinstance(rec, int) and rec > 0
+    # the algorithmic bytes are 15 planes in and 5 out of 4,194,304 doubles; ncu
+    # sees a little less written (part of the output still in L2)
+    assert 0.9 * 20 * 8 * 4194304 < rec < 1.05 * 20 * 8 * 4194304
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda kind="volume": "0" * 16)
+    assert bench.recorded_traffic("volume_kernel<double, 7>", "channel_N7") is None
+
+
+def test_operation_counts():
+    # each unordered pair once per direction: 3 (Nq - 1)/2 pairs per node
+    for N in range(1, 9):
+        Nq = N + 1
+        expect = bench.PAIR_OPS * 3 * (Nq - 1) / 2 + bench.NODE_OPS + bench.DIAG_OPS * 6 / Nq
+        assert bench.flops_per_dof(N) == pytest.approx(expect)
+        assert bench.flops_per_dof(N, form2d=False) == pytest.approx(expect - bench.DIAG_OPS * 6 / Nq)
+    assert bench.flops_per_dof(7) == pytest.approx(935.0)
+
+
+def test_launch_counts():
+    assert [bench.step_launches(p) for p in ("fp64", "fp64ff", "fp32")] == [25, 20, 5]
+    assert [bench.rhs_launches(p) for p in ("fp64", "fp64ff", "fp32")] == [4, 4, 1]
