@@ -132,6 +132,28 @@ def test_fp32_rhs_one_launch_parity(N, bc, dissipation):
     assert e.max() < hz.TOL["fp32"], e
 
 
+@pytest.mark.parametrize("K", [(1, 1, 1), (1, 3, 1), (2, 1, 1)])
+@pytest.mark.parametrize("bc", [(0, 0, 0), (1, 1, 1), (0, 1, 0)])
+def test_fp32_rhs_one_launch_degenerate_meshes(K, bc):
+    """The one-launch FP32 right-hand side on meshes of one or two elements
+    per direction: periodic faces whose neighbour is the element itself, and
+    walls on every side; against the oracle."""
+    cfg = wl.small_config(3, K=K, warp=True, precision="fp32", bc=bc, state="noisy")
+    g = wl.generate(cfg)
+    op = fd.VolumeOperator(cfg.Kx, cfg.Ky, cfg.Kz, 3, "fp32", "2d", bc=bc)
+    dg = hz.to_device(g)
+    Ja = op.set_geometry(dg["x"], dg["y"], dg["z"])
+    q = dg["q"].to(op.dtype).contiguous()
+    phi = dg["phi"].to(op.dtype).contiguous()
+    got = op.rhs(q, Ja, phi).double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert op.status() == 0
+    vref, vscale = hz.run_oracle(cfg, g)
+    sref, sscale = hz.run_oracle_surface(cfg, g)
+    e, _ = hz.errors(got, vref + sref, vscale + sscale)
+    assert e.max() < hz.TOL["fp32"], e
+
+
 def test_surface_is_deterministic():
     cfg = wl.small_config(7, K=(3, 3, 2), warp=True, bc=(0, 1, 1), state="noisy")
     g = wl.generate(cfg)
