@@ -10,6 +10,7 @@
 // lives in the file-scope array below, which the CUDA runtime places in
 // device memory when the library is loaded on a device and keeps there until
 // the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -28,25 +29,76 @@ static __device__ __align__(256) unsigned g_noalloc_scratch[kScratchWords];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-unsigned* g_scratch_addr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
+// Device address of g_noalloc_scratch per device, with the identifier of the
+// context it was looked up in.  A context that is destroyed and created
+// again (cudaDeviceReset, or a driver-API caller replacing its context)
+// reloads the module, and the array can then sit at another address: the
+// identifier shows that, and the address is looked up again.
+struct ScratchAddr {
+    unsigned long long ctx_id;
+    unsigned* addr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
 int noalloc_fail(int code, const std::string& msg) {
     esdg::set_unhandled_error(msg);  // reported by esdg_last_error(NULL)
     return code;
 }
 
+// The current context's process-unique identifier, through the driver's
+// cuCtxGetCurrent and cuCtxGetId (resolved once through the runtime, so the
+// library does not link the driver library itself).  False when either is
+// unavailable or no context is current yet.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+std::once_flag g_resolve_once;
+
+bool current_context_id(unsigned long long* id) {
+    std::call_once(g_resolve_once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &r) == cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &r) == cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    if (!g_ctx_current || !g_ctx_id) return false;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
 // Host code must not pass &g_noalloc_scratch to a kernel: on the host that
-// name is only a stand-in.  The real device address is looked up once per
-// device, with that device current.
+// name is only a stand-in.  The real device address is looked up with the
+// device current: on the first call on a device (which also loads the module
+// there, so that first call should come before any stream capture), and again
+// whenever the device's context has changed since.
 cudaError_t scratch_address(int dev, unsigned** out) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = static_cast<unsigned*>(p);
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    if (have_id && g_scratch[dev].addr && g_scratch[dev].ctx_id == id) {
+        *out = g_scratch[dev].addr;
+        return cudaSuccess;
     }
-    *out = g_scratch_addr[dev];
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    // the lookup above makes the primary context current if none was: take
+    // its identifier now; without one the address is looked up every call
+    unsigned long long id_after = 0;
+    if (current_context_id(&id_after)) {
+        g_scratch[dev].ctx_id = id_after;
+        g_scratch[dev].addr = static_cast<unsigned*>(p);
+    } else {
+        g_scratch[dev].addr = nullptr;
+    }
+    *out = static_cast<unsigned*>(p);
     return cudaSuccess;
 }
 

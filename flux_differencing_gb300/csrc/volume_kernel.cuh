@@ -1140,13 +1140,13 @@ cudaError_t launch_volume_mode(const VolumeArgs<T>& a, cudaStream_t s) {
     const long long K = a.e_end - a.e_begin;
     if (K <= 0) return cudaSuccess;
     const size_t smem = volume_smem_bytes<C, N, MODE>();
-    static bool attr_done = false;  // per instantiation; set once per process
-    if (!attr_done) {
-        cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N, C, MODE>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        attr_done = true;
-    }
+    // The dynamic shared-memory limit is an attribute of the function on the
+    // current device (and is lost when that device's context is reset), so it
+    // is set on every launch: a host-side call, no stream work, and no shared
+    // host state between threads or devices.
+    cudaError_t err = cudaFuncSetAttribute(volume_kernel<T, N, C, MODE>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
     const long long blocks = (K + S::EPB - 1) / S::EPB;
     volume_kernel<T, N, C, MODE><<<(unsigned)blocks, Launch<N, C>::THREADS, smem, s>>>(a);
     return cudaGetLastError();

@@ -358,8 +358,11 @@ int esdg_version(void);
  *   stream     cudaStream_t cast to void*.
  *
  * The first call on a device looks up the device address of the scratch
- * array with cudaGetSymbolAddress (once per device, with that device
- * current); make that first call before any stream capture.  Every call on a
+ * array with cudaGetSymbolAddress (with that device current) and keeps it
+ * for that device's context; make that first call before any stream
+ * capture.  If the context is destroyed and created again (cudaDeviceReset),
+ * the next call sees a new context identifier and looks the address up
+ * again.  Every call on a
  * device shares the one status word: the call clears it on `stream` before
  * its kernel, so calls whose work overlaps on the GPU (different streams)
  * race on it and may see each other's bits.

@@ -2,6 +2,7 @@
 roofline, the guard that drops a committed ncu traffic record once the kernel
 source changes, and the operation-count formula."""
 import itertools
+import os
 from types import SimpleNamespace
 
 import pytest
@@ -43,11 +44,23 @@ def test_channel_face_counts():
 
 
 def test_traffic_record_only_for_the_committed_source(monkeypatch):
-    rec = bench.recorded_traffic("volume_kernel<double, 7>", "channel_N7")
-    assert isinstance(rec, int) and rec > 0
+    """A committed ncu record is used only while the kernel source hash equals
+    the one it was captured with (the guard itself, independent of whether the
+    working tree's kernel has been re-profiled yet)."""
+    import glob
+    import json
+    recs = []
+    for path in glob.glob(os.path.join(bench.ROOT, "profiles", "*.md")):
+        with open(path) as f:
+            recs += [json.loads(line.split(":", 1)[1]) for line in f if line.startswith("traffic_record:")]
+    rec = [r for r in recs if r["kernel"] == "volume_kernel<double, 7>" and r["workload"] == "channel_N7"]
+    assert rec, "no committed traffic record for the FP64 N = 7 channel kernel"
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda kind="volume": rec[0]["source_sha"])
+    got = bench.recorded_traffic("volume_kernel<double, 7>", "channel_N7")
+    assert isinstance(got, int) and got > 0
     # the algorithmic bytes are 15 planes in and 5 out of 4,194,304 doubles; ncu
     # sees a little less written (part of the output still in L2)
-    assert 0.9 * 20 * 8 * 4194304 < rec < 1.05 * 20 * 8 * 4194304
+    assert 0.9 * 20 * 8 * 4194304 < got < 1.05 * 20 * 8 * 4194304
     monkeypatch.setattr(bench, "kernel_source_sha", lambda kind="volume": "0" * 16)
     assert bench.recorded_traffic("volume_kernel<double, 7>", "channel_N7") is None
 

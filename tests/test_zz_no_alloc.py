@@ -32,19 +32,21 @@ def _noalloc(lib, cfg, precision, q, Ja, phi, out, form=fd.ESDG_FORM_2D):
     return status.value
 
 
-@pytest.mark.parametrize("precision,N", [("fp64", 4), ("fp64", 7), ("fp32", 3), ("fp32", 7)])
-def test_noalloc_matches_handle_path_on_two_calls(cuda_ok, precision, N):
+@pytest.mark.parametrize("precision,N,form", [("fp64", 4, "2d"), ("fp64", 7, "2d"), ("fp32", 3, "2d"),
+                                              ("fp32", 7, "2d"), ("fp64", 5, "skew"), ("fp32", 7, "skew")])
+def test_noalloc_matches_handle_path_on_two_calls(cuda_ok, precision, N, form):
     lib = fd.load_library(build_if_missing=True)
     cfg = wl.small_config(N, K=(3, 2, 2), warp=True, precision=precision)
     g = wl.generate(cfg)
-    ref, op, Ja = hz.run_gpu(cfg, g)                       # handle path
-    _, scale = hz.run_oracle(cfg, g)                        # term scale for the tolerance
+    ref, op, Ja = hz.run_gpu(cfg, g, form=form)             # handle path, same form
+    _, scale = hz.run_oracle(cfg, g, form=0 if form == "2d" else 1)  # term scale for the tolerance
     dg = hz.to_device(g)
     q = dg["q"].to(op.dtype).contiguous()
     phi = dg["phi"].to(op.dtype).contiguous()
+    abi_form = fd.ESDG_FORM_2D if form == "2d" else fd.ESDG_FORM_SKEW
     for call in range(2):
         out = torch.full((5, cfg.n), float("nan"), dtype=op.dtype, device="cuda")
-        status = _noalloc(lib, cfg, precision, q, Ja, phi, out)
+        status = _noalloc(lib, cfg, precision, q, Ja, phi, out, form=abi_form)
         assert status == 0
         got = out.double().cpu().numpy()
         e, _ = hz.errors(got, ref, scale)
