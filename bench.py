@@ -236,6 +236,21 @@ def element_shard(K: int, world: int, rank: int):
     return e_begin, base + (1 if rank < extra else 0)
 
 
+def rank_work(K: int, world: int, rank: int, split: bool):
+    """Element range (e_begin, e_count) this rank evaluates: with --split, its
+    element_shard range of the one mesh (strong scaling: the job's work is
+    fixed and divided); otherwise the whole mesh (replicas: weak scaling)."""
+    if split and world > 1:
+        return element_shard(K, world, rank)
+    return 0, K
+
+
+def job_nodes(n: int, world: int, split: bool) -> int:
+    """Nodes the whole job evaluates per step: one mesh when split, one per rank
+    otherwise."""
+    return n if (split and world > 1) else world * n
+
+
 def max_over_ranks(x: float, group=None, device=None) -> float:
     """Largest value over all ranks (the timing rule: the slowest rank counts)."""
     import torch
@@ -272,7 +287,7 @@ def _setup(cfg, device):
     return op, q, Ja, phi, out
 
 
-def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier, what="volume"):
+def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier, what="volume", erange=None):
     """Per-call times with CUDA events on the launching stream.
 
     what: "volume" (one launch), "surface" (three launches, accumulating into
@@ -289,7 +304,10 @@ def _time_device(op, q, Ja, phi, out, steps, warmup, stream, barrier, what="volu
 
     def call():
         if what == "volume":
-            op.volume_rhs(q, Ja, phi, out=out, stream=stream)
+            if erange is None:
+                op.volume_rhs(q, Ja, phi, out=out, stream=stream)
+            else:  # one element range of the mesh (esdg_volume_rhs_range)
+                op.volume_rhs(q, Ja, phi, out=out, stream=stream, e_begin=erange[0], e_count=erange[1])
         elif what == "surface":
             op.surface_rhs(q, Ja, phi, out, stream=stream)
         elif what == "rhs":
@@ -454,7 +472,7 @@ def _cpu_baseline(cfg, budget_s: float = 12.0):
     return {"value": nodes / dt / 1e9, "unit": "GDOF/s", "cores": nthreads, "kind": "oracle",
             "sample": f"first {count} of {cfg.K} elements of {cfg.name} ({nodes} nodes), FP64 oracle, "
                       f"{dt:.1f} s, OpenMP over elements",
-            "single_core": single}
+            "elements": count, "single_core": single}
 
 
 def _cpu_single_core(cfg, budget_s: float = 2.0):
@@ -479,6 +497,75 @@ def _cpu_single_core(cfg, budget_s: float = 2.0):
     nodes = count * cfg.Nq ** 3
     return {"value": nodes / dt / 1e9, "unit": "GDOF/s", "cores": 1,
             "sample": f"first {count} of {cfg.K} elements of {cfg.name}, {dt:.1f} s"}
+
+
+PARITY_TOL = {"fp64": 1e-11, "fp32": 1e-4, "fp64ff": 1e-11}
+VARS = ("rho", "rho_u1", "rho_u2", "rho_u3", "E")
+
+
+def oracle_reference(cfg, elems):
+    """The oracle's volume term and term scale S (per node and variable) on
+    the given elements of a workload (FP64, OpenMP over elements)."""
+    import oracle
+    import workloads as wl
+
+    oracle.build()
+    elems = np.asarray(elems)
+    g = wl.generate_elements(cfg, elems)
+    gc = {k: v.numpy() for k, v in g.items()}
+    Ja, _ = oracle.metrics(cfg.N, len(elems), gc["x"], gc["y"], gc["z"])
+    out, scale = oracle.volume(cfg.N, len(elems), gc["q"], Ja, gc["phi"], with_scale=True,
+                               nthreads=oracle.max_threads())
+    return out, scale
+
+
+def parity_numbers(got, ref, scale, precision):
+    """Per conserved variable: the normalised error e_c = max|gpu - oracle| / S_c
+    (S_c = max_i sum |2 D (F + G)_c|, the magnitude of the terms the sum adds),
+    the plain relative error max|gpu - oracle| / max|oracle| and the
+    conditioning kappa_c = S_c / max|oracle_c| that separates the two."""
+    rows = {}
+    for c, name in enumerate(VARS):
+        d = float(np.max(np.abs(got[c] - ref[c])))
+        S = float(np.max(scale[c]))
+        o = float(np.max(np.abs(ref[c])))
+        rows[name] = {"e_c": d / S, "plain": d / o if o > 0 else None, "kappa": S / o if o > 0 else None}
+    worst = max(r["e_c"] for r in rows.values())
+    return {"max_e_c": worst, "tolerance": PARITY_TOL[precision], "pass": bool(worst <= PARITY_TOL[precision]),
+            "per_variable": rows}
+
+
+def _same_mesh(a, b):
+    """Whether two workloads share mesh and state (the FP32 and float-float
+    variants of a workload do; only the precision differs)."""
+    return (a.N, a.Kx, a.Ky, a.Kz, a.state, a.domain, a.warp, a.seed) == (b.N, b.Kx, b.Ky, b.Kz, b.state,
+                                                                          b.domain, b.warp, b.seed)
+
+
+def gpu_rows(out_host, cfg, elems):
+    """Columns of the given elements from a (5, n) host array of the whole mesh."""
+    np3 = cfg.Nq ** 3
+    idx = (np.asarray(elems)[:, None] * np3 + np.arange(np3)[None, :]).ravel()
+    return out_host[:, idx]
+
+
+ISSUE_PEAK_WARP_INST_PER_S = 152 * 4 * 2.07e9  # one warp instruction per SMSP and cycle at the top SM clock
+
+
+def issue_roofline(kernel, cfg, t_s):
+    """Instruction-issue roofline of a kernel that is bound by issue rather than
+    by one pipe (float-float; packed FP32): warp instructions per launch from
+    the committed ncu record of the same source (thread instructions per node
+    / 32) over the launch time, against one issue per SMSP and cycle."""
+    per_node = recorded_field(kernel, cfg.name, "inst_per_node")
+    if per_node is None:
+        return None
+    rate = per_node / 32.0 * cfg.n / t_s
+    return {"bound": "issue", "achieved": rate / 1e9, "peak": ISSUE_PEAK_WARP_INST_PER_S / 1e9,
+            "unit": "G warp instructions/s", "frac": rate / ISSUE_PEAK_WARP_INST_PER_S,
+            "inst_per_node": per_node,
+            "source": "ncu instruction count of the committed profile (same kernel source); peak = 152 SMs x 4 "
+                      "schedulers x 2.07 GHz"}
 
 
 def run_oracle_sweep(args):
@@ -563,6 +650,13 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     results = {}
     clocks = None
+    # --split: the ranks divide one mesh by element ranges (no exchange: the
+    # volume term is element-local); the surface term, the time step and the
+    # host-buffer pipeline need the whole mesh (or a face halo) and are skipped
+    split = bool(args.split and ws > 1)
+    if split:
+        args.no_surface = args.no_e2e = True
+        args.large = ""
     extra = [w for w in (args.fp32_workload, args.ff_workload) if w]
     for wname in [args.workload] + extra:
         cfg = wl.get_config(wname)
@@ -570,17 +664,20 @@ def run_ours(args):
         sampler = ClockSampler(local) if (rank == 0 and wname == args.workload) else None
         if sampler:
             sampler.start()
-        total_ms, per = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier)
+        e_range = rank_work(cfg.K, ws, rank, args.split)
+        total_ms, per = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier,
+                                     erange=e_range if split else None)
         if sampler:
             clocks = sampler.stop()
         assert op.status() == 0, "non-physical state in the bench inputs"
+        out_host = out.double().cpu().numpy() if (rank == 0 and not args.no_parity) else None
         total_ms = slowest(total_ms)
         ms = total_ms / args.steps
-        gdof = ws * cfg.n / (ms * 1e-3) / 1e9
+        gdof = job_nodes(cfg.n, ws, args.split) / (ms * 1e-3) / 1e9
         fl = flops_per_dof(cfg.N) * cfg.n
         res = {"cfg": cfg, "ms": ms, "gdof": gdof, "per": per,
                "flops_per_launch": fl, "achieved_tflops": fl / (statistics.mean(per) * 1e-3) / 1e12,
-               "bytes_per_launch": BYTES_PER_DOF[cfg.precision] * cfg.n}
+               "bytes_per_launch": BYTES_PER_DOF[cfg.precision] * cfg.n, "out_host": out_host}
         if not args.no_surface:
             s_total, s_per = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier,
                                           what="surface")
@@ -636,6 +733,31 @@ def run_ours(args):
         del q, Ja, phi, out
         torch.cuda.empty_cache()
 
+    # the largest single-GPU configuration (order sweep at N = 7, about 6.4e7
+    # nodes), FP64 and FP32, each with its own clock record and a sampled parity
+    large = []
+    for wname in [w for w in (args.large or "").split(",") if w]:
+        cfg = wl.get_config(wname)
+        op, q, Ja, phi, out = _setup(cfg, device)
+        sampler = ClockSampler(local) if rank == 0 else None
+        if sampler:
+            sampler.start()
+        total_ms, per = _time_device(op, q, Ja, phi, out, args.steps, args.warmup, stream, barrier)
+        lclocks = sampler.stop() if sampler else None
+        assert op.status() == 0, "non-physical state in the bench inputs"
+        ms = slowest(total_ms) / args.steps
+        entry = {"cfg": cfg, "ms": ms, "per": per, "clocks": lclocks}
+        if rank == 0 and not args.no_parity:
+            elems = np.asarray(wl.element_subset(cfg, min(cfg.K, args.parity_sample)))
+            np3 = cfg.Nq ** 3
+            idx = torch.from_numpy((elems[:, None] * np3 + np.arange(np3)[None, :]).ravel()).to(device)
+            entry["parity_elems"] = elems
+            entry["gpu_rows"] = out[:, idx].double().cpu().numpy()
+        large.append(entry)
+        op.close()
+        del q, Ja, phi, out
+        torch.cuda.empty_cache()
+
     if rank != 0:
         if ws > 1:
             dist.destroy_process_group()
@@ -662,11 +784,13 @@ def run_ours(args):
     line = {
         "metric": "volume-term GDOF/s (FP64)", "value": main["gdof"], "unit": "GDOF/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms"], "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "scaling": "strong" if split else "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.name, "N": cfg.N, "K": cfg.K, "elements": [cfg.Kx, cfg.Ky, cfg.Kz],
                    "nodes": cfg.n, "precision": cfg.precision, "form": "2d",
                    "l2": f"inputs {15 * cfg.n * 8 / 1e6:.0f} MB > 129 MB L2, no flush",
-                   "parallelism": f"elements, {ws} rank(s), no exchange"},
+                   "parallelism": (f"one mesh split into {ws} contiguous element ranges (esdg_volume_rhs_range), "
+                                   "no exchange" if split else f"elements, {ws} rank(s) with a mesh each, "
+                                   "no exchange")},
         "roofline": roof,
         "gpu_launches": args.steps,
         "clocks": clocks,
@@ -685,7 +809,9 @@ def run_ours(args):
                          "traffic": recorded_traffic(f"volume_kernel<float, {c32.N}>", c32.name),
                          "peak_source": "measured FP32 vector FMA",
                          "hbm": {"achieved_gbs": hbm32, "peak_gbs": peaks.get("hbm_gbs"),
-                                 "frac": hbm32 / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None}},
+                                 "frac": hbm32 / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None},
+                         "issue": issue_roofline(f"volume_kernel<float, {c32.N}>", c32,
+                                                 statistics.mean(r32["per"]) * 1e-3)},
         }
         if "e2e" in r32:
             line["fp32"]["e2e"] = {k: v for k, v in r32["e2e"].items() if k != "ms_per_step"}
@@ -707,10 +833,11 @@ def run_ours(args):
             "workload": cf.name, "value": rf["gdof"], "unit": "GDOF/s", "ms_per_step": rf["ms"],
             "dtype": "f64 storage, f32x2 (float-float) arithmetic",
             "speedup_vs_fp64": main["ms"] / rf["ms"],
-            "roofline": {"bound": "alu", "achieved_fp64_equivalent": rf["achieved_tflops"],
-                         "unit": "TFLOP/s", "fp64_peak": peak64,
-                         "frac_of_fp64_peak": rf["achieved_tflops"] / peak64,
-                         "traffic": recorded_traffic(f"volume_kernel<double, {cf.N}, ff>", cf.name)},
+            # the float-float arithmetic runs on the FP32 pipes and is bound by
+            # instruction issue, not by one pipe: its roofline is the issue rate
+            "roofline": issue_roofline(f"volume_kernel<double, {cf.N}, ff>", cf, statistics.mean(rf["per"]) * 1e-3),
+            "algorithmic_fp64_equivalent_TFLOP/s": rf["achieved_tflops"],
+            "traffic": recorded_traffic(f"volume_kernel<double, {cf.N}, ff>", cf.name),
         }
         if "e2e" in rf:
             line["fp64ff"]["e2e"] = {k: v for k, v in rf["e2e"].items() if k != "ms_per_step"}
@@ -731,12 +858,53 @@ def run_ours(args):
         line["gpu_launches"] += (3 + rhs_launches("fp32")) * args.steps
     if args.ff_workload and "surface" in results[args.ff_workload]:
         rf = results[args.ff_workload]
-        line["fp64ff"]["surface"] = _surface_report(rf["cfg"], rf["surface"], ws, peak64, "FP64 vector",
+        line["fp64ff"]["surface"] = _surface_report(rf["cfg"], rf["surface"], ws, None,
+                                                    "none: float-float on the FP32 pipes, latency-bound",
                                                     peaks.get("hbm_gbs"))
         line["gpu_launches"] += (3 + rhs_launches("fp64ff")) * args.steps
     line["peaks_measured"] = {"fp64_tflops": fp64_meas, "fp32_tflops": fp32_meas}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(cfg, args.cpu_seconds)
+    if not args.no_parity:
+        # every timed kernel's output against the oracle, element by element, on
+        # the elements the CPU baseline covered (the whole mesh when it fits)
+        count = line.get("cpu_baseline", {}).get("elements") or min(cfg.K, args.parity_sample)
+        count = min(count, rank_work(cfg.K, ws, 0, split)[1])  # rank 0 holds its own range only
+        elems = np.arange(count)
+        ref, scale = oracle_reference(cfg, elems)
+        par = {"sample": f"first {count} of {cfg.K} elements of {cfg.name}",
+               "oracle": "FP64 oracle on the FP64 inputs (FP32 kernel: its inputs are those rounded to FP32)"}
+        for key, wname in (("fp64", args.workload), ("fp32", args.fp32_workload), ("fp64ff", args.ff_workload)):
+            if wname and results[wname].get("out_host") is not None and \
+                    (wname == args.workload or _same_mesh(results[wname]["cfg"], cfg)):
+                par[key] = parity_numbers(gpu_rows(results[wname]["out_host"], cfg, elems), ref, scale,
+                                          results[wname]["cfg"].precision)
+        line["parity"] = par
+    if large:
+        line["largest"] = []
+        for ent in large:
+            lc = ent["cfg"]
+            t = statistics.mean(ent["per"]) * 1e-3
+            fl = flops_per_dof(lc.N) * lc.n
+            ach = fl / t / 1e12
+            pk = peak64 if lc.precision == "fp64" else fp32_meas
+            hbm = BYTES_PER_DOF[lc.precision] * lc.n / t / 1e9
+            rep = {"workload": lc.name, "precision": lc.precision, "N": lc.N,
+                   "elements": [lc.Kx, lc.Ky, lc.Kz], "nodes": lc.n,
+                   "value": ws * lc.n / (ent["ms"] * 1e-3) / 1e9, "unit": "GDOF/s", "ms_per_step": ent["ms"],
+                   "roofline": {"bound": "alu", "achieved": ach, "peak": pk, "unit": "TFLOP/s",
+                                "frac": ach / pk if pk == pk else None,
+                                "peak_source": ("FP64" if lc.precision == "fp64" else "FP32") + " vector FMA",
+                                "hbm": {"achieved_gbs": hbm, "peak_gbs": peaks.get("hbm_gbs"),
+                                        "frac": hbm / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None}},
+                   "clocks": ent["clocks"]}
+            if "gpu_rows" in ent:
+                r2, sc2 = oracle_reference(lc, ent["parity_elems"])
+                rep["parity"] = dict(parity_numbers(ent["gpu_rows"], r2, sc2, lc.precision),
+                                     sample=f"{len(ent['parity_elems'])} elements spread over the mesh "
+                                            f"(first and last included)")
+            line["largest"].append(rep)
+            line["gpu_launches"] += args.steps
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -766,7 +934,7 @@ def _surface_report(cfg, sres, ws, alu_peak_tflops, alu_peak_name, hbm_peak_gbs)
     t = statistics.mean(sres["per"]) * 1e-3
     tfl = flops / t / 1e12
     gbs = nbytes / t / 1e9
-    f_alu = tfl / alu_peak_tflops if alu_peak_tflops == alu_peak_tflops else None
+    f_alu = tfl / alu_peak_tflops if (alu_peak_tflops is not None and alu_peak_tflops == alu_peak_tflops) else None
     f_hbm = gbs / hbm_peak_gbs if hbm_peak_gbs else None
     bound = "hbm" if (f_hbm or 0) >= (f_alu or 0) else "alu"
     kname = {"fp64": "surface_kernel<double>", "fp32": "surface_kernel<float>",
@@ -898,6 +1066,11 @@ def run_sweep(args):
 
     orders:   the ~6.4e7-node warped cube for N = 2..8 in FP64 and FP32
               (the order-sweep workloads).
+    parity:   the named workloads (tiny box, bubble, channel, order sweep at
+              N = 7) in each precision against the oracle: normalised error,
+              plain relative error and conditioning per variable (whole mesh
+              up to 4.2e6 nodes, a spread sample of elements beyond).
+    Every point carries the SM clocks sampled during its timed region.
     elements: throughput against element count for several orders on a
               warped cube with K = k^3 elements (as in the paper's Fig. 5:
               single-GPU saturation), reported in GDOF/s and in thousands of
@@ -918,6 +1091,14 @@ def run_sweep(args):
         for N in [int(v) for v in args.orders.split(",")]:
             for prec in precs:
                 points.append(wl.get_config(f"sweep_N{N}" + {"fp64": "", "fp32": "_fp32", "fp64ff": "_ff"}[prec]))
+    elif args.sweep == "parity":
+        # the five named workloads in every precision (the FP32 and float-float
+        # variants share mesh and state), compared with the oracle
+        import dataclasses
+        for name in ("tiny_box_N3", "bubble_N4", "channel_N7", "sweep_N7"):
+            base = wl.get_config(name)
+            for prec in precs:
+                points.append(dataclasses.replace(base, name=f"{name}:{prec}", precision=prec))
     else:
         for N in (2, 4, 7, 8):
             for k in (2, 4, 8, 16, 32, 48, 64):
@@ -927,15 +1108,30 @@ def run_sweep(args):
                     points.append(wl.small_config(N, K=(k, k, k), warp=True, precision=prec))
     for cfg in points:
         op, q, Ja, phi, out = _setup(cfg, device)
-        # short launches need more of them for a stable mean
+        # short launches need more of them for a stable mean, and a timed
+        # region long enough for the clock samples (100 ms apart)
         steps = max(args.steps, 3)
+        _time_device(op, q, Ja, phi, out, 2, 1, stream, lambda: None)
+        probe = (lambda t: t[0] / 2)(_time_device(op, q, Ja, phi, out, 2, 0, stream, lambda: None))
+        steps = max(steps, int(0.5 / max(probe * 1e-3, 1e-6)))
+        sampler = ClockSampler(0)
+        sampler.start()
         total_ms, per = _time_device(op, q, Ja, phi, out, steps, args.warmup, stream, lambda: None)
+        clocks = sampler.stop()
         ms = total_ms / steps
         line = {"sweep": args.sweep, "config": cfg.name, "N": cfg.N, "K": cfg.K, "nodes": cfg.n,
                 "precision": cfg.precision, "ms_per_launch": ms, "GDOF/s": cfg.n / (ms * 1e-3) / 1e9,
                 "kilo_element_evals_per_s": cfg.K / (ms * 1e-3) / 1e3,
                 "algorithmic_TFLOP/s": flops_per_dof(cfg.N) * cfg.n / (ms * 1e-3) / 1e12,
-                "HBM_GB/s": BYTES_PER_DOF[cfg.precision] * cfg.n / (ms * 1e-3) / 1e9}
+                "HBM_GB/s": BYTES_PER_DOF[cfg.precision] * cfg.n / (ms * 1e-3) / 1e9,
+                "steps": steps, "clocks": clocks}
+        if args.sweep == "parity":
+            elems = (np.arange(cfg.K) if cfg.n <= 1 << 22 else
+                     np.asarray(wl.element_subset(cfg, min(cfg.K, args.parity_sample))))
+            ref, scale = oracle_reference(cfg, elems)
+            line["parity"] = dict(parity_numbers(gpu_rows(out.double().cpu().numpy(), cfg, elems), ref, scale,
+                                                 cfg.precision),
+                                  sample=f"{len(elems)} of {cfg.K} elements")
         print(json.dumps(line), flush=True)
         op.close()
         del q, Ja, phi, out
@@ -959,11 +1155,19 @@ def main():
     ap.add_argument("--no-peaks", action="store_true", help="skip the FMA-throughput peak measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=int, default=256)
-    ap.add_argument("--sweep", choices=["orders", "elements", "graph", "oracle"], default=None,
+    ap.add_argument("--sweep", choices=["orders", "elements", "graph", "oracle", "parity"], default=None,
                     help="opt-in measurement sweeps (one JSON line per point) instead of the bench line")
     ap.add_argument("--precisions", default="fp64,fp32,fp64ff",
                     help="comma-separated precisions of the orders and elements sweeps")
     ap.add_argument("--orders", default="2,3,4,5,6,7,8", help="comma-separated orders N of the orders sweep")
+    ap.add_argument("--large", default="sweep_N7,sweep_N7_fp32",
+                    help="largest single-GPU workloads timed in the same run (comma-separated; '' for none)")
+    ap.add_argument("--no-parity", action="store_true", help="skip the parity report against the oracle")
+    ap.add_argument("--split", action="store_true",
+                    help="under torchrun: divide one mesh among the ranks by element ranges (strong scaling) "
+                         "instead of one mesh per rank (weak scaling)")
+    ap.add_argument("--parity-sample", type=int, default=512,
+                    help="elements compared with the oracle when the CPU baseline does not set the sample")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

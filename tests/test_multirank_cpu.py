@@ -2,10 +2,10 @@
 
 The volume term is element-local, so ranks that each evaluate one contiguous
 element range need no exchange; the only collective of the benchmark is the
-max-over-ranks of its timed region.  Each rank here evaluates its range with
-the oracle (CPU) and rank 0 gathers the pieces: they must reproduce the
-single-process result bitwise, and the max reduction must return the slowest
-rank's value.
+max-over-ranks of its timed region.  Each rank here takes the element range
+that bench.py --split gives it (bench.rank_work), evaluates it with the oracle
+(CPU) and rank 0 gathers the pieces: they must reproduce the single-process
+result bitwise, and the max reduction must return the slowest rank's value.
 """
 import os
 import socket
@@ -35,7 +35,9 @@ def _rank_main(rank, world, port, cfg_args, result_path):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         cfg = wl.small_config(*cfg_args[0], K=cfg_args[1], warp=True)
-        e0, ec = bench.element_shard(cfg.K, world, rank)
+        # the bench's --split arithmetic decides this rank's element range
+        e0, ec = bench.rank_work(cfg.K, world, rank, split=True)
+        assert (e0, ec) == bench.element_shard(cfg.K, world, rank)
         g = wl.generate_elements(cfg, np.arange(e0, e0 + ec))
         gc = {k: v.numpy() for k, v in g.items()}
         Ja, _ = oracle.metrics(cfg.N, ec, gc["x"], gc["y"], gc["z"])
@@ -70,6 +72,20 @@ def test_element_shard_covers_range():
                 pos += ec
             assert pos == K
             assert max(c for _, c in rng) - min(c for _, c in rng) <= 1
+
+
+def test_split_and_replica_work():
+    """--split: each rank its element_shard range and the job one mesh (strong
+    scaling); replicas: each rank the whole mesh and the job one per rank."""
+    for K in (1, 15, 8192):
+        for world in (1, 2, 4, 8):
+            ranges = [bench.rank_work(K, world, r, split=True) for r in range(world)]
+            assert ranges == [bench.element_shard(K, world, r) for r in range(world)]
+            assert sum(c for _, c in ranges) == K
+            assert all(bench.rank_work(K, world, r, split=False) == (0, K) for r in range(world))
+            n = K * 64
+            assert bench.job_nodes(n, world, split=True) == n
+            assert bench.job_nodes(n, world, split=False) == world * n
 
 
 def test_two_rank_partition_matches_single_process(tmp_path):
