@@ -73,6 +73,8 @@ _SIGS = {
     "esdg_selftest_rcp": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, _P, _P, _P]),
     "esdg_selftest_ff": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, _P, _P, _P, _P]),
     "esdg_selftest_log": (ctypes.c_int, [ctypes.c_long, _P, _P, _P]),
+    "esdg_selftest_index_maps": (ctypes.c_int, [ctypes.c_int, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                                ctypes.POINTER(ctypes.c_int), ctypes.c_char_p, ctypes.c_int]),
 }
 
 

@@ -36,6 +36,7 @@ def _units():
              ("geometry", os.path.join(CSRC, "geometry.cu"), []),
              ("peak_bench", os.path.join(CSRC, "peak_bench.cu"), []),
              ("esdg_noalloc", os.path.join(CSRC, "esdg_noalloc.cu"), []),
+             ("index_check", os.path.join(CSRC, "index_check.cu"), []),
              ("time", os.path.join(CSRC, "time_kernel.cu"), []),
              ("pipeline", os.path.join(CSRC, "esdg_pipeline.cu"), [])]
     for prec, tag in ((0, "fp64"), (1, "fp32"), (2, "fp64ff")):

@@ -120,19 +120,26 @@ void lgl_operators(int N, double* nodes, double* weights, double* D) {
 
 void set_unhandled_error(const char* msg) { g_create_error = msg; }
 
-}  // namespace esdg
-
-namespace {
-
 template <typename T>
-void fill_tables(esdg::OpTables<T>& t, int N, const double* w, const double* D) {
+void fill_op_tables(OpTables<T>& t, int N) {
+    double x[kMaxNq], w[kMaxNq], D[kMaxNq * kMaxNq];
+    lgl_operators(N, x, w, D);
     const int Nq = N + 1;
     std::memset(&t, 0, sizeof(t));
     for (int i = 0; i < Nq; ++i) {
         t.invw[i] = (T)(1.0L / (long double)w[i]);
         for (int j = 0; j < Nq; ++j) t.Q2[i * Nq + j] = (T)(2.0L * (long double)w[i] * (long double)D[i * Nq + j]);
     }
+    t.diag[0] = (T)(2.0L * (long double)D[0]);
+    t.diag[N] = (T)(2.0L * (long double)D[N * Nq + N]);
 }
+template void fill_op_tables<double>(OpTables<double>&, int);
+template void fill_op_tables<float>(OpTables<float>&, int);
+
+}  // namespace esdg
+
+namespace {
+
 
 template <typename T>
 esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja, const void* phi, void* out,
@@ -360,8 +367,8 @@ int esdg_create(esdg_handle* out, long Kx, long Ky, long Kz, int N, int precisio
     h->precision = precision;
     h->form = form;
     esdg::lgl_operators(N, h->nodes, h->weights, h->D);
-    fill_tables(h->op64, N, h->weights, h->D);
-    fill_tables(h->op32, N, h->weights, h->D);
+    esdg::fill_op_tables(h->op64, N);
+    esdg::fill_op_tables(h->op32, N);
     cudaError_t e = cudaGetDevice(&h->device);
     if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(unsigned));

@@ -15,11 +15,18 @@ constexpr int kMaxNq = kMaxN + 1;
 // kernel's parameter space, i.e. the constant bank).
 //   Q2[i*Nq + j] = 2 w_i D_ij   (twice the SBP matrix Q = W D)
 //   invw[i]      = 1 / w_i
+//   diag[i]      = 2 D_ii at the end nodes i = 0, N (the 2D form's diagonal
+//                  factor), 0 at interior nodes
 template <typename T>
 struct OpTables {
     T Q2[kMaxNq * kMaxNq];
     T invw[kMaxNq];
+    T diag[kMaxNq];
 };
+
+// Fill the tables of order N from the library's LGL operators (host).
+template <typename T>
+void fill_op_tables(OpTables<T>& t, int N);
 
 // Surface term: constants derived from gamma.
 template <typename T>

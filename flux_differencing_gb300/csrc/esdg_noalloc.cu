@@ -103,18 +103,6 @@ cudaError_t scratch_address(int dev, unsigned** out) {
 }
 
 template <typename T>
-void fill_ops(esdg::OpTables<T>& t, int N) {
-    double x[esdg::kMaxNq], w[esdg::kMaxNq], D[esdg::kMaxNq * esdg::kMaxNq];
-    esdg::lgl_operators(N, x, w, D);
-    const int Nq = N + 1;
-    std::memset(&t, 0, sizeof(t));
-    for (int i = 0; i < Nq; ++i) {
-        t.invw[i] = (T)(1.0L / (long double)w[i]);
-        for (int j = 0; j < Nq; ++j) t.Q2[i * Nq + j] = (T)(2.0L * (long double)w[i] * (long double)D[i * Nq + j]);
-    }
-}
-
-template <typename T>
 cudaError_t launch_noalloc(long K, int N, int form, double gamma, const void* q, const void* Ja, const void* phi,
                            void* out, unsigned* status, cudaStream_t s) {
     esdg::VolumeArgs<T> a{};  // value-initialised: the fused-stage fields stay null
@@ -137,7 +125,7 @@ cudaError_t launch_noalloc(long K, int N, int form, double gamma, const void* q,
     a.rk_S = nullptr;
     a.rk_J = nullptr;
     a.rk_A = a.rk_B = a.rk_dt = a.rk_f = T(0);
-    fill_ops(a.ops, N);
+    esdg::fill_op_tables(a.ops, N);
     if constexpr (sizeof(T) == sizeof(double)) {
         switch (N) {
             case 1: return esdg::launch_volume_fp64_n1(a, s);

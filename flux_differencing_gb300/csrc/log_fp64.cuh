@@ -1,6 +1,7 @@
-// Natural logarithm of a positive normal double in 15 FP64-pipe operations
+// Natural logarithm of a positive normal double in 12 FP64-pipe operations
 // (CUDA's log() takes 28 on sm_103a, counted with ncu), for the volume
-// kernel's two per-node logarithms.
+// kernel's two per-node logarithms, whose only use is in differences
+// ln a+ - ln a- of two nodes (the logarithmic means and their closeness test).
 //
 // Method: table-driven argument reduction, P. T. P. Tang, "Table-driven
 // implementation of the logarithm function in IEEE floating-point
@@ -10,20 +11,26 @@
 //     ln x = k ln 2 + ln F + ln(1 + r),   r = (m - F)/F,   |r| <= 2^-8,
 // where m - F is exact (Sterbenz's lemma: m and F are within a factor two),
 // 1/F and ln F come from a 130-entry table (log_table.inc, written by
-// gen_log_table.py from 50-digit arithmetic; ln F as a lead and a trail
-// double, since ln F and ln(1 + r) can have opposite signs and a singly
-// rounded ln F would then cost up to one ulp of the result), and ln(1 + r)
-// is its Taylor series to r^7 (the first dropped term is below 2^-59 |r|).
-// ln 2 is split so that k ln2_hi is exact.
+// gen_log_table.py from 50-digit arithmetic), and ln(1 + r) is its Taylor
+// series to r^7 (the first dropped term is below 2^-59 |r|).  The result is
+// formed as k ln2 + (ln F + ln(1 + r)) with ln 2 and ln F each rounded once.
+//
+// Accuracy for the use made of it: the rounding of ln 2 (below 2^-55) is
+// multiplied by k, the same k for both nodes of nearly every pair, so it
+// cancels in the difference of two logarithms unless the two values straddle
+// a power of two (then it contributes |k+ - k-| 2^-55); the rounding of ln F
+// (below 2^-55) and of the inner sum (half an ulp of a number below 0.41)
+// are far below the final rounding, half an ulp of the result.  So a
+// difference of two of these logarithms is within one ulp of the larger
+// result (plus |k+ - k-| 2^-55) of the exact ln(a+/a-), as for correctly
+// rounded logarithms; the absolute value carries up to |k| 2^-55 more.
 //
 // The reduction to [0.75, 1.5) rather than [1, 2) keeps every x near 1 on
 // the k = 0 branch, with F = 1 and r = x - 1 exactly when |x - 1| < 2^-9:
-// there is no cancellation of ln F against k ln 2, so the result keeps its
-// relative accuracy near 1 (checked on the GPU against the host's log: within
-// 2 ulp).  Exponent and mantissa are taken apart on the integer pipe.  Inputs
-// that are not positive normal numbers give a meaningless value without
-// faulting (the table index is always in range); the kernel flags such
-// non-physical states separately.
+// the result keeps its relative accuracy near 1.  Exponent and mantissa are
+// taken apart on the integer pipe.  Inputs that are not positive normal
+// numbers give a meaningless value without faulting (the table index is
+// always in range); the kernel flags such non-physical states separately.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -42,7 +49,6 @@ __device__ __forceinline__ double log_fp64(double x) {
     const double m = __hiloint2double(ebits | mant, lo);
     const double F = __hiloint2double(ebits + (j << 13), 0);  // j = 128, halved: exactly 1
     const double2 t = __ldg(&kLogTable[j + half]);    // (1/F, ln F rounded)
-    const double tl = __ldg(&kLogTail[j + half]);      // ln F - t.y
     const int k = ((hi >> 20) & 0x7ff) - 1023 + half;
     // (double)k without a conversion instruction: 2^52 + (k + 1024) has k + 1024
     // in its low mantissa word
@@ -56,7 +62,7 @@ __device__ __forceinline__ double log_fp64(double x) {
     q = fma(q, r, 1.0 / 3.0);
     q = fma(q, r, -0.5);
     const double p = fma(r2, q, r);
-    return fma(kd, kLn2Hi, t.y) + (fma(kd, kLn2Lo, p) + tl);
+    return fma(kd, kLn2, t.y + p);
 }
 
 }  // namespace esdg

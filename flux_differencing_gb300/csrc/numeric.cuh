@@ -67,8 +67,13 @@ struct Num<ff> {
         return (__float_as_uint(f.hi) & 0x7fffffffu) < 0x3C23D70Au;  // |f| < 0.01
     }
 };
-// x > 0 (false for NaN), for the non-physical-state check
-__device__ __forceinline__ bool positive(double x) { return x > 0.0; }
+// x > 0 (false for NaN), for the non-physical-state check.  FP64: a test of
+// the high word on the integer pipe (1 <= hi <= 0x7fefffff), which also takes
+// +infinity and the positive numbers below 2^-1042 (high word zero) as not
+// positive -- neither is a physical density or pressure.
+__device__ __forceinline__ bool positive(double x) {
+    return static_cast<unsigned>(__double2hiint(x) - 1) < 0x7fefffffu;
+}
 __device__ __forceinline__ bool positive(float x) { return x > 0.0f; }
 __device__ __forceinline__ bool positive(ff x) { return x.hi > 0.0f; }
 

@@ -40,19 +40,11 @@
 #include "esdg_internal.h"
 #include "numeric.cuh"
 #include "surface_flux.cuh"
+#include "surface_index.cuh"
 
 namespace esdg {
 
 namespace {
-
-// Node index of face node (s1, s2) on the face a_DIR = A of a (N+1)^3 element.
-template <int N, int DIR>
-__device__ __forceinline__ int face_node(int A, int s1, int s2) {
-    constexpr int NQ = N + 1;
-    if constexpr (DIR == 0) return A + NQ * (s1 + NQ * s2);
-    else if constexpr (DIR == 1) return s1 + NQ * (A + NQ * s2);
-    else return s1 + NQ * (s2 + NQ * A);
-}
 
 template <typename T>
 __device__ __forceinline__ void load_node(const SurfaceArgs<T>& a, long long g, int dir, T (&q)[5], T& phi,
@@ -99,36 +91,16 @@ struct SurfaceOccupancy {
 template <typename T, typename C, int N, int DIR>
 __global__ void __launch_bounds__(256, SurfaceOccupancy<C>::value) surface_kernel(const __grid_constant__ SurfaceArgs<T> a) {
     constexpr int NQ = N + 1;
-    constexpr int NF = NQ * NQ;
     using CV = Conv<T, C>;
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long K = a.Kx * a.Ky * a.Kz;
     const long long Kd[3] = {a.Kx, a.Ky, a.Kz};
     const long long stride = (DIR == 0) ? 1 : (DIR == 1) ? a.Kx : a.Kx * a.Ky;
     const bool wall_dir = a.bc[DIR] != 0;
-    const long long n_plus = K * NF;
-    const long long n_minus = wall_dir ? (K / Kd[DIR]) * NF : 0;
-    if (t >= n_plus + n_minus) return;
-
-    long long e;
+    long long e, er;
     int f;
     bool plus_face;
-    if (t < n_plus) {
-        e = t / NF;
-        f = (int)(t - e * NF);
-        plus_face = true;
-    } else {
-        const long long u = t - n_plus;
-        const long long k = u / NF;
-        f = (int)(u - k * NF);
-        // element with index 0 along DIR, k enumerating the other two indices
-        if (DIR == 0) e = k * a.Kx;
-        else if (DIR == 1) e = (k % a.Kx) + (k / a.Kx) * a.Kx * a.Ky;
-        else e = k;
-        plus_face = false;
-    }
+    if (!surface_slot<N>(DIR, t, a.Kx, a.Ky, a.Kz, wall_dir, e, f, plus_face, er)) return;
     const int s1 = f % NQ, s2 = f / NQ;
-    const long long er = (DIR == 0) ? e % a.Kx : (DIR == 1) ? (e / a.Kx) % a.Ky : e / (a.Kx * a.Ky);
     const long long NP3 = (long long)NQ * NQ * NQ;
     Consts<C> k;
     k.gm1 = CV::in(a.k.gm1);

@@ -123,7 +123,7 @@ struct Slots {
     static constexpr int NQ = S::NQ;
     static constexpr int ES = Lo::SWZ ? S::NP3 : Lo::P2 * NQ;  // element stride
     static constexpr int SIZE = S::EPB * ES;                    // values per field
-    static __device__ __forceinline__ int at(int el, int a, int b, int c) {
+    static __host__ __device__ __forceinline__ int at(int el, int a, int b, int c) {
         if constexpr (Lo::SWZ) return el * ES + NQ * (b + NQ * c) + (a ^ ((c ^ (b & Lo::MASK)) & (NQ - 1)));
         else return el * ES + a + Lo::P1 * b + Lo::P2 * c;
     }
@@ -147,7 +147,7 @@ struct Num<p2> {
 // Node (a, b, c) of line `ell` of direction R at line position p.  R may be
 // a compile-time constant (folded) or a runtime value.
 template <int N>
-__device__ __forceinline__ void line_node(int R, int ell, int p, int& a, int& b, int& c) {
+__host__ __device__ __forceinline__ void line_node(int R, int ell, int p, int& a, int& b, int& c) {
     using Lo = Layout<N>;
     constexpr int NQ = N + 1;
     const int ord = (R == 0) ? Lo::ORD0 : (R == 1) ? Lo::ORD1 : Lo::ORD2;
@@ -173,7 +173,7 @@ struct FaceFirst {
 };
 
 template <int N>
-__device__ __forceinline__ int face_first_node(int k) {
+__host__ __device__ __forceinline__ int face_first_node(int k) {
     constexpr int NQ = N + 1;
     constexpr int SLAB = NQ * NQ;
     constexpr int NI = N - 1;                    // interior nodes per line
@@ -304,10 +304,10 @@ struct FaceSlots {
     static constexpr int PER_EL = 6 * NF;
     static constexpr int COUNT = PER_EL * Shape<N>::EPB;
     static constexpr int FIELDS = 11;
-    static __device__ __forceinline__ int slot(int el, int dir, int side, int i1, int i2) {
+    static __host__ __device__ __forceinline__ int slot(int el, int dir, int side, int i1, int i2) {
         return el * PER_EL + (2 * dir + side) * NF + i1 + NQ * i2;
     }
-    static __device__ __forceinline__ void decode(int s, int& el, int& dir, int& side, int& i1, int& i2) {
+    static __host__ __device__ __forceinline__ void decode(int s, int& el, int& dir, int& side, int& i1, int& i2) {
         el = s / PER_EL;
         const int r = s - el * PER_EL;
         const int f = r / NF;
@@ -318,7 +318,7 @@ struct FaceSlots {
         i2 = w / NQ;
     }
     // (a, b, c) of the node at index A along dir with other indices (i1, i2)
-    static __device__ __forceinline__ void node(int dir, int A, int i1, int i2, int& na, int& nb, int& nc) {
+    static __host__ __device__ __forceinline__ void node(int dir, int A, int i1, int i2, int& na, int& nb, int& nc) {
         na = dir == 0 ? A : i1;
         nb = dir == 1 ? A : (dir == 0 ? i1 : i2);
         nc = dir == 2 ? A : i2;
@@ -329,7 +329,7 @@ struct FaceSlots {
 // (64-bit divisions: evaluated once per element and face, into the CTA's
 // neighbour table).
 template <typename T>
-__device__ __forceinline__ long long neighbour_element(const VolumeArgs<T>& a, long long e, int dir, int side) {
+__host__ __device__ __forceinline__ long long neighbour_element(const VolumeArgs<T>& a, long long e, int dir, int side) {
     const long long Kd = dir == 0 ? a.Kx : dir == 1 ? a.Ky : a.Kz;
     const long long stride = dir == 0 ? 1 : dir == 1 ? a.Kx : a.Kx * a.Ky;
     const long long r = (e / stride) % Kd;  // element index along dir
@@ -341,8 +341,8 @@ __device__ __forceinline__ long long neighbour_element(const VolumeArgs<T>& a, l
 // local element el, with the neighbour table nbr[6 el + 2 dir + side]; false
 // at a slip wall.
 template <int N>
-__device__ __forceinline__ bool face_neighbour(const long long* nbr, int el, int dir, int side, int i1, int i2,
-                                               long long& g) {
+__host__ __device__ __forceinline__ bool face_neighbour(const long long* nbr, int el, int dir, int side, int i1,
+                                                        int i2, long long& g) {
     constexpr int NQ = N + 1;
     const long long en = nbr[6 * el + 2 * dir + side];
     if (en < 0) return false;
@@ -379,33 +379,48 @@ constexpr size_t volume_smem_bytes() {
                : volume_smem_fields<C, N, MODE>();
 }
 
-// One pair (i, m) of a line, evaluated once for both nodes.  cq = Q_{pp'}
-// with p, p' the positions of i and m.  Adds node i's share 2Q_{pp'} (F +
-// G(i,m)) to o0..o4 and returns node m's share 2Q_{p'p} (F + G(m,i)) =
-// -2Q_{pp'} (F + G(m,i)) in t0..t4, G(m,i) = -G(i,m) b_i/b_m (Sec. 4.1);
-// t0 and t4 are returned with the opposite sign (the receiver subtracts
-// them), which saves two negations per pair.  Both shares still need the
-// 1/w scaling of their own node.
+// The scalars of one pair (i, m) of a line from which both nodes' shares
+// are formed (see pair_flux): cq = Q_{pp'} with p, p' the positions of i and m
+// on the line, c_g2 = 1/(gamma - 1).
+//   fr      2Q F_rho (mass flux times 2Q_{pp'})
+//   fE      2Q F_E
+//   Pi, Pm  the momentum flux's scalar factor of A at node i and at node m:
+//           Q (p_hat + gravity scaled at b_i) and Q (-p_hat + gravity scaled
+//           at b_m), G(m,i) = -G(i,m) b_i/b_m (Sec. 4.1)
+//   s       the mean velocity {{u}}, A = Ja_i + Ja_m (twice the averaged metric)
+// Node i's share of the momentum is fr s + A Pi, node m's -fr s + A Pm; the
+// mass and energy shares are +-fr and +-fE.
 //
 // Scaling of the per-node values (chosen so that no factor of 2 is applied
 // per pair): u holds u/2, so s = u_i + u_m is the mean velocity; b holds
 // b2 = 2b = rho/p (1/b and ln b2 as stored); phi holds phi/8; the metric
 // terms are unscaled, so A = Ja_i + Ja_m is twice the averaged metric and
-// Un = s.A twice the contravariant velocity U.  c_g2 = 1/(gamma - 1).
+// Un = s.A twice the contravariant velocity U.
 template <typename T>
-__device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T>& M, T cq, T c_g2, T& o0, T& o1,
-                                          T& o2, T& o3, T& o4, T& t0, T& t1, T& t2, T& t3, T& t4) {
-    const T A0 = I.A0 + M.A0, A1 = I.A1 + M.A1, A2 = I.A2 + M.A2;
-    const T s1 = I.u1 + M.u1, s2 = I.u2 + M.u2, s3 = I.u3 + M.u3;
-    const T Un = fma(s3, A2, fma(s2, A1, s1 * A0));
+struct PairTerms {
+    T fr, fE, Pi, Pm, s1, s2, s3, A0, A1, A2;
+};
 
-    // rho_ln = {{rho}}_log, inv_bsum = 1/(b2+ + b2-) = 1/(4{{b}}) and
-    // inv_bln = 1/(2{{b}}_log)
+template <typename T>
+__device__ __forceinline__ PairTerms<T> pair_terms(const NodeVals<T>& I, const NodeVals<T>& M, T cq, T c_g2) {
+    PairTerms<T> o;
+    o.A0 = I.A0 + M.A0;
+    o.A1 = I.A1 + M.A1;
+    o.A2 = I.A2 + M.A2;
+    o.s1 = I.u1 + M.u1;
+    o.s2 = I.u2 + M.u2;
+    o.s3 = I.u3 + M.u3;
+    const T Un = fma(o.s3, o.A2, fma(o.s2, o.A1, o.s1 * o.A0));
+
+    // crl = Q {{rho}}_log, inv_bsum = 1/(b2+ + b2-) = 1/(4{{b}}) and
+    // inv_bln = 1/(2{{b}}_log); cqr = Q (rho+ + rho-) serves the pressure
+    // mean and the close density branch
     const T rsum = I.rho + M.rho;
     const T bsum = I.b + M.b;
     const T dlr = M.lr - I.lr;
     const T dlb = M.lb - I.lb;
-    T rho_ln, inv_bsum, inv_bln;
+    const T cqr = cq * rsum;
+    T crl, inv_bsum, inv_bln;
     if constexpr (std::is_same<T, float>::value || std::is_same<T, p2>::value) {
         // FP32: per-lane selects (the vote of the FP64 branch was measured
         // slower for this issue-bound kernel: 0.215 -> 0.237 ms on the N = 7
@@ -417,7 +432,7 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
         const T ur = tr * tr;
         // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945)
         const T polr = fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
-        rho_ln = sel(cr, rsum * polr, tr);
+        crl = sel(cr, cqr * polr, cq * tr);
 
         // 1/(b2+ + b2-) and the inverse log mean from one reciprocal
         const T db = M.b - I.b;
@@ -449,11 +464,11 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
             return fma(v, fma(v, fma(v, T(1.0 / 15120.0), T(-1.0 / 360.0)), T(1.0 / 6.0)), T(2.0));
         };
         if (!__any_sync(mask, cr)) {
-            rho_ln = (M.rho - I.rho) * Num<T>::rcp(dlr);
+            crl = (cq * (M.rho - I.rho)) * Num<T>::rcp(dlr);
         } else if (__all_sync(mask, cr)) {
-            rho_ln = rsum * series_r(dlr * dlr);
+            crl = cqr * series_r(dlr * dlr);
         } else {
-            rho_ln = sel(cr, rsum * series_r(dlr * dlr), (M.rho - I.rho) * Num<T>::rcp(dlr));
+            crl = sel(cr, cqr * series_r(dlr * dlr), (cq * (M.rho - I.rho)) * Num<T>::rcp(dlr));
         }
 
         // 1/(b2+ + b2-) and, far, 1/(2{{b}}_log) = dlb/db2 from one reciprocal
@@ -475,28 +490,51 @@ __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T
 
     // flux scalars, already multiplied by 2Q_{pp'} (momentum parts by Q, as
     // they multiply A = 2 x averaged metric)
-    const T cr = cq * rho_ln;
-    const T fr = cr * Un;                               // 2Q F_rho
-    const T gq = cr * (bsum * (M.phi - I.phi));         // Q rho_ln {{b}} [[phi]] / 2: gravity
-    const T phq = cq * (rsum * inv_bsum);               // Q p_hat, p_hat = {{rho}}/(2{{b}})
+    o.fr = crl * Un;                                    // 2Q F_rho
+    const T gq = crl * (bsum * (M.phi - I.phi));        // Q rho_ln {{b}} [[phi]] / 2: gravity
+    const T phq = cqr * inv_bsum;                       // Q p_hat, p_hat = {{rho}}/(2{{b}})
     // 1/(2 (gamma-1) {{b}}_log) - {{|u|^2}}/2 + {{phi}} + |{{u}}|^2
     const T hs = I.h + M.h;
-    const T Kf = fma(c_g2, inv_bln, fma(s3, s3, fma(s2, s2, fma(s1, s1, hs))));
-    const T fE = fma(fr, Kf, phq * Un);                 // 2Q F_E
-    const T Pi = fma(gq, I.ib, phq);  // own: pressure mean + gravity scaled at b_i
-    const T Pm = fma(gq, M.ib, -phq); // partner: -pressure mean + gravity scaled at b_m
-
-    o0 += fr;
-    o1 = fma(A0, Pi, fma(fr, s1, o1));
-    o2 = fma(A1, Pi, fma(fr, s2, o2));
-    o3 = fma(A2, Pi, fma(fr, s3, o3));
-    o4 += fE;
-    t0 = fr;  // subtracted by the receiver
-    t1 = fma(A0, Pm, -(fr * s1));
-    t2 = fma(A1, Pm, -(fr * s2));
-    t3 = fma(A2, Pm, -(fr * s3));
-    t4 = fE;  // subtracted by the receiver
+    const T Kf = fma(c_g2, inv_bln, fma(o.s3, o.s3, fma(o.s2, o.s2, fma(o.s1, o.s1, hs))));
+    o.fE = fma(o.fr, Kf, phq * Un);                     // 2Q F_E
+    o.Pi = fma(gq, I.ib, phq);   // own: pressure mean + gravity scaled at b_i
+    o.Pm = fma(gq, M.ib, -phq);  // partner: -pressure mean + gravity scaled at b_m
+    return o;
 }
+
+// One pair (i, m) of a line, evaluated once for both nodes: adds node i's
+// share 2Q_{pp'} (F + G(i,m)) to o0..o4 and returns node m's share
+// 2Q_{p'p} (F + G(m,i)) = -2Q_{pp'} (F + G(m,i)) in t0..t4; t0 and t4 are
+// returned with the opposite sign (the receiver subtracts them), which saves
+// two negations per pair.  Both shares still need the 1/w scaling of their
+// own node.
+template <typename T>
+__device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T>& M, T cq, T c_g2, T& o0, T& o1,
+                                          T& o2, T& o3, T& o4, T& t0, T& t1, T& t2, T& t3, T& t4) {
+    const PairTerms<T> p = pair_terms<T>(I, M, cq, c_g2);
+    o0 += p.fr;
+    o1 = fma(p.A0, p.Pi, fma(p.fr, p.s1, o1));
+    o2 = fma(p.A1, p.Pi, fma(p.fr, p.s2, o2));
+    o3 = fma(p.A2, p.Pi, fma(p.fr, p.s3, o3));
+    o4 += p.fE;
+    t0 = p.fr;  // subtracted by the receiver
+    t1 = fma(p.A0, p.Pm, -(p.fr * p.s1));
+    t2 = fma(p.A1, p.Pm, -(p.fr * p.s2));
+    t3 = fma(p.A2, p.Pm, -(p.fr * p.s3));
+    t4 = p.fE;  // subtracted by the receiver
+}
+
+// Whether the partner lane forms its momentum share itself from the pair's
+// scalars (fr, fE, Pm, s, A moved by shuffles: 2 FMAs per component at the
+// receiver) instead of receiving the finished share (a multiply and an FMA at
+// the sender, an add at the receiver): three FP64 operations fewer per pair
+// for four more shuffles.  For native FP64, bound by its FP64 pipe with issue
+// slots to spare; the issue-bound FP32 and float-float kernels keep the
+// finished shares.
+template <typename C>
+struct ReceiverForms {
+    static constexpr bool value = std::is_same<C, double>::value;
+};
 
 // The face contributions of node (na, nb, nc) of local element el from the
 // face phase, added to sv in the fixed order xi, eta, zeta.
@@ -580,6 +618,23 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
     }
 }
 
+// The line a lane works on in a direction phase: the lanes of a warp hold
+// 32/Nq whole lines (slot), lane position p on the line; virtual warp vwarp
+// takes lines vwarp LPW .. vwarp LPW + LPW - 1 of the CTA (element el = L/NL
+// and line L - el NL within it).  Lanes past the last line, or on an element
+// beyond e_count, return false and compute on line 0 (their results are
+// discarded).
+template <int N>
+__host__ __device__ __forceinline__ bool lane_line(int vwarp, int lane, int e_count, int& slot, int& p, int& L) {
+    using S = Shape<N>;
+    slot = lane / S::NQ;
+    p = lane - slot * S::NQ;
+    L = vwarp * S::LPW + slot;
+    const bool valid = (slot < S::LPW) && (L < S::LINES) && (L / S::NL < e_count);
+    if (!valid) L = 0;
+    return valid;
+}
+
 // One direction phase.  R = 0 (xi), 1 (eta), 2 (zeta).  FINAL = 0: add the
 // scaled sum to the shared accumulators; 1, 2, 3: add the shared
 // accumulators and store the node's result with store_node in MODE FINAL - 1
@@ -597,11 +652,8 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
     constexpr int NEAR = (S::EVEN && SplitAntipodal<C>::value) ? S::H - 1 : S::H;
 
     const int lane = threadIdx.x & 31;
-    const int slot = lane / NQ;
-    const int p = lane - slot * NQ;
-    int L = vwarp * S::LPW + slot;
-    const bool valid = (slot < S::LPW) && (L < S::LINES) && (L / S::NL < e_count);
-    if (!valid) L = 0;  // compute on element 0's first line, discard
+    int slot, p, L;
+    const bool valid = lane_line<N>(vwarp, lane, e_count, slot, p, L);
     const int el = L / S::NL;
     const int ell = L - el * S::NL;
     int ia, ib, ic;
@@ -619,22 +671,42 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         else if (R == 1) mb = pm;
         else mc = pm;
         const NodeVals<C> M = load_node<N>(sm, SL::at(el, ma, mb, mc), R);
-        C t0, t1, t2, t3, t4;
-        pair_flux<C>(I, M, cqd, c_g, acc0, acc1, acc2, acc3, acc4, t0, t1, t2, t3, t4);
-        // In-phase antipodal offset (when not split off): both nodes evaluate
-        // the pair and keep their own share -- Fig. 1(b)'s two weight-1/2
-        // evaluations summed per node.
-        if (S::EVEN && d == S::H) return;
         // the partner share goes to the lane at position p + d; this lane
         // receives from the lane at p - d
         int src = p - d;
         if (src < 0) src += NQ;
         src += slot * NQ;
-        acc0 -= shfl(t0, src);
-        acc1 += shfl(t1, src);
-        acc2 += shfl(t2, src);
-        acc3 += shfl(t3, src);
-        acc4 -= shfl(t4, src);
+        if constexpr (ReceiverForms<C>::value) {
+            const PairTerms<C> pt = pair_terms<C>(I, M, cqd, c_g);
+            acc0 += pt.fr;
+            acc1 = fma(pt.A0, pt.Pi, fma(pt.fr, pt.s1, acc1));
+            acc2 = fma(pt.A1, pt.Pi, fma(pt.fr, pt.s2, acc2));
+            acc3 = fma(pt.A2, pt.Pi, fma(pt.fr, pt.s3, acc3));
+            acc4 += pt.fE;
+            if (S::EVEN && d == S::H) return;  // in-phase antipodal offset: own share only
+            // this lane is node m of the pair evaluated by the lane at p - d:
+            // -fr, -fE, and -fr s + A Pm for the momentum
+            const C rfr = shfl(pt.fr, src), rfE = shfl(pt.fE, src), rPm = shfl(pt.Pm, src);
+            const C rs1 = shfl(pt.s1, src), rs2 = shfl(pt.s2, src), rs3 = shfl(pt.s3, src);
+            const C rA0 = shfl(pt.A0, src), rA1 = shfl(pt.A1, src), rA2 = shfl(pt.A2, src);
+            acc0 -= rfr;
+            acc1 = fma(-rfr, rs1, fma(rA0, rPm, acc1));
+            acc2 = fma(-rfr, rs2, fma(rA1, rPm, acc2));
+            acc3 = fma(-rfr, rs3, fma(rA2, rPm, acc3));
+            acc4 -= rfE;
+        } else {
+            C t0, t1, t2, t3, t4;
+            pair_flux<C>(I, M, cqd, c_g, acc0, acc1, acc2, acc3, acc4, t0, t1, t2, t3, t4);
+            // In-phase antipodal offset (when not split off): both nodes evaluate
+            // the pair and keep their own share -- Fig. 1(b)'s two weight-1/2
+            // evaluations summed per node.
+            if (S::EVEN && d == S::H) return;
+            acc0 -= shfl(t0, src);
+            acc1 += shfl(t1, src);
+            acc2 += shfl(t2, src);
+            acc3 += shfl(t3, src);
+            acc4 -= shfl(t4, src);
+        }
     };
     if constexpr (IsFF<C>::value) {
         // one copy of the (long) float-float pair evaluation: no unrolling,
@@ -767,6 +839,18 @@ __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, C* __res
         direction_lines<T, C, N, FINAL>(a, sm, e_count, node0, cq, iw, c_g, warp + rep * LA::WARPS, R);
 }
 
+// Pair k of the antipodal pass: element el, line ell, lower position p
+// (the pair is (p, p + Nq/2)); consecutive k walk a line.
+template <int N>
+__host__ __device__ __forceinline__ void antipodal_pair(int k, int& el, int& p, int& ell) {
+    constexpr int H = Shape<N>::H;
+    constexpr int PER_EL = Shape<N>::NL * H;
+    el = k / PER_EL;
+    const int kk = k - el * PER_EL;
+    p = kk % H;
+    ell = kk / H;
+}
+
 // Antipodal pairs (p, p + Nq/2) of every line of direction R, for even Nq.
 // Each node belongs to exactly one such pair per direction, so the pairs are
 // disjoint: one thread evaluates a pair once and adds both shares to the
@@ -783,11 +867,9 @@ __device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, C* __res
     constexpr int PER_EL = S::NL * H;
     C* s_acc = sm + F_ACC0 * FS;
     for (int k = threadIdx.x; k < S::EPB * PER_EL; k += Launch<N, C>::THREADS) {
-        const int el = k / PER_EL;
+        int el, p, ell;
+        antipodal_pair<N>(k, el, p, ell);
         if (el >= e_count) break;
-        const int kk = k - el * PER_EL;
-        const int p = kk % H;   // position of the lower node; consecutive threads walk a line
-        const int ell = kk / H;
         int ia, ib, ic, ja, jb, jc;
         line_node<N>(R, ell, p, ia, ib, ic);
         line_node<N>(R, ell, p + H, ja, jb, jc);
@@ -795,20 +877,22 @@ __device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, C* __res
         const int j = SL::at(el, ja, jb, jc);
         const NodeVals<C> I = load_node<N>(sm, i, R);
         const NodeVals<C> M = load_node<N>(sm, j, R);
-        C o0 = C(0.0), o1 = C(0.0), o2 = C(0.0), o3 = C(0.0), o4 = C(0.0), t0, t1, t2, t3, t4;
         const C cq = Conv<T, C>::in(T(0.5) * a.ops.Q2[p * NQ + p + H]);
-        pair_flux<C>(I, M, cq, c_g, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
+        const PairTerms<C> pt = pair_terms<C>(I, M, cq, c_g);
+        // both shares straight from the pair's scalars: fr s_k is common to
+        // node i (+fr s + A Pi) and node j (-fr s + A Pm)
+        const C x1 = pt.fr * pt.s1, x2 = pt.fr * pt.s2, x3 = pt.fr * pt.s3;
         const C iwi = Conv<T, C>::in(a.ops.invw[p]), iwj = Conv<T, C>::in(a.ops.invw[p + H]);
-        s_acc[0 * FS + i] = fma(o0, iwi, s_acc[0 * FS + i]);
-        s_acc[1 * FS + i] = fma(o1, iwi, s_acc[1 * FS + i]);
-        s_acc[2 * FS + i] = fma(o2, iwi, s_acc[2 * FS + i]);
-        s_acc[3 * FS + i] = fma(o3, iwi, s_acc[3 * FS + i]);
-        s_acc[4 * FS + i] = fma(o4, iwi, s_acc[4 * FS + i]);
-        s_acc[0 * FS + j] = fma(-t0, iwj, s_acc[0 * FS + j]);
-        s_acc[1 * FS + j] = fma(t1, iwj, s_acc[1 * FS + j]);
-        s_acc[2 * FS + j] = fma(t2, iwj, s_acc[2 * FS + j]);
-        s_acc[3 * FS + j] = fma(t3, iwj, s_acc[3 * FS + j]);
-        s_acc[4 * FS + j] = fma(-t4, iwj, s_acc[4 * FS + j]);
+        s_acc[0 * FS + i] = fma(pt.fr, iwi, s_acc[0 * FS + i]);
+        s_acc[1 * FS + i] = fma(fma(pt.A0, pt.Pi, x1), iwi, s_acc[1 * FS + i]);
+        s_acc[2 * FS + i] = fma(fma(pt.A1, pt.Pi, x2), iwi, s_acc[2 * FS + i]);
+        s_acc[3 * FS + i] = fma(fma(pt.A2, pt.Pi, x3), iwi, s_acc[3 * FS + i]);
+        s_acc[4 * FS + i] = fma(pt.fE, iwi, s_acc[4 * FS + i]);
+        s_acc[0 * FS + j] = fma(-pt.fr, iwj, s_acc[0 * FS + j]);
+        s_acc[1 * FS + j] = fma(fma(pt.A0, pt.Pm, -x1), iwj, s_acc[1 * FS + j]);
+        s_acc[2 * FS + j] = fma(fma(pt.A1, pt.Pm, -x2), iwj, s_acc[2 * FS + j]);
+        s_acc[3 * FS + j] = fma(fma(pt.A2, pt.Pm, -x3), iwj, s_acc[3 * FS + j]);
+        s_acc[4 * FS + j] = fma(-pt.fE, iwj, s_acc[4 * FS + j]);
     }
 }
 
@@ -989,21 +1073,23 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         for (int k = 0; k < 9; ++k) ja[k] = PV::in(ja_t[k]);
         const P gm1 = PV::in(a.gm1);
         const P irho = Num<P>::rcp(rho);
-        const P u1 = m1 * irho, u2 = m2 * irho, u3 = m3 * irho;
-        const P uu = fma(u3, u3, fma(u2, u2, u1 * u1));
-        P pr = perturbed ? fma(gm1, E - fma(P(0.5) * rho, uu, rho_p * phi), PV::in(pr_t))
-                         : gm1 * (E - rho * fma(P(0.5), uu, phi));
+        const P ih = P(0.5) * irho;
+        // v = u/2 (the scaling pair_terms expects) and vv = |u|^2/4
+        const P v1 = m1 * ih, v2 = m2 * ih, v3 = m3 * ih;
+        const P vv = fma(v3, v3, fma(v2, v2, v1 * v1));
+        P pr = perturbed ? fma(gm1, E - fma(P(2.0) * rho, vv, rho_p * phi), PV::in(pr_t))
+                         : gm1 * (E - rho * fma(P(2.0), vv, phi));
         if (!real) pr = P(0.5) * gm1;  // padding node: finite values, never stored
         bad |= !positive(rho) || !positive(pr);
-        // stored with the scalings pair_flux expects: u/2, b2 = 2b = rho/p,
+        // stored with the scalings pair_terms expects: u/2, b2 = 2b = rho/p,
         // ln b2, phi/8 (1/b and h = phi/2 - |u|^2/4 unscaled)
         const P b2 = rho * Num<P>::rcp(pr);
-        const P ib = P(2.0) * pr * irho;
-        const P h = fma(P(-0.25), uu, P(0.5) * phi);
+        const P ib = P(4.0) * pr * ih;
+        const P h = P(0.5) * phi - vv;
         sm[F_RHO * FS + sl] = rho;
-        sm[F_U1 * FS + sl] = P(0.5) * u1;
-        sm[F_U2 * FS + sl] = P(0.5) * u2;
-        sm[F_U3 * FS + sl] = P(0.5) * u3;
+        sm[F_U1 * FS + sl] = v1;
+        sm[F_U2 * FS + sl] = v2;
+        sm[F_U3 * FS + sl] = v3;
         sm[F_B * FS + sl] = b2;
         sm[F_INVB * FS + sl] = ib;
         sm[F_LNRHO * FS + sl] = Num<P>::log_(rho);
@@ -1021,18 +1107,22 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             with_diag = with_diag && __any_sync(__activemask(), na == 0 || na == N || nb == 0 || nb == N ||
                                                                     nc == 0 || nc == N);
         if (with_diag) {
-            const P dA = PV::in((na == 0 || na == N) ? a.ops.Q2[na * NQ + na] * a.ops.invw[na] : T(0));
-            const P dB = PV::in((nb == 0 || nb == N) ? a.ops.Q2[nb * NQ + nb] * a.ops.invw[nb] : T(0));
-            const P dC = PV::in((nc == 0 || nc == N) ? a.ops.Q2[nc * NQ + nc] * a.ops.invw[nc] : T(0));
+            // 2 D_ii of the node's position along each direction (0 inside)
+            const P dA = PV::in(a.ops.diag[na]);
+            const P dB = PV::in(a.ops.diag[nb]);
+            const P dC = PV::in(a.ops.diag[nc]);
             const P V0 = fma(dC, ja[6], fma(dB, ja[3], dA * ja[0]));
             const P V1 = fma(dC, ja[7], fma(dB, ja[4], dA * ja[1]));
             const P V2 = fma(dC, ja[8], fma(dB, ja[5], dA * ja[2]));
-            const P rU = rho * fma(u3, V2, fma(u2, V1, u1 * V0));
+            // rho U = m.V; 2 rho U multiplies v = u/2
+            const P rU = fma(m3, V2, fma(m2, V1, m1 * V0));
+            const P rU2 = P(2.0) * rU;
             f0 = rU;
-            f1 = fma(rU, u1, pr * V0);
-            f2 = fma(rU, u2, pr * V1);
-            f3 = fma(rU, u3, pr * V2);
-            f4 = rU * fma(PV::in(a.c_h), ib, P(2.0) * (phi - h));  // (E + p) U
+            f1 = fma(rU2, v1, pr * V0);
+            f2 = fma(rU2, v2, pr * V1);
+            f3 = fma(rU2, v3, pr * V2);
+            // (E + p) U = rho U (gamma/(gamma-1) p/rho + |u|^2/2 + phi)
+            f4 = rU * fma(PV::in(a.c_h), ib, fma(P(2.0), vv, phi));
         }
         sm[(F_ACC0 + 0) * FS + sl] = f0;
         sm[(F_ACC0 + 1) * FS + sl] = f1;

@@ -50,6 +50,19 @@ int esdg_selftest_ff(int op, long n, const double* x, const double* y, double* o
  * 1 (bad argument) or 4 (CUDA launch error). */
 int esdg_selftest_log(long n, const double* x, double* y, void* stream);
 
+/* Host-only check of the kernels' index arithmetic for order N on a
+ * Kx x Ky x Kz brick with per-direction boundary kinds bc[3] (0 periodic,
+ * 1 slip wall): walks the same index functions the kernels use -- shared-
+ * memory slots, the lines dealt to lanes (for every CTA fill and every
+ * precision's launch shape), the FP64 load order, the antipodal pairs, the
+ * fused kernel's face slots and neighbour traces, the face-centric surface
+ * kernel's slots -- and checks that every index is in range, that the maps
+ * meant to be bijections are, and that every node is visited exactly as
+ * often as the kernels require.  No GPU needed.  msg (may be NULL) receives
+ * the first failure.  Returns 0 (all hold), 1 (bad argument; at most 5e7
+ * nodes) or 2 (a check failed). */
+int esdg_selftest_index_maps(int N, long Kx, long Ky, long Kz, const int* bc, char* msg, int msglen);
+
 #ifdef __cplusplus
 }
 #endif

@@ -3,11 +3,15 @@
 The kernel (csrc/log_fp64.cuh) reduces x = 2^k m with m in [0.75, 1.5) to the
 nearest point F of a 1/128 grid (1/256 below 1) and evaluates
     ln x = k ln 2 + ln F + ln(1 + r),  r = (m - F)/F,
-with 1/F and ln F (lead and trail) from log_table.inc and ln(1 + r) by its
-Taylor series to r^7 (P. T. P. Tang, ACM TOMS 16(4), 1990).  These tests pin
-the committed table to 50-digit arithmetic and run the same steps in Python,
-with exactly rounded fused multiply-adds, against the host's log.  The GPU
-test of the compiled function is test_gpu_numerics.py.
+with 1/F and ln F from log_table.inc and ln(1 + r) by its Taylor series to
+r^7 (P. T. P. Tang, ACM TOMS 16(4), 1990), summed as k ln2 + (ln F + ln(1 + r))
+with ln 2 and ln F each rounded once.  The kernel uses the logarithms only in
+differences of two nodes' values, where the rounding of ln 2 cancels.  These
+tests pin the committed table to 50-digit arithmetic and run the same steps
+in Python, with exactly rounded fused multiply-adds, against 50-digit
+logarithms: the absolute value, and the difference of two of them.  The GPU
+test of the compiled function (test_gpu_numerics.py) checks it bit for bit
+against these steps.
 """
 import math
 import os
@@ -27,11 +31,8 @@ def _table():
     txt = open(INC).read()
     pairs = [(float.fromhex(a), float.fromhex(b))
              for a, b in re.findall(r"\{(-?0x[0-9a-fp.+-]+), (-?0x[0-9a-fp.+-]+)\}", txt)]
-    tail_block = txt[txt.index("kLogTail"):]
-    tail = [float.fromhex(v) for v in re.findall(r"^\s+(-?0x[0-9a-fp.+-]+),$", tail_block, re.M)]
-    hi = float.fromhex(re.search(r"kLn2Hi = (-?0x[^;]+);", txt).group(1))
-    lo = float.fromhex(re.search(r"kLn2Lo = (-?0x[^;]+);", txt).group(1))
-    return pairs, tail, hi, lo
+    ln2 = float.fromhex(re.search(r"kLn2 = (-?0x[^;]+);", txt).group(1))
+    return pairs, ln2
 
 
 def _grid_point(idx):
@@ -43,18 +44,14 @@ def _grid_point(idx):
 
 def test_table_entries_are_correctly_rounded():
     mpmath.mp.dps = 50
-    pairs, tail, hi, lo = _table()
-    assert len(pairs) == 130 and len(tail) == 130
-    for idx, ((inv_f, ln_f), ln_t) in enumerate(zip(pairs, tail)):
+    pairs, ln2 = _table()
+    assert len(pairs) == 130
+    for idx, (inv_f, ln_f) in enumerate(pairs):
         F = _grid_point(idx)
         assert inv_f == float(1 / F), idx
         assert ln_f == float(mpmath.log(F)), idx
-        # lead + trail carries ln F to ~106 bits
-        assert abs(mpmath.mpf(ln_f) + mpmath.mpf(ln_t) - mpmath.log(F)) <= mpmath.mpf(2) ** -100, idx
-    ln2 = mpmath.log(2)
-    assert hi == float(mpmath.floor(ln2 * 2 ** 42) / 2 ** 42)
-    assert hi * 2 ** 42 == int(hi * 2 ** 42)  # k ln2_hi exact for |k| < 2^11
-    assert abs(mpmath.mpf(hi) + mpmath.mpf(lo) - ln2) < mpmath.mpf(2) ** -95
+    assert ln2 == float(mpmath.log(2))
+    assert abs(mpmath.mpf(ln2) - mpmath.log(2)) < mpmath.mpf(2) ** -55
 
 
 def _fma(a, b, c):
@@ -71,7 +68,7 @@ def _from_hilo(hi, lo):
     return struct.unpack("<d", struct.pack("<Q", ((hi & 0xFFFFFFFF) << 32) | (lo & 0xFFFFFFFF)))[0]
 
 
-def _log_steps(x, pairs, tail, ln2_hi, ln2_lo):
+def log_steps(x, pairs, ln2):
     """The kernel's steps, integer manipulations included, in Python."""
     hi, lo = _hilo(x)
     mant = hi & 0x000FFFFF
@@ -81,7 +78,6 @@ def _log_steps(x, pairs, tail, ln2_hi, ln2_lo):
     m = _from_hilo(ebits | mant, lo)
     F = _from_hilo(ebits + (j << 13), 0)
     inv_f, ln_f = pairs[j + half]
-    ln_t = tail[j + half]
     k = ((hi >> 20) & 0x7FF) - 1023 + half
     kd = _from_hilo(0x43300000, k + 1024) - 4503599627371520.0
     assert kd == k
@@ -95,29 +91,68 @@ def _log_steps(x, pairs, tail, ln2_hi, ln2_lo):
     q = _fma(q, r, 1.0 / 3.0)
     q = _fma(q, r, -0.5)
     p = _fma(r2, q, r)
-    return _fma(kd, ln2_hi, ln_f) + (_fma(kd, ln2_lo, p) + ln_t)
+    return _fma(kd, ln2, ln_f + p), k
 
 
-def test_method_within_one_ulp_of_host_log():
-    pairs, tail, hi, lo = _table()
-    rng = np.random.default_rng(5)
-    xs = np.concatenate([
-        np.exp(rng.uniform(np.log(1e-300), np.log(1e300), 1500)),
-        1.0 + rng.uniform(-2.0 ** -8, 2.0 ** -8, 500),   # around 1: relative accuracy
-        rng.uniform(0.75, 1.0, 400),                      # halved branch, ln F < 0
-        rng.uniform(0.97, 1.03, 400),                     # cancellation of ln F against ln(1 + r)
-        0.75 * (1.0 + rng.uniform(-1e-6, 1e-6, 100)),     # reduction boundaries
-        1.5 * (1.0 + rng.uniform(-1e-6, 1e-6, 100)),
+def sample_points(rng, n=1):
+    return np.concatenate([
+        np.exp(rng.uniform(np.log(1e-300), np.log(1e300), 1500 * n)),
+        1.0 + rng.uniform(-2.0 ** -8, 2.0 ** -8, 500 * n),   # around 1: relative accuracy
+        rng.uniform(0.75, 1.0, 400 * n),                      # halved branch, ln F < 0
+        rng.uniform(0.97, 1.03, 400 * n),                     # ln F against ln(1 + r)
+        0.75 * (1.0 + rng.uniform(-1e-6, 1e-6, 100 * n)),     # reduction boundaries
+        1.5 * (1.0 + rng.uniform(-1e-6, 1e-6, 100 * n)),
         1.0 + np.arange(-50, 51) * 2.0 ** -52,
-        rng.uniform(1e-6, 1e-4, 200),                     # 2b = rho/p of the workloads
+        rng.uniform(1e-6, 1e-4, 200 * n),                     # 2b = rho/p of the workloads
+        rng.uniform(0.01, 2.0, 200 * n),                      # densities
     ])
+
+
+def _ulp(x):
+    return float(np.spacing(abs(x)))
+
+
+def test_method_absolute_error():
+    """|L(x) - ln x| <= half an ulp of the result + |k| 2^-55 + 2^-54 (the
+    roundings of ln 2, ln F and the inner sum)."""
+    mpmath.mp.dps = 50
+    pairs, ln2 = _table()
+    rng = np.random.default_rng(5)
+    worst = 0.0
+    for x in sample_points(rng):
+        x = float(x)
+        y, k = log_steps(x, pairs, ln2)
+        ref = mpmath.log(mpmath.mpf(x))
+        if x == 1.0:
+            assert y == 0.0
+            continue
+        err = abs(mpmath.mpf(y) - ref)
+        bound = 0.5 * _ulp(y) + abs(k) * 2.0 ** -55 + 2.0 ** -54
+        worst = max(worst, float(err / bound))
+    assert worst <= 1.0, worst
+
+
+def test_method_differences_within_one_ulp():
+    """The kernel's use: ln a+ - ln a- for two nodes.  Pairs at the relative
+    distances of neighbouring nodes (1e-12 .. 0.5) and across powers of two:
+    |L(y) - L(x) - ln(y/x)| <= one ulp of the larger result, plus |k_y - k_x|
+    2^-55 when the two straddle a power of two, plus the roundings of ln F and
+    the inner sums (2^-53)."""
+    mpmath.mp.dps = 50
+    pairs, ln2 = _table()
+    rng = np.random.default_rng(6)
+    xs = sample_points(rng)
     worst = 0.0
     for x in xs:
         x = float(x)
-        y = _log_steps(x, pairs, tail, hi, lo)
-        ref = math.log(x)
-        if ref == 0.0:
-            assert y == 0.0
-            continue
-        worst = max(worst, abs(y - ref) / np.spacing(abs(ref)))
+        for rel in (1e-12, 1e-6, 3e-3, 0.02, 0.3):
+            y = x * (1.0 + rel * rng.uniform(-1.0, 1.0))
+            if not (0.0 < y < 1.7e308):
+                continue
+            lx, kx = log_steps(x, pairs, ln2)
+            ly, ky = log_steps(y, pairs, ln2)
+            ref = mpmath.log(mpmath.mpf(y)) - mpmath.log(mpmath.mpf(x))
+            err = abs(mpmath.mpf(ly) - mpmath.mpf(lx) - ref)
+            bound = max(_ulp(lx), _ulp(ly)) + abs(ky - kx) * 2.0 ** -55 + 2.0 ** -53
+            worst = max(worst, float(err / bound))
     assert worst <= 1.0, worst
