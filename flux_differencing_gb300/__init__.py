@@ -15,7 +15,7 @@ import threading
 import numpy as np
 
 __all__ = [
-    "ESDG_OK", "ESDG_FP64", "ESDG_FP32", "ESDG_FP64_FF", "ESDG_FORM_2D", "ESDG_FORM_SKEW", "ESDG_STATUS_NONPHYSICAL",
+    "ESDG_OK", "ESDG_FP64", "ESDG_FP32", "ESDG_FP64_FF", "ESDG_FORM_2D", "ESDG_FORM_SKEW", "ESDG_STATUS_NONPHYSICAL", "ESDG_STATUS_INDEX",
     "EsdgError", "library_path", "load_library", "operators", "pair_schedule", "VolumeOperator",
 ]
 
@@ -25,12 +25,14 @@ ESDG_FP64, ESDG_FP32, ESDG_FP64_FF = 0, 1, 2
 _PRECISIONS = {"fp64": ESDG_FP64, "fp32": ESDG_FP32, "fp64ff": ESDG_FP64_FF}
 ESDG_FORM_2D, ESDG_FORM_SKEW = 0, 1
 ESDG_STATUS_NONPHYSICAL = 1
+ESDG_STATUS_INDEX = 4  # debug library only: a kernel index was out of range
 
 _ERRNAMES = {1: "ESDG_ERR_ARG", 2: "ESDG_ERR_UNSUPPORTED", 3: "ESDG_ERR_ALIGN", 4: "ESDG_ERR_CUDA",
              5: "ESDG_ERR_STATE"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
+_lib_debug = None
 _lock = threading.Lock()
 
 # every symbol include/esdg.h declares, with its ctypes signature
@@ -84,21 +86,24 @@ class EsdgError(RuntimeError):
         self.code = code
 
 
-def library_path() -> str:
+def library_path(debug: bool = False) -> str:
+    if debug:
+        return os.path.join(_HERE, "_build_debug", "libesdg_debug.so")
     return os.path.join(_HERE, "_build", "libesdg.so")
 
 
-def load_library(build_if_missing: bool = False):
-    """Load libesdg.so.  Raises if it is missing (no CPU fallback exists)."""
-    global _lib
+def load_library(build_if_missing: bool = False, debug: bool = False):
+    """Load libesdg.so (debug=True: libesdg_debug.so, the kernels with their index
+    checks compiled in).  Raises if it is missing (no CPU fallback exists)."""
+    global _lib, _lib_debug
     with _lock:
-        if _lib is not None:
-            return _lib
-        path = library_path()
-        if not os.path.exists(path):
+        if (_lib_debug if debug else _lib) is not None:
+            return _lib_debug if debug else _lib
+        path = library_path(debug)
+        if not os.path.exists(path) or (debug and build_if_missing):
             if build_if_missing:
                 from . import build as _build
-                _build.build()
+                _build.build(debug=debug)
             else:
                 raise RuntimeError(
                     f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
@@ -108,13 +113,20 @@ def load_library(build_if_missing: bool = False):
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
-        _lib = lib
+        if debug:
+            _lib_debug = lib
+        else:
+            _lib = lib
         return lib
 
 
-def _check(rc: int, h=None):
+def _chk(op, rc: int, h=None):
+    _check(rc, h, op.lib)
+
+
+def _check(rc: int, h=None, lib=None):
     if rc != ESDG_OK:
-        lib = load_library()
+        lib = lib or load_library()
         msg = lib.esdg_last_error(h).decode()
         raise EsdgError(rc, msg)
 
@@ -152,7 +164,7 @@ class Pipeline:
         self.op = op
         self.lib = op.lib
         p = ctypes.c_void_p()
-        _check(self.lib.esdg_pipeline_create(op.h, int(depth), ctypes.byref(p)))
+        _chk(self, self.lib.esdg_pipeline_create(op.h, int(depth), ctypes.byref(p)))
         self.p = p
         self.depth = int(depth)
 
@@ -217,9 +229,9 @@ class VolumeOperator:
     """
 
     def __init__(self, Kx: int, Ky: int, Kz: int, N: int, precision: str = "fp64", form: str = "2d",
-                 gamma: float = 1.4, bc=(0, 0, 0), dissipation: bool = True):
+                 gamma: float = 1.4, bc=(0, 0, 0), dissipation: bool = True, debug: bool = False):
         import torch
-        self.lib = load_library()
+        self.lib = load_library(build_if_missing=debug, debug=debug)
         self.Kx, self.Ky, self.Kz, self.N = int(Kx), int(Ky), int(Kz), int(N)
         self.K = self.Kx * self.Ky * self.Kz
         self.n = self.K * (self.N + 1) ** 3
@@ -228,21 +240,21 @@ class VolumeOperator:
         prec = _PRECISIONS[precision]
         frm = {"2d": ESDG_FORM_2D, "skew": ESDG_FORM_SKEW}[form]
         h = ctypes.c_void_p()
-        _check(self.lib.esdg_create(ctypes.byref(h), self.Kx, self.Ky, self.Kz, self.N, prec, frm))
+        _chk(self, self.lib.esdg_create(ctypes.byref(h), self.Kx, self.Ky, self.Kz, self.N, prec, frm))
         self.h = h
         if gamma != 1.4:
-            _check(self.lib.esdg_set_params(self.h, float(gamma)), self.h)
+            _chk(self, self.lib.esdg_set_params(self.h, float(gamma)), self.h)
         self.set_boundary(*bc)
         self.set_dissipation(dissipation)
 
     def set_boundary(self, bc_xi: int = 0, bc_eta: int = 0, bc_zeta: int = 0):
         """Surface-term boundary kind per reference direction: 0 periodic, 1 slip wall."""
-        _check(self.lib.esdg_set_boundary(self.h, int(bc_xi), int(bc_eta), int(bc_zeta)), self.h)
+        _chk(self, self.lib.esdg_set_boundary(self.h, int(bc_xi), int(bc_eta), int(bc_zeta)), self.h)
         self.bc = (int(bc_xi), int(bc_eta), int(bc_zeta))
 
     def set_dissipation(self, on: bool = True):
         """Surface flux with (default) or without the matrix dissipation."""
-        _check(self.lib.esdg_set_dissipation(self.h, int(bool(on))), self.h)
+        _chk(self, self.lib.esdg_set_dissipation(self.h, int(bool(on))), self.h)
         self.dissipation = bool(on)
 
     def close(self):
@@ -272,7 +284,7 @@ class VolumeOperator:
         self._req(metrics_out, 9 * self.n, name="metrics_out")
         if J_out is not None:
             self._req(J_out, self.n, name="J_out")
-        _check(self.lib.esdg_set_geometry(self.h, _dptr(x), _dptr(y), _dptr(z), _dptr(metrics_out),
+        _chk(self, self.lib.esdg_set_geometry(self.h, _dptr(x), _dptr(y), _dptr(z), _dptr(metrics_out),
                                           _dptr(J_out) if J_out is not None else None, _stream_ptr(stream)),
                self.h)
         return metrics_out
@@ -304,7 +316,7 @@ class VolumeOperator:
         self._req(metrics, 9 * self.n, name="metrics")
         self._req(phi, self.n, name="phi")
         self._req(out, 5 * self.n, name="out")
-        _check(self.lib.esdg_surface_rhs(self.h, _dptr(q), _dptr(metrics), _dptr(phi), _dptr(out),
+        _chk(self, self.lib.esdg_surface_rhs(self.h, _dptr(q), _dptr(metrics), _dptr(phi), _dptr(out),
                                          _stream_ptr(stream)), self.h)
         return out
 
@@ -317,20 +329,20 @@ class VolumeOperator:
         if rho_ref is not None:
             self._req(rho_ref, self.n, name="rho_ref")
             self._req(p_ref, self.n, name="p_ref")
-        _check(self.lib.esdg_set_reference(self.h, _dptr(rho_ref) if rho_ref is not None else None,
+        _chk(self, self.lib.esdg_set_reference(self.h, _dptr(rho_ref) if rho_ref is not None else None,
                                            _dptr(p_ref) if p_ref is not None else None), self.h)
         self._reference = (rho_ref, p_ref)
 
     def set_coriolis(self, f: float = 0.0):
         """f-plane Coriolis parameter (s^-1) of the time-stepping source h."""
-        _check(self.lib.esdg_set_coriolis(self.h, float(f)), self.h)
+        _chk(self, self.lib.esdg_set_coriolis(self.h, float(f)), self.h)
         self.coriolis = float(f)
 
     def rk_stage(self, q, dq, rhs, J, a: float, b: float, dt: float, stream=None):
         """dq <- a dq + dt (h - rhs/J); q <- q + b dq (in place)."""
         for t, nm, k in ((q, "q", 5), (dq, "dq", 5), (rhs, "rhs", 5), (J, "J", 1)):
             self._req(t, k * self.n, name=nm)
-        _check(self.lib.esdg_rk_stage(self.h, _dptr(q), _dptr(dq), _dptr(rhs), _dptr(J), float(a), float(b),
+        _chk(self, self.lib.esdg_rk_stage(self.h, _dptr(q), _dptr(dq), _dptr(rhs), _dptr(J), float(a), float(b),
                                       float(dt), _stream_ptr(stream)), self.h)
 
     def lsrk_step(self, q, dq, rhs, metrics, phi, J, dt: float, stream=None):
@@ -338,7 +350,7 @@ class VolumeOperator:
         for t, nm, k in ((q, "q", 5), (dq, "dq", 5), (rhs, "rhs", 5), (metrics, "metrics", 9),
                          (phi, "phi", 1), (J, "J", 1)):
             self._req(t, k * self.n, name=nm)
-        _check(self.lib.esdg_lsrk_step(self.h, _dptr(q), _dptr(dq), _dptr(rhs), _dptr(metrics), _dptr(phi),
+        _chk(self, self.lib.esdg_lsrk_step(self.h, _dptr(q), _dptr(dq), _dptr(rhs), _dptr(metrics), _dptr(phi),
                                        _dptr(J), float(dt), _stream_ptr(stream)), self.h)
 
     def diagnostics(self, q, J, phi, out=None, stream=None):
@@ -351,7 +363,7 @@ class VolumeOperator:
             out = torch.empty(3, dtype=torch.float64, device=q.device)
         if not (out.is_cuda and out.dtype == torch.float64 and out.numel() >= 3):
             raise ValueError("out: need a CUDA float64 tensor of at least 3 values")
-        _check(self.lib.esdg_diagnostics(self.h, _dptr(q), _dptr(J), _dptr(phi), _dptr(out),
+        _chk(self, self.lib.esdg_diagnostics(self.h, _dptr(q), _dptr(J), _dptr(phi), _dptr(out),
                                          _stream_ptr(stream)), self.h)
         return out
 
@@ -364,12 +376,12 @@ class VolumeOperator:
         if out is None:
             out = torch.empty((5, self.n), dtype=self.dtype, device=q.device)
         self._req(out, 5 * self.n, name="out")
-        _check(self.lib.esdg_rhs(self.h, _dptr(q), _dptr(metrics), _dptr(phi), _dptr(out), _stream_ptr(stream)),
+        _chk(self, self.lib.esdg_rhs(self.h, _dptr(q), _dptr(metrics), _dptr(phi), _dptr(out), _stream_ptr(stream)),
                self.h)
         return out
 
     def status(self, stream=None) -> int:
         """Read and clear the status word (synchronises the stream)."""
         v = ctypes.c_uint(0)
-        _check(self.lib.esdg_get_status(self.h, ctypes.byref(v), _stream_ptr(stream)), self.h)
+        _chk(self, self.lib.esdg_get_status(self.h, ctypes.byref(v), _stream_ptr(stream)), self.h)
         return v.value

@@ -17,6 +17,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libesdg.so")
+# Debug variant: the same sources with -DESDG_DEBUG_CHECKS=1 (every kernel index
+# range-checked into ESDG_STATUS_INDEX, shared memory poisoned with NaN before
+# use), for the tests only.
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libesdg_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
@@ -65,17 +70,20 @@ def _stale(target: str) -> bool:
     return any(os.path.getmtime(s) > t for s in _sources())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, jobs: int | None = None) -> str:
-    """Compile and link libesdg.so; returns its path."""
-    if not force and not ptxas_info and not _stale(LIB):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, jobs: int | None = None,
+          debug: bool = False) -> str:
+    """Compile and link libesdg.so (or, with debug=True, libesdg_debug.so with the
+    kernels' index checks compiled in); returns its path."""
+    lib_path, build_dir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and not ptxas_info and not _stale(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DESDG_DEBUG_CHECKS=1"] if debug else [])
 
     def compile_one(u):
         name, src, defs = u
-        obj = os.path.join(BUILD, name + ".o")
+        obj = os.path.join(build_dir, name + ".o")
         cmd = [nvcc, "-c", src, "-o", obj] + NVCC_FLAGS + defs + extra
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -89,19 +97,19 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, 
         results = list(ex.map(compile_one, units))
     objs = [r[0] for r in results]
     logs = [r[1] for r in results]
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "shared"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     if verbose or ptxas_info:
         for u, log in zip(units, logs):
             if log.strip():
                 sys.stdout.write(f"== {u[0]}\n{log}")
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -10,7 +10,46 @@
 #include "floatfloat.cuh"
 #include "log_fp64.cuh"
 
+// Debug builds (compiled with -DESDG_DEBUG_CHECKS=1 into a library of their
+// own, libesdg_debug.so) range-check every computed shared-memory, face-slot
+// and global index of the volume and surface kernels and poison shared memory
+// before the kernels fill it; release builds compile both to nothing.
+#ifndef ESDG_DEBUG_CHECKS
+#define ESDG_DEBUG_CHECKS 0
+#endif
+
 namespace esdg {
+
+constexpr unsigned kStatusIndex = 4u;  // ESDG_STATUS_INDEX of esdg.h
+
+// Debug builds: an index outside [0, hi) sets ESDG_STATUS_INDEX in the status
+// word and is replaced by 0, so that the access stays in bounds and the kernel
+// runs to its end (nothing traps).  Release builds return i unchanged.
+template <typename I>
+__device__ __forceinline__ I checked(I i, long long hi, unsigned* status) {
+#if ESDG_DEBUG_CHECKS
+    if (i < 0 || static_cast<long long>(i) >= hi) {
+        atomicOr(status, kStatusIndex);
+        return I(0);
+    }
+#endif
+    (void)hi;
+    (void)status;
+    return i;
+}
+
+// Debug builds: fill `bytes` of shared memory with all-ones words, a NaN in
+// FP32 and in FP64, so that a read of a slot no phase has written shows up as
+// NaN in the output.  Called by every thread of the CTA; ends with a barrier.
+__device__ __forceinline__ void poison_shared(void* p, size_t bytes) {
+#if ESDG_DEBUG_CHECKS
+    unsigned* w = static_cast<unsigned*>(p);
+    for (size_t k = threadIdx.x; k < bytes / 4; k += blockDim.x) w[k] = 0xffffffffu;
+    __syncthreads();
+#endif
+    (void)p;
+    (void)bytes;
+}
 
 template <typename T>
 struct Num;
@@ -45,10 +84,9 @@ struct Num<float> {
         asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
         return r;
     }
-    // |d| < 0.2 (0x3E4CCCCD)
-    static __device__ __forceinline__ bool close(float d) {
-        return (__float_as_uint(d) & 0x7fffffffu) < 0x3E4CCCCDu;
-    }
+    // |d| < 0.2: one compare with an absolute-value operand (the issue-bound
+    // FP32 kernel counts instructions, not pipes)
+    static __device__ __forceinline__ bool close(float d) { return fabsf(d) < 0.2f; }
     static __device__ __forceinline__ float log_(float x) { return logf(x); }
     // |f| < 0.1 (0x3DCCCCCD), i.e. |ln a+ - ln a-| < 2 atanh(0.1) ~ 0.2
     static __device__ __forceinline__ bool close_ratio(float f) {

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(256, SurfaceOccupancy<C>::value) surface_kerne
 
     const bool perturbed = a.rho_ref != nullptr;
     T qi[5], phii, ni[3], ri[2];
-    const long long gi = e * NP3 + face_node<N, DIR>(plus_face ? N : 0, s1, s2);
+    const long long gi = checked(e * NP3 + face_node<N, DIR>(plus_face ? N : 0, s1, s2), a.n, a.status);
     load_node(a, gi, DIR, qi, phii, ni, ri);
     const FaceNode<C> I = node_from<T, C>(qi, phii, ri, k.gm1, perturbed);
     bool bad = !positive(I.rho) || !positive(I.p);
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256, SurfaceOccupancy<C>::value) surface_kerne
     const bool interior = plus_face && (er + 1 < Kd[DIR] || !wall_dir);
     if (interior) {
         const long long ej = (er + 1 < Kd[DIR]) ? e + stride : e - (Kd[DIR] - 1) * stride;
-        const long long gj = ej * NP3 + face_node<N, DIR>(0, s1, s2);
+        const long long gj = checked(ej * NP3 + face_node<N, DIR>(0, s1, s2), a.n, a.status);
         T qj[5], phij, nj[3], rj[2];
         load_node(a, gj, DIR, qj, phij, nj, rj);
         const FaceNode<C> J = node_from<T, C>(qj, phij, rj, k.gm1, perturbed);

@@ -430,8 +430,9 @@ __device__ __forceinline__ PairTerms<T> pair_terms(const NodeVals<T>& I, const N
         const T rr = Num<T>::rcp(sel(cr, rsum, dlr));
         const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
         const T ur = tr * tr;
-        // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945)
-        const T polr = fma(ur, fma(ur, fma(ur, T(-22.0 / 945.0), T(-2.0 / 45.0)), T(-1.0 / 6.0)), T(0.5));
+        // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945 - ...); |f| < 0.1
+        // (u < 0.01), so the u^3 term (below 5e-8 relative) is left out
+        const T polr = fma(ur, fma(ur, T(-2.0 / 45.0), T(-1.0 / 6.0)), T(0.5));
         crl = sel(cr, cqr * polr, cq * tr);
 
         // 1/(b2+ + b2-) and the inverse log mean from one reciprocal
@@ -441,8 +442,9 @@ __device__ __forceinline__ PairTerms<T> pair_terms(const NodeVals<T>& I, const N
         inv_bsum = sel(cb, rb, db * rb);
         const T fb = db * inv_bsum;
         const T ub = fb * fb;
-        // 1/(2{{b}}_log) = (1/bsum2)(2 + 2u/3 + 2u^2/5 + 2u^3/7), f = db/bsum
-        const T polb = fma(ub, fma(ub, fma(ub, T(2.0 / 7.0), T(2.0 / 5.0)), T(2.0 / 3.0)), T(2.0));
+        // 1/(2{{b}}_log) = (1/bsum2)(2 + 2u/3 + 2u^2/5 + 2u^3/7 + ...), f = db/bsum;
+        // the u^3 term is below 1.5e-7 relative for u < 0.01 and left out
+        const T polb = fma(ub, fma(ub, T(2.0 / 5.0), T(2.0 / 3.0)), T(2.0));
         inv_bln = sel(cb, inv_bsum * polb, dlb * (bsum * rb));
     } else {
         // Log means from the per-node logarithms: far, (a+ - a-)/(ln a+ - ln a-);
@@ -539,9 +541,11 @@ struct ReceiverForms {
 // The face contributions of node (na, nb, nc) of local element el from the
 // face phase, added to sv in the fixed order xi, eta, zeta.
 template <typename T, int N>
-__device__ __forceinline__ void face_sum(const T* __restrict__ fb, int el, int na, int nb, int nc, T (&sv)[5]) {
+__device__ __forceinline__ void face_sum(const T* __restrict__ fb, int el, int na, int nb, int nc, T (&sv)[5],
+                                         unsigned* status) {
     using FSL = FaceSlots<N>;
     auto add_slot = [&](int sl) {
+        sl = checked(sl, FSL::COUNT, status);
 #pragma unroll
         for (int v = 0; v < 5; ++v) sv[v] += fb[v * FSL::COUNT + sl];
     };
@@ -567,7 +571,7 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
         T* __restrict__ o = a.out;
         if constexpr (FUSED) {
             T sv[5] = {T(0), T(0), T(0), T(0), T(0)};
-            face_sum<T, N>(fb, el, na, nb, nc, sv);
+            face_sum<T, N>(fb, el, na, nb, nc, sv, a.status);
             t0 += sv[0];
             t1 += sv[1];
             t2 += sv[2];
@@ -597,7 +601,7 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
         dqv[v] = use_dq ? dqp[v * n + g] : T(0);
         sv[v] = (!FUSED && face) ? Sp[v * n + g] : T(0);
     }
-    if constexpr (FUSED) face_sum<T, N>(fb, el, na, nb, nc, sv);
+    if constexpr (FUSED) face_sum<T, N>(fb, el, na, nb, nc, sv, a.status);
     const T Jg = a.rk_J[g];
     const T sc = -a.rk_dt * Num<T>::rcp(Jg);
     const T tot[5] = {t0, t1, t2, t3, t4};
@@ -615,6 +619,20 @@ __device__ __forceinline__ void store_node(const VolumeArgs<T>& a, long long g, 
         dqp[v * n + g] = d;
         qo[v * n + g] = fma(a.rk_B, d, qv[v]);
         if (!FUSED && face) Sp[v * n + g] = T(0);
+    }
+}
+
+// (p + d) mod Nq for line positions p and offsets -Nq < d < Nq: a mask when
+// Nq is a power of two (N = 1, 3, 7), a compare and correction otherwise.
+template <int NQ>
+__host__ __device__ __forceinline__ int wrap_pos(int p, int d) {
+    if constexpr ((NQ & (NQ - 1)) == 0) {
+        return (p + d) & (NQ - 1);
+    } else {
+        int q = p + d;
+        if (q >= NQ) q -= NQ;
+        if (q < 0) q += NQ;
+        return q;
     }
 }
 
@@ -658,24 +676,21 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
     const int ell = L - el * S::NL;
     int ia, ib, ic;
     line_node<N>(R, ell, p, ia, ib, ic);
-    const int i = SL::at(el, ia, ib, ic);
+    const int i = checked(SL::at(el, ia, ib, ic), FS, a.status);
     const NodeVals<C> I = load_node<N>(sm, i, R);
 
     C acc0 = C(0.0), acc1 = C(0.0), acc2 = C(0.0), acc3 = C(0.0), acc4 = C(0.0);
 
     auto offset = [&](int d, C cqd) {
-        int pm = p + d;
-        if (pm >= NQ) pm -= NQ;
+        const int pm = wrap_pos<NQ>(p, d);
         int ma = ia, mb = ib, mc = ic;
         if (R == 0) ma = pm;
         else if (R == 1) mb = pm;
         else mc = pm;
-        const NodeVals<C> M = load_node<N>(sm, SL::at(el, ma, mb, mc), R);
+        const NodeVals<C> M = load_node<N>(sm, checked(SL::at(el, ma, mb, mc), FS, a.status), R);
         // the partner share goes to the lane at position p + d; this lane
         // receives from the lane at p - d
-        int src = p - d;
-        if (src < 0) src += NQ;
-        src += slot * NQ;
+        const int src = wrap_pos<NQ>(p, -d) + slot * NQ;
         if constexpr (ReceiverForms<C>::value) {
             const PairTerms<C> pt = pair_terms<C>(I, M, cqd, c_g);
             acc0 += pt.fr;
@@ -712,11 +727,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         // one copy of the (long) float-float pair evaluation: no unrolling,
         // the offset's 2Q/8 read from the operator table each time
 #pragma unroll 1
-        for (int d = 1; d <= NEAR; ++d) {
-            int pm = p + d;
-            if (pm >= NQ) pm -= NQ;
-            offset(d, Conv<T, C>::in(T(0.5) * a.ops.Q2[p * NQ + pm]));
-        }
+        for (int d = 1; d <= NEAR; ++d) offset(d, Conv<T, C>::in(T(0.5) * a.ops.Q2[p * NQ + wrap_pos<NQ>(p, d)]));
     } else if constexpr (PackPairs<C, N>::value) {
         // offsets d and d + 1 in the two halves of packed FP32 operands: one
         // issue slot for two evaluations' arithmetic
@@ -725,37 +736,34 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         p2 o0(0.0), o1(0.0), o2(0.0), o3(0.0), o4(0.0);
 #pragma unroll
         for (int d = 1; d + 1 <= NEAR; d += 2) {
-            int pm = p + d;
-            if (pm >= NQ) pm -= NQ;
-            int pn = pm + 1;
-            if (pn >= NQ) pn -= NQ;
+            const int pm = wrap_pos<NQ>(p, d);
+            const int pn = wrap_pos<NQ>(p, d + 1);
             int ma = ia, mb = ib, mc = ic, na = ia, nb = ib, nc = ic;
             if (R == 0) { ma = pm; na = pn; }
             else if (R == 1) { mb = pm; nb = pn; }
             else { mc = pm; nc = pn; }
-            const NodeVals<p2> M = pack_vals(load_node<N>(sm, SL::at(el, ma, mb, mc), R),
-                                             load_node<N>(sm, SL::at(el, na, nb, nc), R));
+            const NodeVals<p2> M = pack_vals(load_node<N>(sm, checked(SL::at(el, ma, mb, mc), FS, a.status), R),
+                                             load_node<N>(sm, checked(SL::at(el, na, nb, nc), FS, a.status), R));
             p2 t0, t1, t2, t3, t4;
             pair_flux<p2>(I2, M, p2(cq[d - 1], cq[d]), cg2, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
             // partner shares: half x to the lane at p + d, half y to p + d + 1
-            // (none for the in-phase antipodal offset of even Nq)
-            int src = p - d;
-            if (src < 0) src += NQ;
-            src += slot * NQ;
-            acc0 -= shfl(t0.v.x, src);
-            acc1 += shfl(t1.v.x, src);
-            acc2 += shfl(t2.v.x, src);
-            acc3 += shfl(t3.v.x, src);
-            acc4 -= shfl(t4.v.x, src);
+            // (none for the in-phase antipodal offset of even Nq); when both
+            // halves are received they are added to the packed accumulators
+            // (one packed add per component instead of two)
+            const int src = wrap_pos<NQ>(p, -d) + slot * NQ;
             if (!(S::EVEN && d + 1 == S::H)) {
-                int src2 = p - d - 1;
-                if (src2 < 0) src2 += NQ;
-                src2 += slot * NQ;
-                acc0 -= shfl(t0.v.y, src2);
-                acc1 += shfl(t1.v.y, src2);
-                acc2 += shfl(t2.v.y, src2);
-                acc3 += shfl(t3.v.y, src2);
-                acc4 -= shfl(t4.v.y, src2);
+                const int src2 = wrap_pos<NQ>(p, -d - 1) + slot * NQ;
+                o0 = o0 - p2(shfl(t0.v.x, src), shfl(t0.v.y, src2));
+                o1 += p2(shfl(t1.v.x, src), shfl(t1.v.y, src2));
+                o2 += p2(shfl(t2.v.x, src), shfl(t2.v.y, src2));
+                o3 += p2(shfl(t3.v.x, src), shfl(t3.v.y, src2));
+                o4 = o4 - p2(shfl(t4.v.x, src), shfl(t4.v.y, src2));
+            } else {
+                acc0 -= shfl(t0.v.x, src);
+                acc1 += shfl(t1.v.x, src);
+                acc2 += shfl(t2.v.x, src);
+                acc3 += shfl(t3.v.x, src);
+                acc4 -= shfl(t4.v.x, src);
             }
         }
         if constexpr (NEAR % 2 == 1) offset(NEAR, cq[NEAR - 1]);
@@ -782,7 +790,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
         // xi phase: lines of a warp are consecutive (b, c) rows, so the block-
         // linear node L*Nq + p is contiguous across lanes: coalesced stores
         static_assert(Layout<N>::ORD0 == 0, "xi lines must be dealt b-fastest");
-        const long long g = node0 + (long long)L * NQ + p;
+        const long long g = checked(node0 + (long long)L * NQ + p, a.n, a.status);
         store_node<T, N, FINAL - 1>(a, g, ia, ib, ic, el, reinterpret_cast<const T*>(sm + F_COUNT * FS),
                                      Conv<T, C>::out(fma(acc0, iw, s_acc[0 * FS + i])),
                          Conv<T, C>::out(fma(acc1, iw, s_acc[1 * FS + i])),
@@ -873,8 +881,8 @@ __device__ __forceinline__ void antipodal_phase(const VolumeArgs<T>& a, C* __res
         int ia, ib, ic, ja, jb, jc;
         line_node<N>(R, ell, p, ia, ib, ic);
         line_node<N>(R, ell, p + H, ja, jb, jc);
-        const int i = SL::at(el, ia, ib, ic);
-        const int j = SL::at(el, ja, jb, jc);
+        const int i = checked(SL::at(el, ia, ib, ic), FS, a.status);
+        const int j = checked(SL::at(el, ja, jb, jc), FS, a.status);
         const NodeVals<C> I = load_node<N>(sm, i, R);
         const NodeVals<C> M = load_node<N>(sm, j, R);
         const C cq = Conv<T, C>::in(T(0.5) * a.ops.Q2[p * NQ + p + H]);
@@ -923,7 +931,7 @@ __device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict
         int el, dir, side, i1, i2, na, nb, nc;
         FSL::decode(s, el, dir, side, i1, i2);
         FSL::node(dir, side ? N : 0, i1, i2, na, nb, nc);
-        const int sl = SL::at(el, na, nb, nc);
+        const int sl = checked(SL::at(el, na, nb, nc), FS, a.status);
         FaceNode<C> I;
         I.rho = sm[F_RHO * FS + sl];
         I.u1 = C(2) * sm[F_U1 * FS + sl];
@@ -980,6 +988,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     C* sm = reinterpret_cast<C*>(smem_raw);
     using CV = Conv<T, C>;
+    poison_shared(smem_raw, volume_smem_bytes<C, N, MODE>());  // debug builds only
 
     const long long e0 = a.e_begin + (long long)blockIdx.x * S::EPB;
     const long long rem = a.e_end - e0;
@@ -1020,6 +1029,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             FSL::decode(s, el, dir, side, i1, i2);
             long long g;
             if (face_neighbour<N>(nbr, el, dir, side, i1, i2, g)) {
+                g = checked(g, a.n, a.status);
                 trace_ok = true;
                 const long long n = a.n;
 #pragma unroll
@@ -1036,7 +1046,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         const int el = t / NP3;
         const int nd = FaceFirst<C>::value ? face_first_node<N>(t - el * NP3) : t - el * NP3;
         const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
-        const int sl = SL::at(el, na, nb, nc);
+        const int sl = checked(SL::at(el, na, nb, nc), FS, a.status);
         T rho_t = T(1), m1_t = T(0), m2_t = T(0), m3_t = T(0), E_t = T(1), phi_t = T(0);
         T ja_t[9];
 #pragma unroll
@@ -1045,7 +1055,8 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         const bool perturbed = a.rho_ref != nullptr;
         T rr_t = T(0), pr_t = T(0);
         if (real) {
-            const long long g = FaceFirst<C>::value ? node0 + (long long)el * NP3 + nd : node0 + t;
+            const long long g = checked(FaceFirst<C>::value ? node0 + (long long)el * NP3 + nd : node0 + t, a.n,
+                                        a.status);
             const long long n = a.n;
             rho_t = __ldg(a.q + g);
             m1_t = __ldg(a.q + n + g);
@@ -1146,6 +1157,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             FSL::decode(s, el, dir, side, i1, i2);
             long long g;
             if (!face_neighbour<N>(nbr, el, dir, side, i1, i2, g)) continue;
+            g = checked(g, a.n, a.status);
 #pragma unroll
             for (int v = 0; v < 5; ++v) fb[v * CNT + s] = __ldg(a.q + v * n + g);
 #pragma unroll
@@ -1164,11 +1176,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     const int p = lane - (lane / NQ) * NQ;
     C cq[S::H];
 #pragma unroll
-    for (int d = 1; d <= S::H; ++d) {
-        int pm = p + d;
-        if (pm >= NQ) pm -= NQ;
-        cq[d - 1] = CV::in(T(0.5) * a.ops.Q2[p * NQ + pm]);
-    }
+    for (int d = 1; d <= S::H; ++d) cq[d - 1] = CV::in(T(0.5) * a.ops.Q2[p * NQ + wrap_pos<NQ>(p, d)]);
     const C iw = CV::in(a.ops.invw[p]);
     const C c_g = CV::in(T(2) * a.c_g);  // 1/(gamma - 1)
     __syncthreads();
@@ -1200,8 +1208,8 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             const int el = t / NP3;
             const int nd = t - el * NP3;
             const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
-            const int sl = SL::at(el, na, nb, nc);
-            const long long g = node0 + t;
+            const int sl = checked(SL::at(el, na, nb, nc), FS, a.status);
+            const long long g = checked(node0 + t, a.n, a.status);
             store_node<T, N, MODE>(a, g, na, nb, nc, el, nullptr, CV::out(s_acc[0 * FS + sl]),
                                  CV::out(s_acc[1 * FS + sl]),
                              CV::out(s_acc[2 * FS + sl]), CV::out(s_acc[3 * FS + sl]), CV::out(s_acc[4 * FS + sl]));

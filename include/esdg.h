@@ -75,7 +75,10 @@ enum { ESDG_FORM_2D = 0, ESDG_FORM_SKEW = 1 };
 
 /* Status bits set by kernels and read with esdg_get_status(). */
 enum {
-    ESDG_STATUS_NONPHYSICAL = 1u  /* some node had rho <= 0, p <= 0 or NaN */
+    ESDG_STATUS_NONPHYSICAL = 1u, /* some node had rho <= 0, p <= 0 or NaN */
+    ESDG_STATUS_INDEX = 4u        /* debug library only (libesdg_debug.so): a kernel computed a
+                                     shared-memory, face-slot or global index out of range (the
+                                     access was redirected in bounds; results are then invalid) */
 };
 
 /* Create a handle for a mesh of Kx*Ky*Kz elements of order N (1..8).

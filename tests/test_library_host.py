@@ -175,7 +175,7 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(lib):
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """No CPU fallback: without libesdg.so every call raises."""
     monkeypatch.setattr(fd, "_lib", None)
-    monkeypatch.setattr(fd, "library_path", lambda: str(tmp_path / "absent.so"))
+    monkeypatch.setattr(fd, "library_path", lambda debug=False: str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         fd.operators(3)
 
