@@ -466,25 +466,25 @@ __device__ __forceinline__ PairTerms<T> pair_terms(const NodeVals<T>& I, const N
             return fma(v, fma(v, fma(v, T(1.0 / 15120.0), T(-1.0 / 360.0)), T(1.0 / 6.0)), T(2.0));
         };
         if (!__any_sync(mask, cr)) {
-            crl = (cq * (M.rho - I.rho)) * Num<T>::rcp(dlr);
+            crl = (cq * (M.rho - I.rho)) * Num<T>::rcp_pair(dlr);
         } else if (__all_sync(mask, cr)) {
             crl = cqr * series_r(dlr * dlr);
         } else {
-            crl = sel(cr, cqr * series_r(dlr * dlr), (cq * (M.rho - I.rho)) * Num<T>::rcp(dlr));
+            crl = sel(cr, cqr * series_r(dlr * dlr), (cq * (M.rho - I.rho)) * Num<T>::rcp_pair(dlr));
         }
 
         // 1/(b2+ + b2-) and, far, 1/(2{{b}}_log) = dlb/db2 from one reciprocal
         if (!__any_sync(mask, cb)) {
             const T db = M.b - I.b;
-            const T rb = Num<T>::rcp(db * bsum);
+            const T rb = Num<T>::rcp_pair(db * bsum);
             inv_bsum = db * rb;
             inv_bln = dlb * (bsum * rb);
         } else if (__all_sync(mask, cb)) {
-            inv_bsum = Num<T>::rcp(bsum);
+            inv_bsum = Num<T>::rcp_pair(bsum);
             inv_bln = inv_bsum * series_b(dlb * dlb);
         } else {
             const T db = M.b - I.b;
-            const T rb = Num<T>::rcp(sel(cb, bsum, db * bsum));
+            const T rb = Num<T>::rcp_pair(sel(cb, bsum, db * bsum));
             inv_bsum = sel(cb, rb, db * rb);
             inv_bln = sel(cb, inv_bsum * series_b(dlb * dlb), dlb * (bsum * rb));
         }
