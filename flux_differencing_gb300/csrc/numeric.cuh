@@ -65,22 +65,36 @@ struct Num<double> {
         const double e = fma(-x, r, 1.0);
         return fma(r, fma(e, e, e), r);
     }
-    // 1/x for the pair evaluations of the volume kernel: the same estimate and
-    // one Newton-Raphson step of second order, r' = r (1 + e), which squares
-    // the estimate's relative error (one FP64 operation fewer per reciprocal;
-    // the bound is measured on the GPU by the test suite).  The pair
-    // reciprocals scale the pressure mean and the logarithmic means, so their
-    // relative error passes into the flux terms unamplified.
-    static __device__ __forceinline__ double rcp_pair(double x) {
-        double r;
-        asm("rcp.approx.ftz.f64 %0, %1;" : "=d"(r) : "d"(x));
-        return fma(r, fma(-x, r, 1.0), r);
-    }
-    // the hardware estimate alone (for the self-test that measures it)
+    // 1/x for the pair evaluations of the volume kernel: an estimate from the
+    // FP32 reciprocal of x's mantissa, refined by one Newton-Raphson step of
+    // second order, r' = r (1 + e), which squares the estimate's relative error.
+    // The FP64 estimate above reads only the high word of x and is good to
+    // about 2^-20 (measured), so one second-order step would leave 2^-40;
+    // the mantissa's top 23 bits through the FP32 reciprocal give about 2^-22,
+    // and the step then about 2^-44 -- one FP64 operation fewer than rcp(),
+    // the estimate built on the integer and FP32 pipes.  The pair reciprocals
+    // scale the pressure mean and the logarithmic means, so their relative
+    // error passes into the flux terms unamplified.  For normal |x| in
+    // [2^-1020, 2^1020] (the pair quantities are differences and sums of
+    // per-node logarithms and of rho/p); the bound is measured on the GPU by
+    // the test suite.
     static __device__ __forceinline__ double rcp_estimate(double x) {
-        double r;
-        asm("rcp.approx.ftz.f64 %0, %1;" : "=d"(r) : "d"(x));
-        return r;
+        const int hi = __double2hiint(x);
+        const unsigned lo = static_cast<unsigned>(__double2loint(x));
+        // x = +-M 2^(E - 1023), M in [1, 2): M's top 23 bits as a float
+        const float m = __int_as_float(0x3f800000 | ((hi & 0x000fffff) << 3) | static_cast<int>(lo >> 29));
+        float rm;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rm) : "f"(m));  // in (0.5, 1]
+        // 1/x = +-rm 2^(1023 - E): rm's exponent field (126 or 127) rebiased
+        // for a double, its 23 mantissa bits moved to the top of a double's
+        const int rb = __float_as_int(rm);
+        const int E = (hi >> 20) & 0x7ff;
+        const int ohi = (hi & static_cast<int>(0x80000000u)) | ((rb >> 3) + ((1919 - E) << 20));
+        return __hiloint2double(ohi, rb << 29);
+    }
+    static __device__ __forceinline__ double rcp_pair(double x) {
+        const double r = rcp_estimate(x);
+        return fma(r, fma(-x, r, 1.0), r);
     }
     // |d| < 0.02 (high word of 0.02 = 0x3F947AE1), tested on the integer pipe
     static __device__ __forceinline__ bool close(double d) {
