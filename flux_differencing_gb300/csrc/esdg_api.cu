@@ -172,8 +172,8 @@ esdg::SurfaceConsts<T> surface_consts(const esdg_ctx* h) {
     k.igm1 = (T)(1 / (g - 1));
     k.c_g = (T)(1 / (2 * (g - 1)));
     k.gamma = (T)g;
-    k.c_ac = (T)(1 / (2 * g));
-    k.c_en = (T)((g - 1) / g);
+    k.c_ac = (T)(1 / (4 * g));       // half the acoustic-wave scaling 1/(2 gamma)
+    k.c_en = (T)((g - 1) / (2 * g));  // half the entropy-wave scaling (gamma - 1)/gamma
     return k;
 }
 

@@ -35,8 +35,8 @@ struct SurfaceConsts {
     T igm1;    // 1/(gamma - 1)
     T c_g;     // 1/(2 (gamma - 1))
     T gamma;
-    T c_ac;    // 1/(2 gamma): acoustic-wave entry of the eigenvector scaling
-    T c_en;    // (gamma - 1)/gamma: entropy-wave entry of the eigenvector scaling
+    T c_ac;    // 1/(4 gamma): half the acoustic-wave entry 1/(2 gamma) of the eigenvector scaling
+    T c_en;    // (gamma - 1)/(2 gamma): half the entropy-wave entry (gamma - 1)/gamma
 };
 
 template <typename T>

@@ -43,15 +43,19 @@ __global__ void rcp_selftest(const T* __restrict__ x, T* __restrict__ y, long n)
     const long k = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (k < n) y[k] = esdg::Num<T>::rcp(x[k]);
 }
-// mode 2: the pair reciprocal; mode 3: the bare hardware estimate
+// mode 2: the pair reciprocal; 3: its estimate; 4: the reciprocal square
+// root of the surface flux; 5: its estimate
 __global__ void rcp_selftest_fp64_variant(int mode, const double* __restrict__ x, double* __restrict__ y, long n) {
     const long k = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k < n) y[k] = mode == 2 ? esdg::Num<double>::rcp_pair(x[k]) : esdg::Num<double>::rcp_estimate(x[k]);
+    if (k >= n) return;
+    using D = esdg::Num<double>;
+    y[k] = mode == 2 ? D::rcp_pair(x[k]) : mode == 3 ? D::rcp_estimate(x[k])
+         : mode == 4 ? D::rsqrt_pair(x[k]) : D::rsqrt_estimate(x[k]);
 }
 }  // namespace
 
 extern "C" int esdg_selftest_rcp(int fp64, long n, const void* x, void* y, void* stream) {
-    if (n < 1 || !x || !y || fp64 < 0 || fp64 > 3) return 1;
+    if (n < 1 || !x || !y || fp64 < 0 || fp64 > 5) return 1;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const unsigned blocks = (unsigned)((n + 255) / 256);
     if (fp64 >= 2)

@@ -14,6 +14,8 @@
 
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "esdg_internal.h"
 #include "numeric.cuh"
 
@@ -44,7 +46,7 @@ __device__ __forceinline__ FaceNode<C> node_state(C rho_in, C m1, C m2, C m3, C 
                                                   C rho_ref, C p_ref) {
     FaceNode<C> s;
     const C rho = perturbed ? rho_ref + rho_in : rho_in;
-    const C irho = Num<C>::rcp(rho);
+    const C irho = Num<C>::rcp_pair(rho);
     s.rho = rho;
     s.u1 = m1 * irho;
     s.u2 = m2 * irho;
@@ -57,7 +59,7 @@ __device__ __forceinline__ FaceNode<C> node_state(C rho_in, C m1, C m2, C m3, C 
         s.E = E_in;
         s.p = gm1 * (E_in - rho * fma(C(0.5), s.uu, phi));
     }
-    s.b = C(0.5) * rho * Num<C>::rcp(s.p);
+    s.b = C(0.5) * rho * Num<C>::rcp_pair(s.p);
     s.ib = C(2.0) * s.p * irho;  // 1/b
     s.phi = phi;
     return s;
@@ -101,11 +103,11 @@ __device__ __forceinline__ void interface_flux(const FaceNode<C>& I, const FaceN
     //   {{a}}_log = {{a}} (1 - u/3 - 4u^2/45 - 44u^3/945) + O(u^4),
     //   [[ln a]] = 2 atanh(f),  1/{{a}}_log = [[ln a]]/[[a]] = atanh_ratio(u)/(a+ + a-)
     const C rsum = I.rho + J.rho, drho = J.rho - I.rho;
-    const C irs = Num<C>::rcp(rsum);
+    const C irs = Num<C>::rcp_pair(rsum);
     const C fr = drho * irs;
     const C ur = fr * fr;
     const C bsum = I.b + J.b, db = J.b - I.b;
-    const C ibs = Num<C>::rcp(bsum);
+    const C ibs = Num<C>::rcp_pair(bsum);
     const C fb = db * ibs;
     const C ub = fb * fb;
     const bool cr = Num<C>::close_ratio(fr), cb = Num<C>::close_ratio(fb);
@@ -119,8 +121,8 @@ __device__ __forceinline__ void interface_flux(const FaceNode<C>& I, const FaceN
         // a far pair in this warp: logarithms for all its lanes, selected per lane
         const C lr = far_log(J.rho) - far_log(I.rho);
         const C lb = far_log(J.b) - far_log(I.b);
-        rho_ln = sel(cr, rho_ln, drho * Num<C>::rcp(sel(cr, C(1.0), lr)));
-        inv_bln = sel(cb, inv_bln, lb * Num<C>::rcp(sel(cb, C(1.0), db)));
+        rho_ln = sel(cr, rho_ln, drho * Num<C>::rcp_pair(sel(cr, C(1.0), lr)));
+        inv_bln = sel(cb, inv_bln, lb * Num<C>::rcp_pair(sel(cb, C(1.0), db)));
         dlr = sel(cr, dlr, lr);
         dlb = sel(cb, dlb, lb);
     }
@@ -138,9 +140,21 @@ __device__ __forceinline__ void interface_flux(const FaceNode<C>& I, const FaceN
 
     C D0 = C(0.0), D1 = C(0.0), D2 = C(0.0), D3 = C(0.0), D4 = C(0.0);
     if (dissipation) {
-        // averaged state: sound speed and total enthalpy
-        const C a_sq = k.gamma * p_hat * Num<C>::rcp(rho_ln);
-        const C a = sqrt_(a_sq);
+        // averaged state: sound speed and total enthalpy; |n| and 1/|n|.  FP64
+        // takes both square roots from reciprocal square roots (an FP32
+        // estimate and one Newton step, Num<double>::rsqrt_pair).
+        const C a_sq = k.gamma * p_hat * Num<C>::rcp_pair(rho_ln);
+        const C nsq = fma(n2, n2, fma(n1, n1, n0 * n0));
+        C a, nn, inn;
+        if constexpr (std::is_same<C, double>::value) {
+            a = a_sq * Num<C>::rsqrt_pair(a_sq);
+            inn = Num<C>::rsqrt_pair(nsq);
+            nn = nsq * inn;
+        } else {
+            a = sqrt_(a_sq);
+            nn = sqrt_(nsq);
+            inn = Num<C>::rcp(nn);
+        }
         const C a_sq_g = a_sq * k.igm1;  // a^2/(gamma-1)
         const C ke = fma(C(0.5), aa, phib);  // |u|^2/2 + phi
         const C H = a_sq_g + ke;
@@ -154,13 +168,12 @@ __device__ __forceinline__ void interface_flux(const FaceNode<C>& I, const FaceN
         // shear input v = [[w_m]] + u [[w_5]] and its normal part
         const C v1 = fma(a1, d5, dm1), v2 = fma(a2, d5, dm2), v3 = fma(a3, d5, dm3);
         const C vn = fma(v3, n2, fma(v2, n1, v1 * n0));  // n . v (n unnormalised)
-        const C nsq = fma(n2, n2, fma(n1, n1, n0 * n0));
-        const C nn = sqrt_(nsq);
-        const C inn = Num<C>::rcp(nn);
         const C inn2 = inn * inn;
         // wave strengths
         const C beta = fma(H, d5, fma(a3, dm3, fma(a2, dm2, fma(a1, dm1, d1))));
         const C alpha_e = fma(-a_sq_g, d5, beta);
+        // the dissipation's factor 1/2 is carried by c_ac, c_en (halved
+        // constants) and ls, so the wave strengths below are already halved
         const C anu = a * vn * inn;
         const C rc = rho_ln * k.c_ac;
         const C lam_p = fabs(fma(a, nn, U)) * rc;
@@ -169,17 +182,17 @@ __device__ __forceinline__ void interface_flux(const FaceNode<C>& I, const FaceN
         const C cp_ = lam_p * (beta + anu);
         const C cm_ = lam_m * (beta - anu);
         const C ce = aU * rho_ln * k.c_en * alpha_e;
-        const C ls = aU * p_hat;
+        const C ls = aU * (C(0.5) * p_hat);
         const C csum = cp_ + cm_;
         const C cdif = (cp_ - cm_) * a * inn;
         const C c0 = csum + ce;
         const C svn = ls * vn * inn2;
-        D0 = C(0.5) * c0;
-        D1 = C(0.5) * (fma(c0, a1, fma(cdif, n0, ls * v1)) - svn * n0);
-        D2 = C(0.5) * (fma(c0, a2, fma(cdif, n1, ls * v2)) - svn * n1);
-        D3 = C(0.5) * (fma(c0, a3, fma(cdif, n2, ls * v3)) - svn * n2);
+        D0 = c0;
+        D1 = fma(c0, a1, fma(cdif, n0, ls * v1)) - svn * n0;
+        D2 = fma(c0, a2, fma(cdif, n1, ls * v2)) - svn * n1;
+        D3 = fma(c0, a3, fma(cdif, n2, ls * v3)) - svn * n2;
         const C uv = fma(a3, v3, fma(a2, v2, a1 * v1));
-        D4 = C(0.5) * (fma(csum, H, fma(cdif, U, fma(ce, ke, ls * uv))) - svn * U);
+        D4 = fma(csum, H, fma(cdif, U, fma(ce, ke, ls * uv))) - svn * U;
     }
 
     // momentum: F_rho {{u}} + p_hat n (+ gravity, scaled per side)

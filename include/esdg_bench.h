@@ -28,8 +28,9 @@ int esdg_bench_fma(int fp64, long blocks, int threads, int iters, void* sink, vo
  * correctly rounded division.  fp64 = 1: the FP64 per-node reciprocal
  * (hardware estimate plus one third-order Newton-Raphson step); 2: the FP64
  * pair reciprocal (an estimate from the FP32 reciprocal of the mantissa plus
- * one second-order step); 3: that estimate alone; 0: FP32 (the hardware
- * estimate alone).
+ * one second-order step); 3: that estimate alone; 4: the FP64 reciprocal
+ * square root of the surface flux (y[k] = 1/sqrt(x[k]), x > 0, built the same
+ * way); 5: its estimate alone; 0: FP32 (the hardware estimate alone).
  * x, y: device arrays of n doubles (fp64 != 0) or floats.  Asynchronous on
  * `stream`.  Returns 0, 1 (bad argument) or 4 (CUDA launch error). */
 int esdg_selftest_rcp(int fp64, long n, const void* x, void* y, void* stream);

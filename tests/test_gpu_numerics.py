@@ -74,6 +74,28 @@ def test_rcp_fp64_pair_relative_error(cuda_ok):
     assert rel.max() <= 2.0 ** -43, rel.max()
 
 
+def test_rsqrt_fp64_pair_relative_error(cuda_ok):
+    """The reciprocal square root of the FP64 surface flux (|n| and the sound
+    speed): FP32 estimate of the mantissa (times 2 for odd exponents), then one
+    second-order Newton step.  Required: the estimate within 2^-21.5 relative
+    and the result within 2^-42 (about 2.3e-13) over 1e-300 .. 1e300, odd and
+    even exponents, mantissas next to 1 and 2."""
+    lib = fd.load_library(build_if_missing=True)
+    rng = np.random.default_rng(20)
+    x = np.abs(_inputs(rng, 1 << 20, 1e-300, 1e300))
+    x[128:192] = np.ldexp(1.0, np.arange(-32, 32))  # exact powers of two, both parities
+    ref = 1.0 / np.sqrt(x)
+    est = _run(lib, x, True, mode=5)
+    y = _run(lib, x, True, mode=4)
+    rel_est = np.abs(est - ref) / ref
+    rel = np.abs(y - ref) / ref
+    print(f"rsqrt estimate: max rel {rel_est.max():.3e} = 2^{np.log2(rel_est.max()):.2f}; "
+          f"rsqrt: max rel {rel.max():.3e} = 2^{np.log2(rel.max()):.2f}")
+    assert np.all(np.isfinite(y))
+    assert rel_est.max() <= 2.0 ** -21.5, rel_est.max()
+    assert rel.max() <= 2.0 ** -42, rel.max()
+
+
 def test_rcp_fp32_relative_error(cuda_ok):
     lib = fd.load_library(build_if_missing=True)
     rng = np.random.default_rng(18)
