@@ -1091,30 +1091,6 @@ def run_graph_sweep(args, device, stream):
         torch.cuda.empty_cache()
 
 
-def run_mixed_sweep(args, device, stream):
-    import torch
-
-    import workloads as wl
-
-    for name in ("channel_N7_ff", "sweep_N7_ff"):
-        cfg = wl.get_config(name)
-        op, q, Ja, phi, out = _setup(cfg, device)
-        for k in [int(v) for v in args.mixed.split(",")]:
-            op.set_mixed_pipes(k)
-            steps = max(args.steps, 10)
-            sampler = ClockSampler(0)
-            sampler.start()
-            total_ms, per = _time_device(op, q, Ja, phi, out, steps, args.warmup, stream, lambda: None)
-            clocks = sampler.stop()
-            ms = total_ms / steps
-            print(json.dumps({"sweep": "mixed", "config": cfg.name, "N": cfg.N, "nodes": cfg.n, "sixteenths": k,
-                              "ms_per_launch": ms, "GDOF/s": cfg.n / (ms * 1e-3) / 1e9, "clocks": clocks}),
-                  flush=True)
-        op.close()
-        del q, Ja, phi, out
-        torch.cuda.empty_cache()
-
-
 def run_sweep(args):
     """Opt-in measurement sweeps, one JSON line per point on stdout.
 
@@ -1145,12 +1121,6 @@ def run_sweep(args):
         for N in [int(v) for v in args.orders.split(",")]:
             for prec in precs:
                 points.append(wl.get_config(f"sweep_N{N}" + {"fp64": "", "fp32": "_fp32", "fp64ff": "_ff"}[prec]))
-    elif args.sweep == "mixed":
-        # share of native-FP64 elements in the float-float volume kernel
-        # (sixteenths; 0 = float-float only) on the N = 7 channel and the order
-        # sweep's N = 7 cube
-        run_mixed_sweep(args, device, stream)
-        return
     elif args.sweep == "parity":
         # the five named workloads in every precision (the FP32 and float-float
         # variants share mesh and state), compared with the oracle
@@ -1216,7 +1186,7 @@ def main():
     ap.add_argument("--no-peaks", action="store_true", help="skip the FMA-throughput peak measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-elements", type=int, default=256)
-    ap.add_argument("--sweep", choices=["orders", "elements", "graph", "oracle", "parity", "mixed"], default=None,
+    ap.add_argument("--sweep", choices=["orders", "elements", "graph", "oracle", "parity"], default=None,
                     help="opt-in measurement sweeps (one JSON line per point) instead of the bench line")
     ap.add_argument("--precisions", default="fp64,fp32,fp64ff",
                     help="comma-separated precisions of the orders and elements sweeps")
@@ -1224,8 +1194,6 @@ def main():
     ap.add_argument("--large", default="sweep_N7,sweep_N7_fp32",
                     help="largest single-GPU workloads timed in the same run (comma-separated; '' for none)")
     ap.add_argument("--no-parity", action="store_true", help="skip the parity report against the oracle")
-    ap.add_argument("--mixed", default="0,1,2,3,4,5,6,8",
-                    help="sixteenths of native-FP64 elements tried by --sweep mixed")
     ap.add_argument("--split", action="store_true",
                     help="under torchrun: divide one mesh among the ranks by element ranges (strong scaling) "
                          "instead of one mesh per rank (weak scaling)")

@@ -45,7 +45,6 @@ _SIGS = {
     "esdg_set_geometry": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     "esdg_volume_rhs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "esdg_volume_rhs_range": (ctypes.c_int, [_P, ctypes.c_long, ctypes.c_long, _P, _P, _P, _P, _P]),
-    "esdg_set_mixed_pipes": (ctypes.c_int, [_P, ctypes.c_int]),
     "esdg_set_boundary": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "esdg_set_dissipation": (ctypes.c_int, [_P, ctypes.c_int]),
     "esdg_surface_rhs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
@@ -252,11 +251,6 @@ class VolumeOperator:
         """Surface-term boundary kind per reference direction: 0 periodic, 1 slip wall."""
         _chk(self, self.lib.esdg_set_boundary(self.h, int(bc_xi), int(bc_eta), int(bc_zeta)), self.h)
         self.bc = (int(bc_xi), int(bc_eta), int(bc_zeta))
-
-    def set_mixed_pipes(self, sixteenths: int):
-        """fp64ff handles: elements with e mod 16 < sixteenths take native FP64 in the
-        volume term, the rest float-float, on the two pipes at once (0: float-float only)."""
-        _chk(self, self.lib.esdg_set_mixed_pipes(self.h, int(sixteenths)), self.h)
 
     def set_dissipation(self, on: bool = True):
         """Surface flux with (default) or without the matrix dissipation."""

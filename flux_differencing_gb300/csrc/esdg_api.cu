@@ -23,8 +23,6 @@ struct esdg_ctx {
     int device = 0;
     unsigned* d_status = nullptr;
     double* d_partials = nullptr;  // diagnostics scratch, 3 * kDiagBlocks doubles
-    int* d_work = nullptr;         // ESDG_FP64_FF: counters of the mixed-pipe volume kernel
-    int mixed_k = 3;               // ESDG_FP64_FF: elements with e mod 16 < mixed_k in native FP64
     double nodes[esdg::kMaxNq];
     double weights[esdg::kMaxNq];
     double D[esdg::kMaxNq * esdg::kMaxNq];
@@ -34,8 +32,6 @@ struct esdg_ctx {
 };
 
 namespace {
-
-constexpr int kWorkInts = 2 + 256;  // the mixed-pipe kernel's class and per-SM role counters
 
 thread_local std::string g_create_error;
 
@@ -164,8 +160,6 @@ esdg::VolumeArgs<T> volume_args(const esdg_ctx* h, const void* q, const void* Ja
     a.status = h->d_status;
     a.rho_ref = static_cast<const T*>(h->ref_rho);
     a.p_ref = static_cast<const T*>(h->ref_p);
-    a.work = h->d_work;
-    a.mixed_k = h->mixed_k;
     a.ops = ops;
     return a;
 }
@@ -379,12 +373,10 @@ int esdg_create(esdg_handle* out, long Kx, long Ky, long Kz, int N, int precisio
     if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_partials, sizeof(double) * 3 * esdg::kDiagBlocks);
-    if (e == cudaSuccess && precision == ESDG_FP64_FF) e = cudaMalloc(&h->d_work, sizeof(int) * kWorkInts);
     if (e != cudaSuccess) {
         std::string msg = std::string("device status word: ") + cudaGetErrorString(e);
         if (h->d_status) cudaFree(h->d_status);
         if (h->d_partials) cudaFree(h->d_partials);
-        if (h->d_work) cudaFree(h->d_work);
         delete h;
         return fail(nullptr, ESDG_ERR_CUDA, msg);
     }
@@ -396,16 +388,7 @@ int esdg_destroy(esdg_handle h) {
     if (!h) return ESDG_OK;
     if (h->d_status) cudaFree(h->d_status);
     if (h->d_partials) cudaFree(h->d_partials);
-    if (h->d_work) cudaFree(h->d_work);
     delete h;
-    return ESDG_OK;
-}
-
-int esdg_set_mixed_pipes(esdg_handle h, int sixteenths) {
-    if (!h) return fail(nullptr, ESDG_ERR_ARG, "null handle");
-    if (h->precision != ESDG_FP64_FF) return fail(h, ESDG_ERR_UNSUPPORTED, "only ESDG_FP64_FF handles mix pipes");
-    if (sixteenths < 0 || sixteenths > 16) return fail(h, ESDG_ERR_ARG, "sixteenths must be in 0..16");
-    h->mixed_k = sixteenths;
     return ESDG_OK;
 }
 

@@ -80,13 +80,6 @@ struct VolumeArgs {
     int dissipation;       // 0: entropy-conserving interface flux only
     T inv_w0;              // 1 / (LGL end weight)
     SurfaceConsts<T> sk;
-    // ESDG_FP64_FF, plain volume term: elements with e mod 16 < mixed_k take
-    // native FP64 arithmetic and the rest float-float, one CTA of each per SM
-    // (volume_kernel_mixed); work is the handle's scratch of 2 + 256 ints
-    // (class counters, per-SM role counters), cleared on the stream before
-    // each launch.  mixed_k = 0 or work = nullptr: float-float only.
-    int* work;
-    int mixed_k;
     OpTables<T> ops;
 };
 

@@ -977,20 +977,20 @@ __device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict
 // MODE (store_node): 0 volume to out, 1 fused Runge-Kutta stage, 2 (FP32)
 // volume + faces to out; separate instantiations, so that the plain kernel's
 // code and registers are those of a store to out.
-// The elements e0 .. e0 + EPB - 1 (up to e_end) of one CTA: load phase,
-// direction phases, store.  Called by the kernels below with the CTA's
-// dynamic shared memory.
 template <typename T, int N, typename C, int MODE>
-__device__ __forceinline__ void volume_elements(const VolumeArgs<T>& a, long long e0, unsigned char* smem_raw) {
+__global__ void __launch_bounds__(Launch<N, C>::THREADS, Launch<N, C>::MIN_BLOCKS)
+volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     using S = Shape<N>;
     using SL = Slots<N>;
     constexpr int NQ = S::NQ;
     constexpr int NP3 = S::NP3;
     constexpr int FS = SL::SIZE;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     C* sm = reinterpret_cast<C*>(smem_raw);
     using CV = Conv<T, C>;
     poison_shared(smem_raw, volume_smem_bytes<C, N, MODE>());  // debug builds only
 
+    const long long e0 = a.e_begin + (long long)blockIdx.x * S::EPB;
     const long long rem = a.e_end - e0;
     const int e_count = rem < S::EPB ? (int)rem : S::EPB;
     const long long node0 = e0 * NP3;
@@ -1233,101 +1233,6 @@ __device__ __forceinline__ void volume_elements(const VolumeArgs<T>& a, long lon
 }
 
 template <typename T, int N, typename C, int MODE>
-__global__ void __launch_bounds__(Launch<N, C>::THREADS, Launch<N, C>::MIN_BLOCKS)
-volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    volume_elements<T, N, C, MODE>(a, a.e_begin + (long long)blockIdx.x * Shape<N>::EPB, smem_raw);
-}
-
-// FP64 results from both arithmetic pipes (ESDG_FP64_FF handles).  GB300
-// runs FP32 at 64 times its FP64 rate: the float-float kernel keeps the FP32
-// pipes and the instruction issue busy and leaves the FP64 pipe nearly idle,
-// the native FP64 kernel the reverse.  This kernel runs both on one SM: a
-// persistent grid of two CTAs per SM, the first CTA to start on an SM works
-// in float-float, the second in native FP64, each taking elements from a
-// counter of its own class.  The class of an element is fixed by its index
-// (FP64 when e mod 16 < k, k = VolumeArgs::mixed_k), so each element always
-// takes the same arithmetic path (results are bitwise reproducible, and
-// element ranges compose); a CTA whose class is exhausted helps with the other
-// class, on that class's path, so neither pipe waits for the other at the end.
-// Built where both paths have the same CTA shape and shared memory (one
-// element per CTA).
-template <int N>
-struct MixedPipes {
-    static constexpr bool value = Shape<N>::EPB == 1 && Launch<N, double>::THREADS == Launch<N, ff>::THREADS &&
-                                  volume_smem_bytes<double, N, 0>() == volume_smem_bytes<ff, N, 0>();
-};
-constexpr int kMixedSmSlots = 256;  // per-SM role counters of the work array (SM ids taken modulo 256)
-
-// Next element of class cls (1: FP64, e mod 16 < k; 0: float-float) in
-// [e_begin, e_end), counted by work[cls] over 16-element blocks aligned at
-// multiples of 16; -1 when the class is exhausted.
-__device__ __forceinline__ long long mixed_next(int* work, int cls, int k, long long e_begin, long long e_end) {
-    const int per = cls ? k : 16 - k;
-    if (per <= 0) return -1;
-    const long long base = e_begin - (e_begin % 16);
-    for (;;) {
-        const long long j = atomicAdd(work + cls, 1);
-        const long long e = base + (j / per) * 16 + (cls ? 0 : k) + j % per;
-        if (e >= e_end) return -1;
-        if (e >= e_begin) return e;
-    }
-}
-
-template <int N>
-__global__ void __launch_bounds__(Launch<N, ff>::THREADS, 2)
-volume_kernel_mixed(const __grid_constant__ VolumeArgs<double> a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    __shared__ long long s_e;
-    __shared__ int s_role, s_cls;
-    if (threadIdx.x == 0) {
-        unsigned smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        s_role = atomicAdd(a.work + 2 + (smid % kMixedSmSlots), 1) & 1;  // 0: float-float, 1: FP64
-    }
-    __syncthreads();
-    const int role = s_role;
-#pragma unroll 1
-    for (;;) {
-        if (threadIdx.x == 0) {
-            int cls = role;
-            long long e = mixed_next(a.work, cls, a.mixed_k, a.e_begin, a.e_end);
-            if (e < 0) {
-                cls = 1 - role;
-                e = mixed_next(a.work, cls, a.mixed_k, a.e_begin, a.e_end);
-            }
-            s_e = e;
-            s_cls = cls;
-        }
-        __syncthreads();
-        const long long e = s_e;
-        const int cls = s_cls;
-        if (e < 0) break;
-        if (cls) volume_elements<double, N, double, 0>(a, e, smem_raw);
-        else volume_elements<double, N, ff, 0>(a, e, smem_raw);
-        __syncthreads();  // shared memory and s_e reused by the next element
-    }
-}
-
-template <int N>
-cudaError_t launch_volume_mixed(const VolumeArgs<double>& a, cudaStream_t s) {
-    const long long K = a.e_end - a.e_begin;
-    if (K <= 0) return cudaSuccess;
-    const size_t smem = volume_smem_bytes<ff, N, 0>();
-    cudaError_t err = cudaFuncSetAttribute(volume_kernel_mixed<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-    if (err != cudaSuccess) return err;
-    int dev = 0, sms = 0;
-    err = cudaGetDevice(&dev);
-    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess) err = cudaMemsetAsync(a.work, 0, sizeof(int) * (2 + kMixedSmSlots), s);
-    if (err != cudaSuccess) return err;
-    const long long blocks = K < 2LL * sms ? K : 2LL * sms;
-    volume_kernel_mixed<N><<<(unsigned)blocks, Launch<N, ff>::THREADS, smem, s>>>(a);
-    return cudaGetLastError();
-}
-
-template <typename T, int N, typename C, int MODE>
 cudaError_t launch_volume_mode(const VolumeArgs<T>& a, cudaStream_t s) {
     using S = Shape<N>;
     const long long K = a.e_end - a.e_begin;
@@ -1356,9 +1261,6 @@ cudaError_t launch_volume(const VolumeArgs<T>& a, cudaStream_t s) {
     if (a.with_faces) {
         if constexpr (FusedSurface<C>::value) return launch_volume_mode<T, N, C, 2>(a, s);
         else return cudaErrorNotSupported;
-    }
-    if constexpr (IsFF<C>::value && MixedPipes<N>::value) {
-        if (a.work != nullptr && a.mixed_k > 0) return launch_volume_mixed<N>(a, s);
     }
     return launch_volume_mode<T, N, C, 0>(a, s);
 }

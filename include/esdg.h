@@ -144,21 +144,6 @@ enum { ESDG_BC_PERIODIC = 0, ESDG_BC_WALL = 1 };
  * Errors: ESDG_ERR_ARG (null handle or unknown kind). */
 int esdg_set_boundary(esdg_handle h, int bc_xi, int bc_eta, int bc_zeta);
 
-/* ESDG_FP64_FF handles: the share of elements whose volume term takes native
- * FP64 arithmetic instead of float-float, in sixteenths (element e when
- * e mod 16 < sixteenths; default 3).  GB300 runs FP32 at 64 times its FP64
- * rate: float-float work keeps the FP32 pipes and the instruction issue busy
- * and leaves the FP64 pipe nearly idle, native FP64 the reverse, so the
- * volume kernel runs both at once -- two persistent CTAs per SM, one per
- * kind, each taking elements of its own class and helping with the other
- * class when its own is exhausted.  Both paths meet the FP64 accuracy of
- * ESDG_FP64_FF; an element always takes the path of its class, so results
- * are reproducible bit for bit.  0: float-float only.  Used where the two
- * paths share a CTA shape (one element per CTA; N = 7); other orders run
- * float-float.  Errors: ESDG_ERR_ARG (null handle, sixteenths outside 0..16),
- * ESDG_ERR_UNSUPPORTED (not an ESDG_FP64_FF handle). */
-int esdg_set_mixed_pipes(esdg_handle h, int sixteenths);
-
 /* on != 0 (default): the surface flux is the entropy-conserving flux minus
  * the matrix dissipation; on == 0: the entropy-conserving flux alone (the
  * semi-discrete scheme then conserves entropy, which tests use). */
