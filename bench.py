@@ -107,7 +107,7 @@ _CSRC = os.path.join(ROOT, "flux_differencing_gb300", "csrc")
 _NUMERIC = ("numeric.cuh", "floatfloat.cuh", "log_fp64.cuh", "log_table.inc", "esdg_internal.h", "surface_flux.cuh")
 KERNEL_SOURCES = {
     "volume": [os.path.join(_CSRC, f) for f in ("volume_kernel.cuh", "packed.cuh", "volume_inst.cu") + _NUMERIC],
-    "surface": [os.path.join(_CSRC, f) for f in ("surface_kernel.cu",) + _NUMERIC],
+    "surface": [os.path.join(_CSRC, f) for f in ("surface_kernel.cu", "surface_index.cuh") + _NUMERIC],
 }
 
 
