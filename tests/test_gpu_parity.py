@@ -44,6 +44,37 @@ def test_small_meshes(N, K, precision):
     assert e.max() < hz.TOL[precision], e
 
 
+def _wide_ratio_state(cfg, g, amp):
+    """The generated state with the density stretched by exp(amp * smooth
+    field) node by node (velocity and pressure kept, so 2b = rho/p stretches
+    alike): pairs on one line then differ by factors up to about 50, beside
+    close pairs, which drives every precision's far log-mean branch."""
+    g = {k: v.clone() for k, v in g.items()}
+    q = g["q"].double()
+    rho = q[0]
+    u = q[1:4] / rho
+    phi = g["phi"].double()
+    p = 0.4 * (q[4] - 0.5 * rho * (u * u).sum(0) - rho * phi)
+    s = torch.exp(amp * torch.sin(g["x"] * 7.3e-3 + 0.4) * torch.cos(g["y"] * 5.1e-3)
+                  * torch.sin(g["z"] * 3.3e-3 + 1.1))
+    rho2 = rho * s
+    g["q"] = torch.stack([rho2, rho2 * u[0], rho2 * u[1], rho2 * u[2],
+                          p / 0.4 + 0.5 * rho2 * (u * u).sum(0) + rho2 * phi])
+    return g
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 7])
+@pytest.mark.parametrize("precision", PRECISIONS)
+def test_wide_density_ratios(N, precision):
+    cfg = wl.small_config(N, K=(3, 2, 2), warp=True, precision=precision)
+    g = _wide_ratio_state(cfg, wl.generate(cfg), 2.0)
+    got, op, _ = hz.run_gpu(cfg, g)
+    assert op.status() == 0
+    ref, scale = hz.run_oracle(cfg, g)
+    e, _ = hz.errors(got, ref, scale)
+    assert e.max() < hz.TOL[precision], e
+
+
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8])
 @pytest.mark.parametrize("precision", PRECISIONS)
 def test_skew_form(N, precision):
