@@ -5,6 +5,7 @@ import itertools
 import os
 from types import SimpleNamespace
 
+import numpy as np
 import pytest
 
 import bench
@@ -78,3 +79,52 @@ def test_operation_counts():
 def test_launch_counts():
     assert [bench.step_launches(p) for p in ("fp64", "fp64ff", "fp32")] == [25, 20, 5]
     assert [bench.rhs_launches(p) for p in ("fp64", "fp64ff", "fp32")] == [4, 4, 1]
+
+
+def test_parity_numbers_measures():
+    """e_c is the difference over the term scale S_c, plain the difference over
+    max|oracle|, kappa their ratio; pass/fail follows the precision's bar."""
+    ref = np.zeros((5, 6))
+    ref[:, 2] = [2.0, -4.0, 1.0, 0.5, 8.0]
+    scale = np.ones((5, 6)) * 10.0
+    got = ref.copy()
+    got[1, 4] += 1e-12  # only rho_u1 differs
+    par = bench.parity_numbers(got, ref, scale, "fp64")
+    r = par["per_variable"]["rho_u1"]
+    assert r["e_c"] == pytest.approx(1e-13)
+    assert r["plain"] == pytest.approx(1e-12 / 4.0)
+    assert r["kappa"] == pytest.approx(10.0 / 4.0)
+    assert par["per_variable"]["rho"]["e_c"] == 0.0
+    assert par["max_e_c"] == pytest.approx(1e-13) and par["pass"]
+    assert not bench.parity_numbers(got + 1e-9, ref, scale, "fp64")["pass"]
+    assert bench.parity_numbers(got + 1e-9, ref, scale, "fp32")["pass"]
+
+
+def test_gpu_rows_picks_element_columns():
+    cfg = SimpleNamespace(Nq=3)  # 27 nodes per element
+    out = np.arange(5 * 4 * 27, dtype=float).reshape(5, 4 * 27)
+    rows = bench.gpu_rows(out, cfg, np.array([1, 3]))
+    assert rows.shape == (5, 54)
+    assert np.array_equal(rows[:, :27], out[:, 27:54])
+    assert np.array_equal(rows[:, 27:], out[:, 81:108])
+
+
+def test_same_mesh_ignores_precision_only():
+    import dataclasses
+
+    import workloads as wl
+    base = wl.get_config("channel_N7")
+    assert bench._same_mesh(base, wl.get_config("channel_N7_fp32"))
+    assert bench._same_mesh(base, dataclasses.replace(base, precision="fp64ff"))
+    assert not bench._same_mesh(base, wl.get_config("sweep_N7"))
+
+
+def test_issue_roofline_from_record(monkeypatch):
+    cfg = SimpleNamespace(name="channel_N7_ff", n=4194304)
+    monkeypatch.setattr(bench, "recorded_field", lambda kernel, workload, field, kind="volume": 3200.0)
+    r = bench.issue_roofline("volume_kernel<double, 7, ff>", cfg, 1e-3)
+    expect = 3200.0 / 32 * 4194304 / 1e-3
+    assert r["bound"] == "issue" and r["achieved"] == pytest.approx(expect / 1e9)
+    assert r["frac"] == pytest.approx(expect / bench.ISSUE_PEAK_WARP_INST_PER_S)
+    monkeypatch.setattr(bench, "recorded_field", lambda *a, **k: None)
+    assert bench.issue_roofline("volume_kernel<double, 7, ff>", cfg, 1e-3) is None
