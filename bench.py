@@ -106,7 +106,7 @@ NOMINAL_FP64_TFLOPS = 1.25  # GB300 FP64 vector, nominal
 _CSRC = os.path.join(ROOT, "flux_differencing_gb300", "csrc")
 _NUMERIC = ("numeric.cuh", "floatfloat.cuh", "log_fp64.cuh", "log_table.inc", "esdg_internal.h", "surface_flux.cuh")
 KERNEL_SOURCES = {
-    "volume": [os.path.join(_CSRC, f) for f in ("volume_kernel.cuh", "packed.cuh", "volume_inst.cu") + _NUMERIC],
+    "volume": [os.path.join(_CSRC, f) for f in ("volume_kernel.cuh", "packed.cuh", "volume_inst.cu", "logmean_poly.inc") + _NUMERIC],
     "surface": [os.path.join(_CSRC, f) for f in ("surface_kernel.cu", "surface_index.cuh") + _NUMERIC],
 }
 

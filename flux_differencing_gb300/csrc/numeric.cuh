@@ -139,10 +139,14 @@ struct Num<float> {
         return r;
     }
     static __device__ __forceinline__ float rcp_pair(float x) { return rcp(x); }
-    // |d| < 0.2: one compare with an absolute-value operand (the issue-bound
-    // FP32 kernel counts instructions, not pipes)
-    static __device__ __forceinline__ bool close(float d) { return fabsf(d) < 0.2f; }
     static __device__ __forceinline__ float log_(float x) { return logf(x); }
+    // the hardware base-2 logarithm (absolute error about 2^-22)
+    static __device__ __forceinline__ float lg2(float x) {
+        float r;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+        return r;
+    }
+    static __device__ __forceinline__ bool above(float u, float lim) { return u > lim; }
     // |f| < 0.1 (0x3DCCCCCD), i.e. |ln a+ - ln a-| < 2 atanh(0.1) ~ 0.2
     static __device__ __forceinline__ bool close_ratio(float f) {
         return (__float_as_uint(f) & 0x7fffffffu) < 0x3DCCCCCDu;

@@ -80,6 +80,22 @@
 
 namespace esdg {
 
+// FP32 logarithmic-mean polynomials (kLogMeanRatio, kInvLogMeanRatio on
+// u = f^2 <= kLogMeanPolyU), written by gen_logmean_poly.py
+#include "logmean_poly.inc"
+
+// A CTA whose node densities and values of b lie within this factor of one
+// another (largest <= kNarrowRatio x smallest) takes the polynomial log means
+// for all its pairs: |f| <= 1.25/3.25, u <= 0.148, inside the fitted range
+// with room for the rounding of f.  Others select per pair between the
+// polynomials and the logarithm of the pair's ratio.
+constexpr float kNarrowRatio = 2.25f;
+constexpr float kLog2E = 1.4426950408889634f;  // 1/ln 2
+constexpr float kLn2F = 0.6931471805599453f;
+static_assert((kNarrowRatio - 1.0f) * (kNarrowRatio - 1.0f) <
+                  kLogMeanPolyU * (kNarrowRatio + 1.0f) * (kNarrowRatio + 1.0f),
+              "narrow pairs must stay inside the polynomials' range");
+
 template <int N>
 struct Shape {
     static constexpr int NQ = N + 1;
@@ -141,7 +157,10 @@ enum SmemField {
 template <>
 struct Num<p2> {
     static __device__ __forceinline__ p2 rcp(p2 x) { return p2(Num<float>::rcp(x.v.x), Num<float>::rcp(x.v.y)); }
-    static __device__ __forceinline__ m2 close(p2 d) { return m2{Num<float>::close(d.v.x), Num<float>::close(d.v.y)}; }
+    static __device__ __forceinline__ p2 lg2(p2 x) { return p2(Num<float>::lg2(x.v.x), Num<float>::lg2(x.v.y)); }
+    static __device__ __forceinline__ m2 above(p2 u, float lim) {
+        return m2{Num<float>::above(u.v.x, lim), Num<float>::above(u.v.y, lim)};
+    }
 };
 
 // Node (a, b, c) of line `ell` of direction R at line position p.  R may be
@@ -217,6 +236,18 @@ __host__ __device__ __forceinline__ int face_first_node(int k) {
 template <typename T>
 struct SplitAntipodal {
     static constexpr bool value = sizeof(T) == 8;
+};
+
+// Whether the kernel checks, per CTA, that its node values lie within
+// kNarrowRatio of one another.  Such a CTA takes the polynomial log means for
+// every pair, with no test; the others add, per pair, the logarithm of the
+// pair's ratio and a select for the pairs beyond the polynomials' range.
+// The FP32 kernel has no per-node logarithms.  FP64 and float-float keep
+// theirs (series near equal values, logarithms of the node values beyond):
+// polynomials accurate to their precision would need a far higher degree.
+template <typename C>
+struct NarrowCheck {
+    static constexpr bool value = std::is_same<C, float>::value;
 };
 
 // Values of one node that a pair evaluation reads (metric terms of the
@@ -401,7 +432,22 @@ struct PairTerms {
     T fr, fE, Pi, Pm, s1, s2, s3, A0, A1, A2;
 };
 
-template <typename T>
+// Horner evaluation of the degree-4 polynomial of table W (0: kLogMeanRatio,
+// 1: kInvLogMeanRatio) at u.
+template <int W, typename T>
+__device__ __forceinline__ T poly4(T u) {
+    constexpr float c0 = W ? kInvLogMeanRatio[0] : kLogMeanRatio[0];
+    constexpr float c1 = W ? kInvLogMeanRatio[1] : kLogMeanRatio[1];
+    constexpr float c2 = W ? kInvLogMeanRatio[2] : kLogMeanRatio[2];
+    constexpr float c3 = W ? kInvLogMeanRatio[3] : kLogMeanRatio[3];
+    constexpr float c4 = W ? kInvLogMeanRatio[4] : kLogMeanRatio[4];
+    return fma(fma(fma(fma(T(c4), u, T(c3)), u, T(c2)), u, T(c1)), u, T(c0));
+}
+
+// NARROW (FP32 only): every node value of the CTA's elements lies within a
+// factor kNarrowRatio of every other (checked in the load phase), so the
+// logarithmic means come from polynomials, without logarithms or branches.
+template <typename T, bool NARROW = false>
 __device__ __forceinline__ PairTerms<T> pair_terms(const NodeVals<T>& I, const NodeVals<T>& M, T cq, T c_g2) {
     PairTerms<T> o;
     o.A0 = I.A0 + M.A0;
@@ -417,35 +463,38 @@ __device__ __forceinline__ PairTerms<T> pair_terms(const NodeVals<T>& I, const N
     // mean and the close density branch
     const T rsum = I.rho + M.rho;
     const T bsum = I.b + M.b;
-    const T dlr = M.lr - I.lr;
-    const T dlb = M.lb - I.lb;
     const T cqr = cq * rsum;
     T crl, inv_bsum, inv_bln;
-    if constexpr (std::is_same<T, float>::value || std::is_same<T, p2>::value) {
-        // FP32: per-lane selects (the vote of the FP64 branch was measured
-        // slower for this issue-bound kernel: 0.215 -> 0.237 ms on the N = 7
-        // channel), series in f = (a+ - a-)/(a+ + a-) from one reciprocal
+    constexpr bool FP32 = std::is_same<T, float>::value || std::is_same<T, p2>::value;
+    static_assert(FP32 || !NARROW, "the polynomial log means are FP32 only");
+    if constexpr (FP32) {
+        // With f = (a+ - a-)/(a+ + a-) and u = f^2,
+        //   {{rho}}_log = rsum f/(2 atanh f),  1/{{b2}}_log = (2 atanh(f)/f)/bsum,
+        // each ratio a degree-4 polynomial in u (relative error below 3e-8
+        // for u <= kLogMeanPolyU = 0.16, values within a factor 2.33).  No
+        // logarithms: the whole pair costs two reciprocals.
         const T drho = M.rho - I.rho;
-        const auto cr = Num<T>::close(dlr);
-        const T rr = Num<T>::rcp(sel(cr, rsum, dlr));
-        const T tr = drho * rr;  // close: f = drho/rsum ; far: the log mean
-        const T ur = tr * tr;
-        // {{rho}} f/atanh(f) = (rsum/2)(1 - u/3 - 4u^2/45 - 44u^3/945 - ...); |f| < 0.1
-        // (u < 0.01), so the u^3 term (below 5e-8 relative) is left out
-        const T polr = fma(ur, fma(ur, T(-2.0 / 45.0), T(-1.0 / 6.0)), T(0.5));
-        crl = sel(cr, cqr * polr, cq * tr);
-
-        // 1/(b2+ + b2-) and the inverse log mean from one reciprocal
+        const T fr_ = drho * Num<T>::rcp(rsum);
+        const T ur = fr_ * fr_;
+        crl = cqr * poly4<0>(ur);
+        inv_bsum = Num<T>::rcp(bsum);
         const T db = M.b - I.b;
-        const auto cb = Num<T>::close(dlb);
-        const T rb = Num<T>::rcp(sel(cb, bsum, db * bsum));
-        inv_bsum = sel(cb, rb, db * rb);
         const T fb = db * inv_bsum;
         const T ub = fb * fb;
-        // 1/(2{{b}}_log) = (1/bsum2)(2 + 2u/3 + 2u^2/5 + 2u^3/7 + ...), f = db/bsum;
-        // the u^3 term is below 1.5e-7 relative for u < 0.01 and left out
-        const T polb = fma(ub, fma(ub, T(2.0 / 5.0), T(2.0 / 3.0)), T(2.0));
-        inv_bln = sel(cb, inv_bsum * polb, dlb * (bsum * rb));
+        inv_bln = inv_bsum * poly4<1>(ub);
+        if constexpr (!NARROW) {
+            // A CTA with a wider spread: pairs beyond the polynomials' range
+            // take the logarithm of the ratio x = a_m/a_i of their two values
+            // (1/rho_i is the same for every offset of the line, so it is
+            // hoisted; 1/b2_i = (1/b_i)/2 is a node value), selected per lane:
+            //   {{rho}}_log = drho log2(e)/lg2(x_rho),  1/{{b2}}_log = ln2 lg2(x_b)/db.
+            // There |lg2 x| > 1.2, so the absolute error of the hardware
+            // lg2 (2^-22) stays near FP32 rounding in relative terms.
+            const T lr = Num<T>::lg2(M.rho * Num<T>::rcp(I.rho));
+            crl = sel(Num<T>::above(ur, kLogMeanPolyU), (cq * drho) * (T(kLog2E) * Num<T>::rcp(lr)), crl);
+            const T lb = Num<T>::lg2(M.b * (T(0.5) * I.ib));
+            inv_bln = sel(Num<T>::above(ub, kLogMeanPolyU), (T(kLn2F) * lb) * Num<T>::rcp(db), inv_bln);
+        }
     } else {
         // Log means from the per-node logarithms: far, (a+ - a-)/(ln a+ - ln a-);
         // close (|d| < 0.02, d = ln a+ - ln a-), with x = d/2,
@@ -454,6 +503,8 @@ __device__ __forceinline__ PairTerms<T> pair_terms(const NodeVals<T>& I, const N
         // error only enters multiplied by d.  A warp vote skips the branch no
         // lane of the warp needs; a mixed warp evaluates both and selects.
         // Each lane computes the same formula either way.
+        const T dlr = M.lr - I.lr;
+        const T dlb = M.lb - I.lb;
         const auto cr = Num<T>::close(dlr);
         const auto cb = Num<T>::close(dlb);
         const unsigned mask = __activemask();
@@ -510,10 +561,10 @@ __device__ __forceinline__ PairTerms<T> pair_terms(const NodeVals<T>& I, const N
 // returned with the opposite sign (the receiver subtracts them), which saves
 // two negations per pair.  Both shares still need the 1/w scaling of their
 // own node.
-template <typename T>
+template <typename T, bool NARROW = false>
 __device__ __forceinline__ void pair_flux(const NodeVals<T>& I, const NodeVals<T>& M, T cq, T c_g2, T& o0, T& o1,
                                           T& o2, T& o3, T& o4, T& t0, T& t1, T& t2, T& t3, T& t4) {
-    const PairTerms<T> p = pair_terms<T>(I, M, cq, c_g2);
+    const PairTerms<T> p = pair_terms<T, NARROW>(I, M, cq, c_g2);
     o0 += p.fr;
     o1 = fma(p.A0, p.Pi, fma(p.fr, p.s1, o1));
     o2 = fma(p.A1, p.Pi, fma(p.fr, p.s2, o2));
@@ -659,7 +710,7 @@ __host__ __device__ __forceinline__ bool lane_line(int vwarp, int lane, int e_co
 // (to out; as a fused Runge-Kutta stage update; with the faces, to out).  Offsets
 // d = 1..NEAR; the antipodal offset Nq/2 of even Nq is left to
 // antipodal_phase.
-template <typename T, typename C, int N, int FINAL>
+template <typename T, typename C, int N, int FINAL, bool NARROW = false>
 __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count,
                                                 long long node0, const C (&cq)[Shape<N>::H], C iw, C c_g,
                                                 int vwarp, int R) {
@@ -711,7 +762,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
             acc4 -= rfE;
         } else {
             C t0, t1, t2, t3, t4;
-            pair_flux<C>(I, M, cqd, c_g, acc0, acc1, acc2, acc3, acc4, t0, t1, t2, t3, t4);
+            pair_flux<C, NARROW>(I, M, cqd, c_g, acc0, acc1, acc2, acc3, acc4, t0, t1, t2, t3, t4);
             // In-phase antipodal offset (when not split off): both nodes evaluate
             // the pair and keep their own share -- Fig. 1(b)'s two weight-1/2
             // evaluations summed per node.
@@ -745,7 +796,7 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
             const NodeVals<p2> M = pack_vals(load_node<N>(sm, checked(SL::at(el, ma, mb, mc), FS, a.status), R),
                                              load_node<N>(sm, checked(SL::at(el, na, nb, nc), FS, a.status), R));
             p2 t0, t1, t2, t3, t4;
-            pair_flux<p2>(I2, M, p2(cq[d - 1], cq[d]), cg2, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
+            pair_flux<p2, NARROW>(I2, M, p2(cq[d - 1], cq[d]), cg2, o0, o1, o2, o3, o4, t0, t1, t2, t3, t4);
             // partner shares: half x to the lane at p + d, half y to p + d + 1
             // (none for the in-phase antipodal offset of even Nq); when both
             // halves are received they are added to the packed accumulators
@@ -837,14 +888,14 @@ struct Launch {
             : 1;
 };
 
-template <typename T, typename C, int N, int R, int FINAL>
+template <typename T, typename C, int N, int R, int FINAL, bool NARROW>
 __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count,
                                                 long long node0, const C (&cq)[Shape<N>::H], C iw, C c_g) {
     using LA = Launch<N, C>;
     const int warp = threadIdx.x >> 5;
 #pragma unroll 1
     for (int rep = 0; rep < LA::REPS; ++rep)
-        direction_lines<T, C, N, FINAL>(a, sm, e_count, node0, cq, iw, c_g, warp + rep * LA::WARPS, R);
+        direction_lines<T, C, N, FINAL, NARROW>(a, sm, e_count, node0, cq, iw, c_g, warp + rep * LA::WARPS, R);
 }
 
 // Pair k of the antipodal pass: element el, line ell, lower position p
@@ -974,6 +1025,33 @@ __device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict
     }
 }
 
+// The direction phases of a CTA whose values spread wider than kNarrowRatio
+// (FP32), kept out of line so that the kernel's own code and registers are
+// those of the polynomial path.  Measured on GB300 at N = 7 (4.2e6 nodes):
+// with both forms inline the polynomial CTAs ran 11 % slower than a kernel
+// holding the polynomial form alone, and the whole launch was no faster than
+// per-pair selects between series and per-node logarithms; out of line they
+// are 2 % slower than that kernel, and the launch 6-9 % faster.
+template <typename T, typename C, int N, int MODE>
+__device__ __noinline__ void wide_phases(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count, long long node0) {
+    using S = Shape<N>;
+    constexpr int NQ = S::NQ;
+    using CV = Conv<T, C>;
+    static_assert(!SplitAntipodal<C>::value, "no antipodal pass");
+    const int lane = threadIdx.x & 31;
+    const int p = lane - (lane / NQ) * NQ;
+    C cq[S::H];
+#pragma unroll
+    for (int d = 1; d <= S::H; ++d) cq[d - 1] = CV::in(T(0.5) * a.ops.Q2[p * NQ + wrap_pos<NQ>(p, d)]);
+    const C iw = CV::in(a.ops.invw[p]);
+    const C c_g = CV::in(T(2) * a.c_g);
+    direction_phase<T, C, N, 1, 0, false>(a, sm, e_count, node0, cq, iw, c_g);
+    __syncthreads();
+    direction_phase<T, C, N, 2, 0, false>(a, sm, e_count, node0, cq, iw, c_g);
+    __syncthreads();
+    direction_phase<T, C, N, 0, MODE + 1, false>(a, sm, e_count, node0, cq, iw, c_g);
+}
+
 // MODE (store_node): 0 volume to out, 1 fused Runge-Kutta stage, 2 (FP32)
 // volume + faces to out; separate instantiations, so that the plain kernel's
 // code and registers are those of a store to out.
@@ -1013,6 +1091,10 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     using P = typename std::conditional<IsFF<C>::value, ff, T>::type;
     using PV = Conv<T, P>;
     bool bad = false;
+    // NarrowCheck: bit patterns of the smallest and largest density and b2
+    // of this thread's nodes (for positive floats the unsigned order of the
+    // bits is the order of the values)
+    unsigned r_lo = 0xffffffffu, r_hi = 0u, b_lo = 0xffffffffu, b_hi = 0u;
     // FP32 fused stage: the neighbour trace of this thread's first face slot
     // is requested before the element's own planes, so that the latencies of
     // the two sets of loads overlap; it is written to the face buffer after
@@ -1103,8 +1185,18 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         sm[F_U3 * FS + sl] = v3;
         sm[F_B * FS + sl] = b2;
         sm[F_INVB * FS + sl] = ib;
-        sm[F_LNRHO * FS + sl] = Num<P>::log_(rho);
-        sm[F_LNB * FS + sl] = Num<P>::log_(b2);
+        if constexpr (NarrowCheck<C>::value) {
+            // no per-node logarithms: the range of the CTA's values instead
+            if (real) {
+                r_lo = min(r_lo, __float_as_uint(rho));
+                r_hi = max(r_hi, __float_as_uint(rho));
+                b_lo = min(b_lo, __float_as_uint(b2));
+                b_hi = max(b_hi, __float_as_uint(b2));
+            }
+        } else {
+            sm[F_LNRHO * FS + sl] = Num<P>::log_(rho);
+            sm[F_LNB * FS + sl] = Num<P>::log_(b2);
+        }
         sm[F_PHI * FS + sl] = P(0.125) * phi;
         sm[F_H * FS + sl] = h;
 #pragma unroll
@@ -1170,6 +1262,22 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         }
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(a.status, 1u);
+    constexpr int WARPS = Launch<N, C>::THREADS / 32;
+    static_assert(WARPS <= 32, "one range entry per lane");
+    __shared__ unsigned s_range[NarrowCheck<C>::value ? 4 : 1][32];
+    if constexpr (NarrowCheck<C>::value) {
+        r_lo = __reduce_min_sync(0xffffffffu, r_lo);
+        r_hi = __reduce_max_sync(0xffffffffu, r_hi);
+        b_lo = __reduce_min_sync(0xffffffffu, b_lo);
+        b_hi = __reduce_max_sync(0xffffffffu, b_hi);
+        if ((threadIdx.x & 31) == 0) {
+            const int w = threadIdx.x >> 5;
+            s_range[0][w] = r_lo;
+            s_range[1][w] = r_hi;
+            s_range[2][w] = b_lo;
+            s_range[3][w] = b_hi;
+        }
+    }
 
     // lane constants: Q_{p,p+d} for every offset, 1/w_p and 1/(gamma - 1)
     const int lane = threadIdx.x & 31;
@@ -1180,6 +1288,21 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     const C iw = CV::in(a.ops.invw[p]);
     const C c_g = CV::in(T(2) * a.c_g);  // 1/(gamma - 1)
     __syncthreads();
+
+    // NarrowCheck: every warp reduces the CTA's ranges from the warps'
+    // entries, so all take the same decision.  A non-positive, infinite or
+    // NaN value (bits at or above those of +inf) makes the CTA wide.
+    bool narrow = false;
+    if constexpr (NarrowCheck<C>::value) {
+        const bool have = lane < WARPS;
+        const unsigned rl = __reduce_min_sync(0xffffffffu, have ? s_range[0][lane] : 0xffffffffu);
+        const unsigned rh = __reduce_max_sync(0xffffffffu, have ? s_range[1][lane] : 0u);
+        const unsigned bl = __reduce_min_sync(0xffffffffu, have ? s_range[2][lane] : 0xffffffffu);
+        const unsigned bh = __reduce_max_sync(0xffffffffu, have ? s_range[3][lane] : 0u);
+        narrow = rh < 0x7f800000u && bh < 0x7f800000u &&
+                 __uint_as_float(rh) <= kNarrowRatio * __uint_as_float(rl) &&
+                 __uint_as_float(bh) <= kNarrowRatio * __uint_as_float(bl);
+    }
 
     if constexpr (IsFF<C>::value) {
         // Float-float: one pair evaluation is ~850 instructions, so the
@@ -1216,19 +1339,30 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         }
     } else {
         if constexpr (FaceMode<C, MODE>::value) face_phase<T, C, N>(a, sm, nbr, e_count);
-        direction_phase<T, C, N, 1, 0>(a, sm, e_count, node0, cq, iw, c_g);
-        __syncthreads();
-        direction_phase<T, C, N, 2, 0>(a, sm, e_count, node0, cq, iw, c_g);
-        __syncthreads();
-        if constexpr (S::EVEN && SplitAntipodal<C>::value) {
-            antipodal_phase<T, C, N>(a, sm, e_count, c_g, 1);
+        auto phases = [&](auto narrow_tag) {
+            constexpr bool NW = decltype(narrow_tag)::value;
+            direction_phase<T, C, N, 1, 0, NW>(a, sm, e_count, node0, cq, iw, c_g);
             __syncthreads();
-            antipodal_phase<T, C, N>(a, sm, e_count, c_g, 2);
+            direction_phase<T, C, N, 2, 0, NW>(a, sm, e_count, node0, cq, iw, c_g);
             __syncthreads();
-            antipodal_phase<T, C, N>(a, sm, e_count, c_g, 0);
-            __syncthreads();
+            if constexpr (S::EVEN && SplitAntipodal<C>::value) {
+                antipodal_phase<T, C, N>(a, sm, e_count, c_g, 1);
+                __syncthreads();
+                antipodal_phase<T, C, N>(a, sm, e_count, c_g, 2);
+                __syncthreads();
+                antipodal_phase<T, C, N>(a, sm, e_count, c_g, 0);
+                __syncthreads();
+            }
+            direction_phase<T, C, N, 0, MODE + 1, NW>(a, sm, e_count, node0, cq, iw, c_g);
+        };
+        // a CTA-uniform branch: the polynomial form inline, the wide one out
+        // of line
+        if constexpr (NarrowCheck<C>::value) {
+            if (narrow) phases(std::true_type{});
+            else wide_phases<T, C, N, MODE>(a, sm, e_count, node0);
+        } else {
+            phases(std::false_type{});
         }
-        direction_phase<T, C, N, 0, MODE + 1>(a, sm, e_count, node0, cq, iw, c_g);
     }
 }
 

@@ -75,6 +75,45 @@ def test_wide_density_ratios(N, precision):
     assert e.max() < hz.TOL[precision], e
 
 
+def _element_ratio_state(cfg, g, lo, hi):
+    """The generated state with each element's density multiplied by
+    r_e^(cos(pi a/N)/2), a the node's xi index and r_e running from lo to hi
+    over the elements (velocity and pressure kept, so 2b = rho/p stretches
+    alike): within element e the stretch spans a factor r_e."""
+    g = {k: v.clone() for k, v in g.items()}
+    q = g["q"].double()
+    rho = q[0]
+    u = q[1:4] / rho
+    phi = g["phi"].double()
+    p = 0.4 * (q[4] - 0.5 * rho * (u * u).sum(0) - rho * phi)
+    nq = cfg.N + 1
+    node = torch.arange(cfg.n)
+    e = node // nq ** 3
+    a = (node % nq).double()
+    r = lo + (hi - lo) * e.double() / max(1, cfg.K - 1)
+    s = torch.exp(0.5 * torch.log(r) * torch.cos(np.pi * a / cfg.N))
+    rho2 = rho * s
+    g["q"] = torch.stack([rho2, rho2 * u[0], rho2 * u[1], rho2 * u[2],
+                          p / 0.4 + 0.5 * rho2 * (u * u).sum(0) + rho2 * phi])
+    return g
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 7])
+def test_fp32_log_mean_forms_at_the_switch(N):
+    """FP32 CTAs whose densities and values of b lie within a factor 2.25 use
+    the polynomial log means for every pair; wider ones select per pair
+    between the polynomials and the logarithm of the pair's ratio.  Elements
+    stretched by factors from 1.9 to 2.7 put CTAs on both sides of the
+    switch, and pairs on both sides of the polynomials' range."""
+    cfg = wl.small_config(N, K=(4, 3, 2), warp=True, precision="fp32")
+    g = _element_ratio_state(cfg, wl.generate(cfg), 1.9, 2.7)
+    got, op, _ = hz.run_gpu(cfg, g)
+    assert op.status() == 0
+    ref, scale = hz.run_oracle(cfg, g)
+    e, _ = hz.errors(got, ref, scale)
+    assert e.max() < hz.TOL["fp32"], e
+
+
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8])
 @pytest.mark.parametrize("precision", PRECISIONS)
 def test_skew_form(N, precision):
