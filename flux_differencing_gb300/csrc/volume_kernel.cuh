@@ -432,6 +432,9 @@ struct PairTerms {
     T fr, fE, Pi, Pm, s1, s2, s3, A0, A1, A2;
 };
 
+__device__ __forceinline__ bool any_of(bool c) { return c; }
+__device__ __forceinline__ bool any_of(m2 c) { return c.x || c.y; }
+
 // Horner evaluation of the degree-4 polynomial of table W (0: kLogMeanRatio,
 // 1: kInvLogMeanRatio) at u.
 template <int W, typename T>
@@ -490,10 +493,16 @@ __device__ __forceinline__ PairTerms<T> pair_terms(const NodeVals<T>& I, const N
             //   {{rho}}_log = drho log2(e)/lg2(x_rho),  1/{{b2}}_log = ln2 lg2(x_b)/db.
             // There |lg2 x| > 1.2, so the absolute error of the hardware
             // lg2 (2^-22) stays near FP32 rounding in relative terms.
-            const T lr = Num<T>::lg2(M.rho * Num<T>::rcp(I.rho));
-            crl = sel(Num<T>::above(ur, kLogMeanPolyU), (cq * drho) * (T(kLog2E) * Num<T>::rcp(lr)), crl);
-            const T lb = Num<T>::lg2(M.b * (T(0.5) * I.ib));
-            inv_bln = sel(Num<T>::above(ub, kLogMeanPolyU), (T(kLn2F) * lb) * Num<T>::rcp(db), inv_bln);
+            // A warp vote skips them where no lane of the warp needs them
+            // (lines along which the values vary little).
+            const auto far_r = Num<T>::above(ur, kLogMeanPolyU);
+            const auto far_b = Num<T>::above(ub, kLogMeanPolyU);
+            if (__any_sync(__activemask(), any_of(far_r) || any_of(far_b))) {
+                const T lr = Num<T>::lg2(M.rho * Num<T>::rcp(I.rho));
+                crl = sel(far_r, (cq * drho) * (T(kLog2E) * Num<T>::rcp(lr)), crl);
+                const T lb = Num<T>::lg2(M.b * (T(0.5) * I.ib));
+                inv_bln = sel(far_b, (T(kLn2F) * lb) * Num<T>::rcp(db), inv_bln);
+            }
         }
     } else {
         // Log means from the per-node logarithms: far, (a+ - a-)/(ln a+ - ln a-);

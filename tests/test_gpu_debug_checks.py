@@ -84,3 +84,32 @@ def test_debug_fused_stages(cuda_ok, N, precision):
         assert not (st & fd.ESDG_STATUS_INDEX), (bc, st)
         assert torch.isfinite(q).all()
         op.close()
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 7])
+def test_debug_fp32_both_log_mean_paths(cuda_ok, N):
+    """FP32 CTAs on both sides of the log-mean switch (elements stretched by
+    factors from 1.9 to 2.7), so the out-of-line wide phases run with the
+    index checks too; plain volume, volume + faces and the fused stage."""
+    from tests.test_gpu_parity import _element_ratio_state
+    cfg = wl.small_config(N, K=(4, 3, 2), warp=True, precision="fp32")
+    gh = _element_ratio_state(cfg, wl.generate(cfg), 1.9, 2.7)
+    g = hz.to_device(gh)
+    ref, scale = hz.run_oracle(cfg, gh)
+    op = _op(cfg, "fp32", (0, 1, 1))
+    J = torch.empty(cfg.n, dtype=op.dtype, device="cuda")
+    Ja = op.set_geometry(g["x"].contiguous(), g["y"].contiguous(), g["z"].contiguous(), J_out=J)
+    q = g["q"].to(op.dtype).contiguous()
+    phi = g["phi"].to(op.dtype).contiguous()
+    out = torch.full((5, cfg.n), float("nan"), dtype=op.dtype, device="cuda")
+    op.volume_rhs(q, Ja, phi, out=out)
+    assert not (op.status() & fd.ESDG_STATUS_INDEX), op.status()
+    e, _ = hz.errors(out.double().cpu().numpy(), ref, scale)
+    assert e.max() < hz.TOL["fp32"], e
+    r = op.rhs(q, Ja, phi)
+    dq = torch.zeros_like(q)
+    rhs = torch.zeros_like(q)
+    op.lsrk_step(q, dq, rhs, Ja, phi, J, 1e-4)
+    assert not (op.status() & fd.ESDG_STATUS_INDEX), op.status()
+    assert torch.isfinite(r).all() and torch.isfinite(q).all()
+    op.close()
