@@ -14,8 +14,9 @@
 //  * One CTA handles EPB whole elements.  A load phase reads the 15 input
 //    planes with coalesced loads straight into registers and writes per-node
 //    derived quantities to shared memory: u = m/rho, b = rho/(2p), 1/b,
-//    log rho, log b, h = phi/2 - |u|^2/4 (Sec. 4.1: primitives and logarithms
-//    once per node, not per pair), plus phi and the metric terms.  The same
+//    log rho, log b (FP64 and float-float), h = phi/2 - |u|^2/4 (Sec. 4.1:
+//    primitives and logarithms once per node, not per pair), plus phi and the
+//    metric terms.  The same
 //    phase adds the diagonal pairs m == i of the 2D form, which only exist at
 //    element-face nodes, for all three directions at once.
 //  * Three direction phases (eta, zeta, then xi).  In each, every line's Nq
@@ -39,16 +40,16 @@
 //    every direction phase are free of bank conflicts where possible.
 //  * The mass flux is {{rho}}_log {{u}}.n, the energy flux the entropy-
 //    conserving completion; both are formed directly from the contravariant
-//    direction vector, never as a 3x5 flux matrix (Sec. 4.1).  Log means use
-//    the per-node logarithms, switching to a series when the two logarithms
-//    are close -- in FP64 and float-float a series in the difference of the
-//    logarithms itself (no reciprocal), in FP32 one in
-//    ((a+ - a-)/(a+ + a-))^2 -- and 1/{{b}}_log is computed directly
-//    (Sec. 4.1).  The closeness test runs on the integer pipe; in FP64 and
-//    float-float a warp vote skips the branch no lane needs, a mixed warp
-//    (and FP32 always) evaluates both and selects per lane.  The per-node
-//    values are stored pre-scaled (u/2, 2b, phi/8) so that no factor of two
-//    is applied per pair.
+//    direction vector, never as a 3x5 flux matrix (Sec. 4.1).  FP64 and
+//    float-float log means use the per-node logarithms, switching to a series
+//    in the difference of the logarithms (no reciprocal) when the two are
+//    close, and 1/{{b}}_log is computed directly (Sec. 4.1).  The closeness
+//    test runs on the integer pipe; a warp vote skips the branch no lane
+//    needs, a mixed warp evaluates both and selects per lane.  FP32 forms
+//    the log means from polynomials in ((a+ - a-)/(a+ + a-))^2 where the
+//    CTA's values lie within a factor kNarrowRatio, without logarithms
+//    (NarrowCheck).  The per-node values are stored pre-scaled (u/2, 2b,
+//    phi/8) so that no factor of two is applied per pair.
 //  * FP32 at N = 3..8 evaluates two offsets per instruction in packed
 //    float2 registers (issue-bound kernel; PackPairs).
 //  * Further instantiations (MODE) change the final store: a Runge-Kutta
@@ -1047,8 +1048,9 @@ __device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict
 // those of the polynomial path.  Measured on GB300 at N = 7 (4.2e6 nodes):
 // with both forms inline the polynomial CTAs ran 11 % slower than a kernel
 // holding the polynomial form alone, and the whole launch was no faster than
-// per-pair selects between series and per-node logarithms; out of line they
-// are 2 % slower than that kernel, and the launch 6-9 % faster.
+// per-pair selects between series and per-node logarithms; out of line (with
+// the warp vote around the ratio logarithms) they run as fast as in that
+// kernel, and the launch is 9 % faster.
 template <typename T, typename C, int N, int MODE>
 __device__ __noinline__ void wide_phases(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count, long long node0) {
     using S = Shape<N>;
