@@ -81,11 +81,13 @@ __device__ __forceinline__ void add_out(const SurfaceArgs<T>& a, long long g, co
 // Float-float needs ~127 registers unbounded (two CTAs per SM) and is bound by
 // latency there; a bound of three CTAs per SM (80 registers, a 228-byte
 // spill) measured 0.44 -> 0.405 ms per call on the N = 7 channel, four CTAs
-// (64 registers) no better.  The FP32 kernel (59 registers) was slower when
-// bounded to six CTAs per SM (0.143 -> 0.156 ms), so it stays unbounded.
+// (64 registers) no better.  FP32, bound by DRAM line traffic: four CTAs per
+// SM (64 registers, no spill; unbounded it takes 69-72 and runs three) keep
+// more loads in flight, 0.155 -> 0.142 ms per call; five (48 registers)
+// spill.
 template <typename C>
 struct SurfaceOccupancy {
-    static constexpr int value = std::is_same<C, ff>::value ? 3 : 1;
+    static constexpr int value = std::is_same<C, ff>::value ? 3 : std::is_same<C, float>::value ? 4 : 1;
 };
 
 template <typename T, typename C, int N, int DIR>
