@@ -33,11 +33,12 @@ struct Fail {
 
 // Lines dealt to the lanes of the direction phases: every line of every
 // element of a CTA holding e_count elements visited exactly once, at every
-// position, over the virtual warps warp + rep WARPS.
-template <int N, typename C>
+// position, over the virtual warps warp + rep WARPS (for each CTA shape:
+// FACES, the FP32 kernels with the face machinery).
+template <int N, typename C, bool FACES>
 bool check_lanes(Fail& f) {
     using S = Shape<N>;
-    using LA = esdg::Launch<N, C>;
+    using LA = esdg::Launch<N, C, FACES>;
     if (LA::WARPS * LA::REPS * S::LPW < S::LINES) return f.set("too few lane lines", LA::WARPS, LA::REPS);
     for (int e_count = 1; e_count <= S::EPB; ++e_count) {
         std::vector<int> seen(S::LINES * S::NQ, 0);
@@ -96,7 +97,9 @@ bool check_element(Fail& f) {
         esdg::line_node<N>(0, ell + 1, 0, a1, b1, c1);
         if (b1 + NQ * c1 != b0 + NQ * c0 + 1) return f.set("xi lines not in row order", ell);
     }
-    if (!check_lanes<N, double>(f) || !check_lanes<N, float>(f) || !check_lanes<N, esdg::ff>(f)) return false;
+    if (!check_lanes<N, double, false>(f) || !check_lanes<N, float, false>(f) || !check_lanes<N, float, true>(f) ||
+        !check_lanes<N, esdg::ff, false>(f))
+        return false;
     // load order of the FP64 kernel: a permutation, face nodes first
     {
         std::vector<int> seen(NP3, 0);

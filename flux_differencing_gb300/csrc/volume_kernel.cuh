@@ -873,43 +873,50 @@ __device__ __forceinline__ void direction_lines(const VolumeArgs<T>& a, C* __res
 //    (PackPairs) needs more than the 64 registers a 512-thread CTA pair
 //    leaves (N = 6: 4.34 -> 3.98 ms on the order sweep, N = 3: 1.82 ->
 //    1.73); at N = 8 one element's 81 lines would otherwise also need an
-//    864-thread CTA.  At N = 7 one set is faster (3.19 against 3.28 ms).
+//    864-thread CTA.  At N = 7, two sets in 256-thread CTAs, four per SM at
+//    64 registers: 0.1935 -> 0.1806 ms on the channel, 2.757 -> 2.565 ms on
+//    the order sweep, against one set in two 512-thread CTAs per SM.  The
+//    kernels that carry the face machinery (FACES: the FP32 fused stage and
+//    volume + faces) keep one set in 512-thread CTAs: their face buffer
+//    leaves room for three CTAs per SM only, and the face phase's 384 slots
+//    per element would take two rounds of 256 threads (volume + faces
+//    0.261 -> 0.279 ms with the smaller CTA).
 //  * FP64 rechecked with the current kernel: two sets at N = 4, 5, 6 gave
 //    61.8 -> 62.7, 75.5 -> 75.4 and 91.7 -> 94.4 ms, so only N = 7 uses them;
 //    but two CTAs of one set per SM (MIN_BLOCKS = 2: 72, 64 and 72 registers
 //    with 24-128 byte spills) are faster there: 61.8 -> 60.0, 75.5 -> 74.0,
 //    91.7 -> 90.2 ms.  Four CTAs per SM at N = 2, 3 (56 and 64 registers)
 //    were no faster (34.8 -> 35.3, 44.3 -> 44.3 ms).
-template <int N, typename C>
+template <int N, typename C, bool FACES = false>
 struct Launch {
     using S = Shape<N>;
     static constexpr int VWARPS = (S::LINES + S::LPW - 1) / S::LPW;  // warps' worth of lines
     static constexpr bool FP64 = sizeof(C) == 8;
     static constexpr int REPS =
-        IsFF<C>::value ? 2 : FP64 ? (N == 7 ? 2 : 1) : ((N >= 3 && N != 7) ? 2 : 1);
+        IsFF<C>::value ? 2 : FP64 ? (N == 7 ? 2 : 1) : ((N >= 3 && !(N == 7 && FACES)) ? 2 : 1);
     static constexpr int WARPS = (VWARPS + REPS - 1) / REPS;
     static constexpr int THREADS = WARPS * 32;
     static constexpr size_t SMEM = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
     static constexpr bool TWO_FIT = 2 * SMEM <= 227 * 1024;
-    // FP32 at N = 3..6: register bounds that keep one more CTA per SM than
+    // FP32 at N = 3..7: register bounds that keep one more CTA per SM than
     // the unbounded allocation (N = 3: 8 CTAs of 128 threads at 64
-    // registers; N = 4, 6: 4 of 224 at 72; N = 5: 4 of 256 at 64), without
+    // registers; N = 4, 6: 4 of 224 at 72; N = 5, 7: 4 of 256 at 64), without
     // spills in the plain kernel.  Order sweep (ms, about 6.4e7 nodes):
     // N = 3 1.522 -> 1.509, N = 4 2.846 -> 2.631, N = 5 3.163 -> 3.026,
     // N = 6 3.694 -> 3.315.
     static constexpr int MIN_BLOCKS =
         (sizeof(C) == 4 && N == 3) ? 8
-        : (sizeof(C) == 4 && (N == 4 || N == 5 || N == 6)) ? 4
+        : (sizeof(C) == 4 && (N == 4 || N == 5 || N == 6 || (N == 7 && !FACES))) ? 4
         : ((sizeof(C) == 4 && THREADS <= 512) || IsFF<C>::value || (FP64 && (REPS == 2 || (N >= 4 && N <= 6)))) &&
                   TWO_FIT
             ? 2
             : 1;
 };
 
-template <typename T, typename C, int N, int R, int FINAL, bool NARROW>
+template <typename T, typename C, int N, int R, int FINAL, bool NARROW, int MODE>
 __device__ __forceinline__ void direction_phase(const VolumeArgs<T>& a, C* __restrict__ sm, int e_count,
                                                 long long node0, const C (&cq)[Shape<N>::H], C iw, C c_g) {
-    using LA = Launch<N, C>;
+    using LA = Launch<N, C, FaceMode<C, MODE>::value>;
     const int warp = threadIdx.x >> 5;
 #pragma unroll 1
     for (int rep = 0; rep < LA::REPS; ++rep)
@@ -996,7 +1003,7 @@ __device__ __forceinline__ void face_phase(const VolumeArgs<T>& a, C* __restrict
     k.c_ac = a.sk.c_ac;
     k.c_en = a.sk.c_en;
     const bool perturbed = a.rho_ref != nullptr;
-    for (int s = threadIdx.x; s < e_count * FSL::PER_EL; s += Launch<N, C>::THREADS) {
+    for (int s = threadIdx.x; s < e_count * FSL::PER_EL; s += Launch<N, C, true>::THREADS) {
         int el, dir, side, i1, i2, na, nb, nc;
         FSL::decode(s, el, dir, side, i1, i2);
         FSL::node(dir, side ? N : 0, i1, i2, na, nb, nc);
@@ -1064,18 +1071,19 @@ __device__ __noinline__ void wide_phases(const VolumeArgs<T>& a, C* __restrict__
     for (int d = 1; d <= S::H; ++d) cq[d - 1] = CV::in(T(0.5) * a.ops.Q2[p * NQ + wrap_pos<NQ>(p, d)]);
     const C iw = CV::in(a.ops.invw[p]);
     const C c_g = CV::in(T(2) * a.c_g);
-    direction_phase<T, C, N, 1, 0, false>(a, sm, e_count, node0, cq, iw, c_g);
+    direction_phase<T, C, N, 1, 0, false, MODE>(a, sm, e_count, node0, cq, iw, c_g);
     __syncthreads();
-    direction_phase<T, C, N, 2, 0, false>(a, sm, e_count, node0, cq, iw, c_g);
+    direction_phase<T, C, N, 2, 0, false, MODE>(a, sm, e_count, node0, cq, iw, c_g);
     __syncthreads();
-    direction_phase<T, C, N, 0, MODE + 1, false>(a, sm, e_count, node0, cq, iw, c_g);
+    direction_phase<T, C, N, 0, MODE + 1, false, MODE>(a, sm, e_count, node0, cq, iw, c_g);
 }
 
 // MODE (store_node): 0 volume to out, 1 fused Runge-Kutta stage, 2 (FP32)
 // volume + faces to out; separate instantiations, so that the plain kernel's
 // code and registers are those of a store to out.
 template <typename T, int N, typename C, int MODE>
-__global__ void __launch_bounds__(Launch<N, C>::THREADS, Launch<N, C>::MIN_BLOCKS)
+__global__ void __launch_bounds__(Launch<N, C, FaceMode<C, MODE>::value>::THREADS,
+                                  Launch<N, C, FaceMode<C, MODE>::value>::MIN_BLOCKS)
 volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     using S = Shape<N>;
     using SL = Slots<N>;
@@ -1085,6 +1093,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     C* sm = reinterpret_cast<C*>(smem_raw);
     using CV = Conv<T, C>;
+    using LK = Launch<N, C, FaceMode<C, MODE>::value>;
     poison_shared(smem_raw, volume_smem_bytes<C, N, MODE>());  // debug builds only
 
     const long long e0 = a.e_begin + (long long)blockIdx.x * S::EPB;
@@ -1097,7 +1106,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
     long long* nbr = nullptr;
     if constexpr (FaceMode<C, MODE>::value) {
         nbr = reinterpret_cast<long long*>(smem_raw + volume_smem_nbr_offset<C, N, MODE>());
-        static_assert(6 * S::EPB <= Launch<N, C>::THREADS, "one neighbour entry per thread");
+        static_assert(6 * S::EPB <= LK::THREADS, "one neighbour entry per thread");
         const int t = threadIdx.x;
         if (t < 6 * e_count) nbr[t] = neighbour_element(a, e0 + t / 6, (t % 6) >> 1, t & 1);
         __syncthreads();
@@ -1143,7 +1152,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
             }
         }
     }
-    for (int t = threadIdx.x; t < S::NODES; t += Launch<N, C>::THREADS) {
+    for (int t = threadIdx.x; t < S::NODES; t += LK::THREADS) {
         const int el = t / NP3;
         const int nd = FaceFirst<C>::value ? face_first_node<N>(t - el * NP3) : t - el * NP3;
         const int na = nd % NQ, nb = (nd / NQ) % NQ, nc = nd / (NQ * NQ);
@@ -1263,7 +1272,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
 #pragma unroll
             for (int v = 0; v < TR; ++v) fb[v * CNT + threadIdx.x] = trace[v];
         }
-        for (int s = threadIdx.x + Launch<N, C>::THREADS; s < e_count * FSL::PER_EL; s += Launch<N, C>::THREADS) {
+        for (int s = threadIdx.x + LK::THREADS; s < e_count * FSL::PER_EL; s += LK::THREADS) {
             int el, dir, side, i1, i2;
             FSL::decode(s, el, dir, side, i1, i2);
             long long g;
@@ -1281,7 +1290,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         }
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(a.status, 1u);
-    constexpr int WARPS = Launch<N, C>::THREADS / 32;
+    constexpr int WARPS = LK::THREADS / 32;
     static_assert(WARPS <= 32, "one range entry per lane");
     __shared__ unsigned s_range[NarrowCheck<C>::value ? 4 : 1][32];
     if constexpr (NarrowCheck<C>::value) {
@@ -1360,9 +1369,9 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
         if constexpr (FaceMode<C, MODE>::value) face_phase<T, C, N>(a, sm, nbr, e_count);
         auto phases = [&](auto narrow_tag) {
             constexpr bool NW = decltype(narrow_tag)::value;
-            direction_phase<T, C, N, 1, 0, NW>(a, sm, e_count, node0, cq, iw, c_g);
+            direction_phase<T, C, N, 1, 0, NW, MODE>(a, sm, e_count, node0, cq, iw, c_g);
             __syncthreads();
-            direction_phase<T, C, N, 2, 0, NW>(a, sm, e_count, node0, cq, iw, c_g);
+            direction_phase<T, C, N, 2, 0, NW, MODE>(a, sm, e_count, node0, cq, iw, c_g);
             __syncthreads();
             if constexpr (S::EVEN && SplitAntipodal<C>::value) {
                 antipodal_phase<T, C, N>(a, sm, e_count, c_g, 1);
@@ -1372,7 +1381,7 @@ volume_kernel(const __grid_constant__ VolumeArgs<T> a) {
                 antipodal_phase<T, C, N>(a, sm, e_count, c_g, 0);
                 __syncthreads();
             }
-            direction_phase<T, C, N, 0, MODE + 1, NW>(a, sm, e_count, node0, cq, iw, c_g);
+            direction_phase<T, C, N, 0, MODE + 1, NW, MODE>(a, sm, e_count, node0, cq, iw, c_g);
         };
         // a CTA-uniform branch: the polynomial form inline, the wide one out
         // of line
@@ -1399,7 +1408,7 @@ cudaError_t launch_volume_mode(const VolumeArgs<T>& a, cudaStream_t s) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const long long blocks = (K + S::EPB - 1) / S::EPB;
-    volume_kernel<T, N, C, MODE><<<(unsigned)blocks, Launch<N, C>::THREADS, smem, s>>>(a);
+    volume_kernel<T, N, C, MODE><<<(unsigned)blocks, Launch<N, C, FaceMode<C, MODE>::value>::THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 
