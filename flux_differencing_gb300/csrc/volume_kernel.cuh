@@ -898,14 +898,18 @@ struct Launch {
     static constexpr int THREADS = WARPS * 32;
     static constexpr size_t SMEM = sizeof(C) * (size_t)F_COUNT * Slots<N>::SIZE;
     static constexpr bool TWO_FIT = 2 * SMEM <= 227 * 1024;
-    // FP32 at N = 3..7: register bounds that keep one more CTA per SM than
-    // the unbounded allocation (N = 3: 8 CTAs of 128 threads at 64
-    // registers; N = 4, 6: 4 of 224 at 72; N = 5, 7: 4 of 256 at 64), without
-    // spills in the plain kernel.  Order sweep (ms, about 6.4e7 nodes):
-    // N = 3 1.522 -> 1.509, N = 4 2.846 -> 2.631, N = 5 3.163 -> 3.026,
-    // N = 6 3.694 -> 3.315.
+    // FP32 at N = 2..7: register bounds that keep more CTAs per SM than the
+    // unbounded allocation (N = 2: 5 CTAs of 288 threads at 40 registers;
+    // N = 3: 8 of 128 at 64; N = 4: 5 of 224 at 56; N = 6: 4 of 224 at 72;
+    // N = 5, 7: 4 of 256 at 64), without spills in the plain kernel.  Order
+    // sweep (ms, about 6.4e7 nodes): N = 2 1.902 -> 1.877, N = 3 1.522 ->
+    // 1.509, N = 4 2.846 -> 2.631 (4 CTAs) -> 2.571 (5), N = 5 3.163 -> 3.026,
+    // N = 6 3.694 -> 3.315; five CTAs at N = 5 and 6 were slower (3.11,
+    // 3.43).  The kernels with face work keep these bounds only where their
+    // CTA shape is the same.
     static constexpr int MIN_BLOCKS =
-        (sizeof(C) == 4 && N == 3) ? 8
+        (sizeof(C) == 4 && !FACES && (N == 2 || N == 4)) ? 5
+        : (sizeof(C) == 4 && N == 3) ? 8
         : (sizeof(C) == 4 && (N == 4 || N == 5 || N == 6 || (N == 7 && !FACES))) ? 4
         : ((sizeof(C) == 4 && THREADS <= 512) || IsFF<C>::value || (FP64 && (REPS == 2 || (N >= 4 && N <= 6)))) &&
                   TWO_FIT
