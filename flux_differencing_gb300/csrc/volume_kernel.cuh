@@ -905,12 +905,12 @@ struct Launch {
     // sweep (ms, about 6.4e7 nodes): N = 2 1.902 -> 1.877, N = 3 1.522 ->
     // 1.509, N = 4 2.846 -> 2.631 (4 CTAs) -> 2.571 (5), N = 5 3.163 -> 3.026,
     // N = 6 3.694 -> 3.315; five CTAs at N = 5 and 6 were slower (3.11,
-    // 3.43).  The kernels with face work keep these bounds only where their
-    // CTA shape is the same.
+    // 3.43).  The kernels with face work (whose face buffer takes more shared
+    // memory) keep the general rule below.
     static constexpr int MIN_BLOCKS =
         (sizeof(C) == 4 && !FACES && (N == 2 || N == 4)) ? 5
-        : (sizeof(C) == 4 && N == 3) ? 8
-        : (sizeof(C) == 4 && (N == 4 || N == 5 || N == 6 || (N == 7 && !FACES))) ? 4
+        : (sizeof(C) == 4 && !FACES && N == 3) ? 8
+        : (sizeof(C) == 4 && !FACES && (N == 5 || N == 6 || N == 7)) ? 4
         : ((sizeof(C) == 4 && THREADS <= 512) || IsFF<C>::value || (FP64 && (REPS == 2 || (N >= 4 && N <= 6)))) &&
                   TWO_FIT
             ? 2
