@@ -74,3 +74,13 @@ def test_log_mean_identity():
         assert abs((approx - exact) / exact) < 2e-7
         inv = mp.mpf(float(_horner32(c["kInvLogMeanRatio"], u))) / (a + cc)
         assert abs(inv * exact - 1) < 2e-7
+
+
+def test_committed_table_is_the_generator_output():
+    """logmean_poly.inc is exactly what gen_logmean_poly.py writes (about 40 s
+    of 40-digit Remez iterations)."""
+    import subprocess
+    import sys
+    gen = os.path.join(os.path.dirname(INC), "gen_logmean_poly.py")
+    out = subprocess.run([sys.executable, gen], capture_output=True, text=True, check=True).stdout
+    assert out == open(INC).read()
